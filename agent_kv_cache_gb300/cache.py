@@ -1,0 +1,122 @@
+"""Owner of the two device pools plus the cache handle (PyTorch = memory + streams)."""
+import numpy as np
+
+from . import abi
+
+
+class Cache:
+    """A cache over K/V pools allocated with torch on the current CUDA device.
+
+    Methods forward to the C ABI with the same names (without the ``akv_``
+    prefix); tensors are passed by device pointer.  The pools are exposed as
+    ``k_pool`` / ``v_pool`` shaped [phys_layers, max_pages, hkv, page, D].
+    """
+
+    def __init__(self, layers, hq, hkv, head_dim, page_size, dtype, max_pages, max_seqs,
+                 max_slots, rope_theta, phys_layers=0, stream=None):
+        import torch
+        self.torch = torch
+        self.cfg = abi.make_config(layers, hq, hkv, head_dim, page_size, dtype, max_pages,
+                                   max_seqs, max_slots, rope_theta, phys_layers)
+        self.layers, self.hq, self.hkv, self.d, self.page = layers, hq, hkv, head_dim, page_size
+        self.phys = phys_layers or layers
+        self.dtype = dtype
+        self.tdtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.pool_bytes = abi.akv_pool_bytes(self.cfg)
+        if self.pool_bytes == 0:
+            raise abi.AkvError(abi.AKV_EINVAL, "invalid configuration")
+        shape = (self.phys, max_pages, hkv, page_size, head_dim)
+        self.k_pool = torch.empty(shape, dtype=self.tdtype, device="cuda")
+        self.v_pool = torch.empty(shape, dtype=self.tdtype, device="cuda")
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self.handle = abi.akv_cache_create(self.cfg, self.k_pool.data_ptr(),
+                                           self.v_pool.data_ptr(), self.pool_bytes,
+                                           self.stream.cuda_stream)
+
+    def close(self):
+        if self.handle:
+            abi.akv_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- operations ---------------------------------------------------------
+    def seq_create(self):
+        return abi.akv_seq_create(self.handle)
+
+    def seq_fork(self, parent):
+        return abi.akv_seq_fork(self.handle, parent)
+
+    def seq_free(self, seq):
+        abi.akv_seq_free(self.handle, seq)
+
+    def append(self, seqs, n_tokens, k_raw, v, token_ids=None):
+        """k_raw, v: device tensors [layers, T, hkv, D] in the pool dtype."""
+        assert k_raw.is_contiguous() and v.is_contiguous()
+        abi.akv_append(self.handle, seqs, n_tokens, k_raw.data_ptr(), v.data_ptr(), token_ids)
+
+    def drop(self, seq, ranges):
+        abi.akv_drop(self.handle, seq, ranges)
+
+    def reposition(self, seqs):
+        abi.akv_reposition(self.handle, seqs)
+
+    def decode_attention(self, layer, q, seqs, out=None):
+        """q: device [n, hq, D] pool dtype; returns out [n, hq, D] fp32."""
+        torch = self.torch
+        if out is None:
+            out = torch.empty((len(seqs), self.hq, self.d), dtype=torch.float32, device="cuda")
+        assert q.is_contiguous() and out.is_contiguous()
+        abi.akv_decode_attention(self.handle, layer, q.data_ptr(), seqs, out.data_ptr())
+        return out
+
+    # -- introspection ------------------------------------------------------
+    def info(self, seq):
+        return abi.akv_seq_info(self.handle, seq)
+
+    def positions(self, seq):
+        return abi.akv_seq_positions(self.handle, seq, self.info(seq)["n_held"])
+
+    def keep_mask(self, seq):
+        return abi.akv_seq_keep_mask(self.handle, seq, self.info(seq)["n_held"]).astype(bool)
+
+    def logical(self, seq):
+        return abi.akv_seq_logical(self.handle, seq, self.info(seq)["n_held"])
+
+    def gather_map(self, seq):
+        return abi.akv_seq_gather_map(self.handle, seq)
+
+    def page_table(self, seq):
+        return abi.akv_seq_page_table(self.handle, seq)
+
+    def history_key(self, seq):
+        return abi.akv_history_key(self.handle, seq)
+
+    def refcount(self, page):
+        return abi.akv_page_refcount(self.handle, page)
+
+    def pool_stats(self):
+        return abi.akv_pool_stats(self.handle)
+
+    def sync_errors(self):
+        return abi.akv_sync_errors(self.handle)
+
+    def read_kv(self, seq, layer):
+        """Held tokens' stored K and V of one layer, [n_held, hkv, D] (host fp64).
+
+        Reads the pool through the device page table (test introspection).
+        """
+        torch = self.torch
+        n = self.info(seq)["n_held"]
+        pages, _ = self.page_table(seq)
+        slots = np.arange(n)
+        pid = torch.from_numpy(pages[slots // self.page].astype(np.int64)).cuda()
+        off = torch.from_numpy((slots % self.page).astype(np.int64)).cuda()
+        slab = layer % self.phys
+        k = self.k_pool[slab][pid, :, off]          # [n, hkv, D]
+        v = self.v_pool[slab][pid, :, off]
+        return (k.double().cpu().numpy(), v.double().cpu().numpy())

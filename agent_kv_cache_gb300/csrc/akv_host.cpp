@@ -1,0 +1,964 @@
+// Host side of the active-KV cache library: the C ABI of include/akv.h.
+//
+// The host owns page allocation (free list + reference counts), the
+// per-sequence bookkeeping (held slots, active slot intervals, the
+// slot -> logical-index runs, history key) and the launch plans.  Each call
+// (1) checks and plans without changing anything, (2) packs one descriptor
+// blob and copies it to the device through a pinned staging ring, (3)
+// commits the host state and (4) enqueues its kernels.  Nothing on the
+// append / drop / reposition / decode path waits for the GPU.
+//
+// Sources: "Cache Engineering for Agents" paper review, 3.3 (Eqs. 3-5), 3.4
+// (Eq. 6), 4.2.3 (position versions: a reposition by one request makes new
+// K/V, other requests keep the old version); "[Repo Review] AKV", 5.4
+// (OccurrenceState: reuse, borrow, or allocate-and-copy per occurrence;
+// copy-on-write when ownership passes to another branch) and 5.6 (dropping
+// is a visibility change; memory is reclaimed only when no one refers to it).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "akv.h"
+#include "akv_internal.h"
+
+using namespace akv;
+
+namespace {
+
+struct Interval { int64_t a, b; };        // half-open
+struct Run { int64_t slot0, log0, len; }; // slots [slot0, slot0+len) hold logical [log0, ...)
+
+constexpr int kStages = 32;
+constexpr int kMaxItems = 4096;            // decode work items per call
+
+// 128-bit key of an operation history: two independent 64-bit chains, each
+// step finished with the MurmurHash3 64-bit finaliser (Appleby).
+inline uint64_t fmix64(uint64_t k) {
+  k ^= k >> 33; k *= 0xff51afd7ed558ccdULL;
+  k ^= k >> 33; k *= 0xc4ceb9fe1a85ec53ULL;
+  k ^= k >> 33;
+  return k;
+}
+struct HKey {
+  uint64_t a = 0x6a09e667f3bcc908ULL, b = 0xbb67ae8584caa73bULL;
+  void absorb(uint64_t w) {
+    a = fmix64(a ^ (w + 0x9e3779b97f4a7c15ULL));
+    b = fmix64(b + w * 0xc2b2ae3d27d4eb4fULL + 0x165667b19e3779f9ULL) ^ (a >> 7);
+  }
+};
+constexpr uint64_t kRecAppend = 1, kRecDrop = 2, kRecRepos = 3;
+constexpr uint64_t kNoToken = 1ULL << 40;
+
+struct HostSeq {
+  int32_t dslot = -1;
+  int64_t n_logical = 0, n_slots = 0, n_alive = 0;
+  int32_t n_active_pages = 0;
+  std::vector<int32_t> pages;      // per slot page, -1 once released
+  std::vector<Interval> alive;     // active slots, sorted, disjoint, merged
+  std::vector<Run> runs;
+  int64_t gather_n = 0;
+  bool gather_identity = true;     // last reposition moved nothing
+  HKey key;
+};
+
+struct Stage { char* h = nullptr; char* d = nullptr; cudaEvent_t ev = nullptr; bool used = false; };
+
+struct Blob {
+  std::vector<char> b;
+  template <class T> size_t put(const T* p, size_t n) {
+    const size_t off = (b.size() + 15) & ~size_t(15);
+    b.resize(off + n * sizeof(T));
+    if (n) std::memcpy(b.data() + off, p, n * sizeof(T));
+    return off;
+  }
+};
+
+// ---- interval sets --------------------------------------------------------
+
+void iv_subtract(std::vector<Interval>& v, int64_t a, int64_t b, std::vector<Interval>* removed) {
+  if (a >= b) return;
+  std::vector<Interval> out;
+  out.reserve(v.size() + 1);
+  for (const Interval& iv : v) {
+    if (iv.b <= a || iv.a >= b) { out.push_back(iv); continue; }
+    if (iv.a < a) out.push_back({iv.a, a});
+    if (removed) removed->push_back({std::max(iv.a, a), std::min(iv.b, b)});
+    if (iv.b > b) out.push_back({b, iv.b});
+  }
+  v.swap(out);
+}
+
+bool iv_any(const std::vector<Interval>& v, int64_t a, int64_t b) {
+  auto it = std::upper_bound(v.begin(), v.end(), a,
+                             [](int64_t x, const Interval& iv) { return x < iv.b; });
+  return it != v.end() && it->a < b;
+}
+
+int32_t iv_count_pages(const std::vector<Interval>& v, int S) {
+  int64_t last = -1, count = 0;
+  for (const Interval& iv : v) {
+    int64_t k0 = iv.a / S;
+    const int64_t k1 = (iv.b - 1) / S;
+    if (k0 <= last) k0 = last + 1;
+    if (k0 <= k1) count += k1 - k0 + 1;
+    last = std::max(last, k1);
+  }
+  return (int32_t)count;
+}
+
+void logical_to_slots(const std::vector<Run>& runs, int64_t lb, int64_t le,
+                      std::vector<Interval>& out) {
+  auto it = std::upper_bound(runs.begin(), runs.end(), lb,
+                             [](int64_t x, const Run& r) { return x < r.log0 + r.len; });
+  for (; it != runs.end() && it->log0 < le; ++it) {
+    const int64_t a = std::max(lb, it->log0), b = std::min(le, it->log0 + it->len);
+    if (a < b) out.push_back({it->slot0 + (a - it->log0), it->slot0 + (b - it->log0)});
+  }
+}
+
+std::vector<Interval> merge(std::vector<Interval> v) {
+  std::sort(v.begin(), v.end(), [](const Interval& x, const Interval& y) { return x.a < y.a; });
+  std::vector<Interval> out;
+  for (const Interval& iv : v) {
+    if (iv.b <= iv.a) continue;
+    if (!out.empty() && iv.a <= out.back().b) out.back().b = std::max(out.back().b, iv.b);
+    else out.push_back(iv);
+  }
+  return out;
+}
+
+}  // namespace
+
+struct akv_cache {
+  akv_config cfg{};
+  Geom g{};
+  SeqArrays sa{};
+  cudaStream_t stream = nullptr;
+  float2* d_cs = nullptr;
+  float* d_part_acc = nullptr;
+  float2* d_part_ml = nullptr;
+  uint32_t* d_err = nullptr;
+  Stage stages[kStages];
+  size_t stage_bytes = 0;
+  int stage_next = 0;
+  // decode plan (device copy kept while the metadata epoch is unchanged)
+  char* d_plan = nullptr;
+  size_t plan_cap = 0;
+  uint64_t plan_epoch = ~0ULL;
+  std::vector<int64_t> plan_seqs;
+  int plan_items = 0;
+  bool plan_combine = false;
+  // host state
+  std::vector<int32_t> refcnt, free_pages;
+  std::unordered_map<int64_t, HostSeq> seqs;
+  std::vector<int32_t> free_dslots;
+  int64_t next_id = 1;
+  uint64_t epoch = 0;
+  std::string err;
+  uint32_t wait_limit = 1u << 22;
+  int sm_count = 148;
+};
+
+namespace {
+
+int fail(akv_cache* c, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (c) c->err = buf;
+  return code;
+}
+
+#define CK(call)                                                               \
+  do {                                                                         \
+    cudaError_t e_ = (call);                                                   \
+    if (e_ != cudaSuccess)                                                     \
+      return fail(c, AKV_ECUDA, "%s: %s", #call, cudaGetErrorString(e_));      \
+  } while (0)
+
+int check_config(const akv_config* cfg) {
+  if (!cfg) return AKV_EINVAL;
+  const int S = cfg->page_size;
+  const int G = cfg->hkv > 0 ? cfg->hq / cfg->hkv : 0;
+  if (cfg->layers < 1 || cfg->phys_layers < 0 || cfg->phys_layers > cfg->layers) return AKV_EINVAL;
+  if (cfg->hkv < 1 || cfg->hq < cfg->hkv || cfg->hq % cfg->hkv) return AKV_EINVAL;
+  if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return AKV_EINVAL;
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return AKV_EINVAL;
+  if (!(S == 1 || S == 2 || S == 4 || S == 8 || S == 16 || S == 32 || S == 64)) return AKV_EINVAL;
+  if (cfg->dtype != AKV_DTYPE_BF16 && cfg->dtype != AKV_DTYPE_FP32) return AKV_EINVAL;
+  if (cfg->max_pages < 1 || cfg->max_seqs < 1) return AKV_EINVAL;
+  if (cfg->max_slots < 1 || cfg->max_slots > (1 << 30)) return AKV_EINVAL;
+  if (!(cfg->rope_theta > 1.0)) return AKV_EINVAL;
+  return AKV_OK;
+}
+
+HostSeq* find(akv_cache* c, int64_t id) {
+  auto it = c->seqs.find(id);
+  return it == c->seqs.end() ? nullptr : &it->second;
+}
+
+void decref(akv_cache* c, int32_t p) {
+  if (p < 0) return;
+  if (--c->refcnt[p] == 0) c->free_pages.push_back(p);
+}
+
+// The next n page ids the allocator will hand out (without taking them).
+std::vector<int32_t> peek_pages(akv_cache* c, size_t n) {
+  std::vector<int32_t> out(n);
+  for (size_t i = 0; i < n; ++i) out[i] = c->free_pages[c->free_pages.size() - 1 - i];
+  return out;
+}
+void take_pages(akv_cache* c, size_t n) {
+  for (size_t i = 0; i < n; ++i) {
+    const int32_t p = c->free_pages.back();
+    c->free_pages.pop_back();
+    c->refcnt[p] = 1;
+  }
+}
+
+int upload(akv_cache* c, const Blob& blob, char* dst, char** dptr) {
+  if (blob.b.size() > c->stage_bytes)
+    return fail(c, AKV_ECAPACITY, "descriptor of %zu bytes exceeds the staging block (%zu)",
+                blob.b.size(), c->stage_bytes);
+  Stage& s = c->stages[c->stage_next];
+  c->stage_next = (c->stage_next + 1) % kStages;
+  if (s.used) CK(cudaEventSynchronize(s.ev));
+  if (!blob.b.empty()) {
+    std::memcpy(s.h, blob.b.data(), blob.b.size());
+    CK(cudaMemcpyAsync(dst ? dst : s.d, s.h, blob.b.size(), cudaMemcpyHostToDevice, c->stream));
+  }
+  CK(cudaEventRecord(s.ev, c->stream));
+  s.used = true;
+  *dptr = dst ? dst : s.d;
+  return AKV_OK;
+}
+
+void destroy(akv_cache* c) {
+  if (!c) return;
+  cudaStreamSynchronize(c->stream);
+  cudaFree(c->sa.keep);
+  cudaFree(c->sa.pages);
+  cudaFree(c->sa.active);
+  cudaFree(c->sa.gather);
+  cudaFree(c->sa.old_pages);
+  cudaFree(c->d_cs);
+  cudaFree(c->d_part_acc);
+  cudaFree(c->d_part_ml);
+  cudaFree(c->d_err);
+  cudaFree(c->d_plan);
+  for (Stage& s : c->stages) {
+    if (s.h) cudaFreeHost(s.h);
+    if (s.d) cudaFree(s.d);
+    if (s.ev) cudaEventDestroy(s.ev);
+  }
+  delete c;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+
+extern "C" {
+
+size_t akv_pool_bytes(const akv_config* cfg) {
+  if (check_config(cfg) != AKV_OK) return 0;
+  const int64_t phys = cfg->phys_layers ? cfg->phys_layers : cfg->layers;
+  const int64_t elem = cfg->dtype == AKV_DTYPE_BF16 ? 2 : 4;
+  return (size_t)(phys * cfg->max_pages * (int64_t)cfg->hkv * cfg->page_size * cfg->head_dim * elem);
+}
+
+int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t pool_bytes,
+                     void* stream, akv_cache** out) {
+  if (!out) return AKV_EINVAL;
+  *out = nullptr;
+  if (check_config(cfg) != AKV_OK) return AKV_EINVAL;
+  const size_t need = akv_pool_bytes(cfg);
+  if (!k_pool || !v_pool || pool_bytes < need) return AKV_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool)) & 255) return AKV_EINVAL;
+
+  akv_cache* c = new akv_cache();
+  c->cfg = *cfg;
+  if (!c->cfg.phys_layers) c->cfg.phys_layers = c->cfg.layers;
+  c->stream = static_cast<cudaStream_t>(stream);
+  const akv_config& f = c->cfg;
+  Geom& g = c->g;
+  g.k = k_pool;
+  g.v = v_pool;
+  g.layers = f.layers;
+  g.phys_layers = f.phys_layers;
+  g.hq = f.hq;
+  g.hkv = f.hkv;
+  g.d = f.head_dim;
+  g.s = f.page_size;
+  g.dtype = f.dtype;
+  g.max_pages = f.max_pages;
+  g.head_stride = (int64_t)f.page_size * f.head_dim;
+  g.page_stride = g.head_stride * f.hkv;
+  g.layer_stride = g.page_stride * f.max_pages;
+
+  SeqArrays& sa = c->sa;
+  sa.max_slots = f.max_slots;
+  sa.keep_words = (f.max_slots + 31) / 32;
+  sa.seq_pages = (f.max_slots + f.page_size - 1) / f.page_size;
+  const size_t ns = (size_t)f.max_seqs;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, dev);
+#define CKC(call)                                                              \
+  do {                                                                         \
+    cudaError_t e_ = (call);                                                   \
+    if (e_ != cudaSuccess) { destroy(c); return AKV_ECUDA; }                   \
+  } while (0)
+  CKC(e);
+  CKC(cudaMalloc(&sa.keep, ns * sa.keep_words * sizeof(uint32_t)));
+  CKC(cudaMemset(sa.keep, 0, ns * sa.keep_words * sizeof(uint32_t)));
+  CKC(cudaMalloc(&sa.pages, ns * sa.seq_pages * sizeof(int32_t)));
+  CKC(cudaMemset(sa.pages, 0xff, ns * sa.seq_pages * sizeof(int32_t)));
+  CKC(cudaMalloc(&sa.active, ns * sa.seq_pages * sizeof(int32_t)));
+  CKC(cudaMalloc(&sa.old_pages, ns * sa.seq_pages * sizeof(int32_t)));
+  CKC(cudaMalloc(&sa.gather, ns * (size_t)sa.max_slots * sizeof(int32_t)));
+
+  // RoPE table cos/sin(m f_i), m < max_slots: fp64, rounded once to fp32.
+  {
+    const int H = f.head_dim / 2;
+    std::vector<float2> cs((size_t)f.max_slots * H);
+    std::vector<double> fr(H);
+    for (int i = 0; i < H; ++i) fr[i] = std::pow(f.rope_theta, -2.0 * i / f.head_dim);
+    for (int64_t m = 0; m < f.max_slots; ++m)
+      for (int i = 0; i < H; ++i) {
+        const double ang = (double)m * fr[i];
+        cs[m * H + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    CKC(cudaMalloc(&c->d_cs, cs.size() * sizeof(float2)));
+    CKC(cudaMemcpy(c->d_cs, cs.data(), cs.size() * sizeof(float2), cudaMemcpyHostToDevice));
+  }
+  CKC(cudaMalloc(&c->d_part_acc, (size_t)kMaxItems * f.hq * f.head_dim * sizeof(float)));
+  CKC(cudaMalloc(&c->d_part_ml, (size_t)kMaxItems * f.hq * sizeof(float2)));
+  CKC(cudaMalloc(&c->d_err, sizeof(uint32_t)));
+  CKC(cudaMemset(c->d_err, 0, sizeof(uint32_t)));
+  c->plan_cap = kMaxItems * sizeof(DecodeItem) + 2 * ns * sizeof(int32_t) + 64;
+  CKC(cudaMalloc(&c->d_plan, c->plan_cap));
+  c->stage_bytes = std::max<size_t>(1 << 20, 8 * (size_t)f.max_pages + 96 * ns +
+                                                 kMaxItems * sizeof(DecodeItem) + 65536);
+  c->stage_bytes = (c->stage_bytes + 4095) & ~size_t(4095);
+  for (Stage& s : c->stages) {
+    CKC(cudaMallocHost(&s.h, c->stage_bytes));
+    CKC(cudaMalloc(&s.d, c->stage_bytes));
+    CKC(cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming));
+  }
+  CKC(cudaDeviceSynchronize());
+#undef CKC
+
+  c->refcnt.assign(f.max_pages, 0);
+  c->free_pages.resize(f.max_pages);
+  for (int32_t i = 0; i < f.max_pages; ++i) c->free_pages[i] = f.max_pages - 1 - i;
+  c->free_dslots.resize(f.max_seqs);
+  for (int32_t i = 0; i < f.max_seqs; ++i) c->free_dslots[i] = f.max_seqs - 1 - i;
+  *out = c;
+  return AKV_OK;
+}
+
+int akv_cache_destroy(akv_cache* c) {
+  if (!c) return AKV_EINVAL;
+  destroy(c);
+  return AKV_OK;
+}
+
+int akv_set_stream(akv_cache* c, void* stream) {
+  if (!c) return AKV_EINVAL;
+  c->stream = static_cast<cudaStream_t>(stream);
+  return AKV_OK;
+}
+
+int akv_seq_create(akv_cache* c, int64_t* seq) {
+  if (!c || !seq) return AKV_EINVAL;
+  if (c->free_dslots.empty()) return fail(c, AKV_ECAPACITY, "max_seqs (%d) sequences alive", c->cfg.max_seqs);
+  HostSeq s;
+  s.dslot = c->free_dslots.back();
+  c->free_dslots.pop_back();
+  const int64_t id = c->next_id++;
+  c->seqs.emplace(id, std::move(s));
+  ++c->epoch;
+  *seq = id;
+  return AKV_OK;
+}
+
+int akv_seq_fork(akv_cache* c, int64_t parent, int64_t* child) {
+  if (!c || !child) return AKV_EINVAL;
+  HostSeq* p = find(c, parent);
+  if (!p) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)parent);
+  if (c->free_dslots.empty()) return fail(c, AKV_ECAPACITY, "max_seqs (%d) sequences alive", c->cfg.max_seqs);
+  HostSeq s = *p;
+  s.dslot = c->free_dslots.back();
+  const SeqArrays& sa = c->sa;
+  const int64_t ps = p->dslot, cs = s.dslot;
+  const size_t nw = (size_t)((p->n_slots + 31) / 32);
+  const size_t np = p->pages.size();
+  CK(cudaMemcpyAsync(sa.keep + cs * sa.keep_words, sa.keep + ps * sa.keep_words,
+                     nw * sizeof(uint32_t), cudaMemcpyDeviceToDevice, c->stream));
+  CK(cudaMemcpyAsync(sa.pages + cs * sa.seq_pages, sa.pages + ps * sa.seq_pages,
+                     np * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
+  CK(cudaMemcpyAsync(sa.active + cs * sa.seq_pages, sa.active + ps * sa.seq_pages,
+                     (size_t)p->n_active_pages * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
+  if (!p->gather_identity && p->gather_n)
+    CK(cudaMemcpyAsync(sa.gather + cs * sa.max_slots, sa.gather + ps * sa.max_slots,
+                       (size_t)p->gather_n * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
+  c->free_dslots.pop_back();
+  for (int32_t pg : s.pages)
+    if (pg >= 0) ++c->refcnt[pg];
+  const int64_t id = c->next_id++;
+  c->seqs.emplace(id, std::move(s));
+  ++c->epoch;
+  *child = id;
+  return AKV_OK;
+}
+
+int akv_seq_free(akv_cache* c, int64_t seq) {
+  if (!c) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  // a free device row keeps all keep bits clear (append only sets bits)
+  CK(cudaMemsetAsync(c->sa.keep + (int64_t)s->dslot * c->sa.keep_words, 0,
+                     (size_t)c->sa.keep_words * sizeof(uint32_t), c->stream));
+  for (int32_t pg : s->pages) decref(c, pg);
+  c->free_dslots.push_back(s->dslot);
+  c->seqs.erase(seq);
+  ++c->epoch;
+  return AKV_OK;
+}
+
+// ---- Eq. (3) ---------------------------------------------------------------
+
+int akv_append(akv_cache* c, const int64_t* seqs, const int32_t* n_tokens, int32_t n_seqs,
+               const void* k_raw, const void* v, const int32_t* token_ids) {
+  if (!c || n_seqs < 0 || (n_seqs > 0 && (!seqs || !n_tokens))) return AKV_EINVAL;
+  const int S = c->cfg.page_size;
+  std::vector<HostSeq*> hs(n_seqs);
+  int64_t total = 0;
+  size_t need_pages = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    hs[i] = find(c, seqs[i]);
+    if (!hs[i]) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seqs[i]);
+    for (int j = 0; j < i; ++j)
+      if (hs[j] == hs[i]) return fail(c, AKV_EINVAL, "sequence %lld repeated", (long long)seqs[i]);
+    const int64_t n = n_tokens[i];
+    if (n < 0) return fail(c, AKV_EINVAL, "negative token count");
+    if (hs[i]->n_slots + n > c->cfg.max_slots)
+      return fail(c, AKV_ECAPACITY, "sequence %lld would hold %lld > max_slots %d tokens",
+                  (long long)seqs[i], (long long)(hs[i]->n_slots + n), c->cfg.max_slots);
+    if (n == 0) continue;
+    const int64_t old = hs[i]->n_slots;
+    need_pages += (size_t)((old + n + S - 1) / S - (old + S - 1) / S);
+    if (old % S && c->refcnt[hs[i]->pages[old / S]] > 1) ++need_pages;   // copy-on-write
+    total += n;
+  }
+  if (total == 0) return AKV_OK;
+  if (!k_raw || !v) return AKV_EINVAL;
+  if (total > INT32_MAX) return fail(c, AKV_ECAPACITY, "too many tokens in one call");
+  if (need_pages > c->free_pages.size())
+    return fail(c, AKV_ENOPAGES, "append needs %zu pages, %zu free", need_pages, c->free_pages.size());
+
+  // plan
+  std::vector<int32_t> fresh = peek_pages(c, need_pages);
+  size_t fi = 0;
+  std::vector<AppendItem> items;
+  std::vector<AppendBlock> blocks;
+  std::vector<int32_t> ids, act;
+  std::vector<PagePair> cow;
+  struct Commit { HostSeq* s; int64_t n; std::vector<std::pair<int64_t, int32_t>> set; int32_t n_act_new; };
+  std::vector<Commit> commits;
+  int64_t tok = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    const int64_t n = n_tokens[i];
+    if (n == 0) continue;
+    HostSeq* s = hs[i];
+    const int64_t old = s->n_slots;
+    AppendItem it{};
+    it.dslot = s->dslot;
+    it.slot0 = (int32_t)old;
+    it.n = (int32_t)n;
+    it.tok0 = (int32_t)tok;
+    it.k0 = (int32_t)(old / S);
+    const int64_t k1 = (old + n - 1) / S;
+    it.nk = (int32_t)(k1 - it.k0 + 1);
+    it.ids_off = (int32_t)ids.size();
+    it.act0 = s->n_active_pages;
+    it.act_off = (int32_t)act.size();
+    Commit cm{s, n, {}, 0};
+    for (int64_t k = it.k0; k <= k1; ++k) {
+      int32_t pid;
+      if (k < (int64_t)s->pages.size()) {          // partly filled tail page
+        pid = s->pages[k];
+        if (c->refcnt[pid] > 1) {
+          const int32_t np = fresh[fi++];
+          cow.push_back({pid, np});
+          cm.set.push_back({k, np});
+          pid = np;
+        }
+        if (!iv_any(s->alive, k * S, (k + 1) * S)) act.push_back((int32_t)k);
+      } else {
+        pid = fresh[fi++];
+        cm.set.push_back({k, pid});
+        act.push_back((int32_t)k);
+      }
+      ids.push_back(pid);
+    }
+    it.n_act = (int32_t)(act.size() - it.act_off);
+    cm.n_act_new = it.n_act;
+    for (int64_t t0 = 0; t0 < n; t0 += kAppendTokens) blocks.push_back({(int32_t)items.size(), (int32_t)t0});
+    items.push_back(it);
+    commits.push_back(std::move(cm));
+    tok += n;
+  }
+  Blob blob;
+  const size_t o_items = blob.put(items.data(), items.size());
+  const size_t o_blocks = blob.put(blocks.data(), blocks.size());
+  const size_t o_ids = blob.put(ids.data(), ids.size());
+  const size_t o_act = blob.put(act.data(), act.size());
+  const size_t o_cow = blob.put(cow.data(), cow.size());
+  char* d = nullptr;
+  int rc = upload(c, blob, nullptr, &d);
+  if (rc) return rc;
+
+  // commit
+  take_pages(c, need_pages);
+  size_t ti = 0;
+  for (Commit& cm : commits) {
+    HostSeq* s = cm.s;
+    const int64_t old = s->n_slots;
+    for (auto& kp : cm.set) {
+      if (kp.first < (int64_t)s->pages.size()) {
+        decref(c, s->pages[kp.first]);
+        s->pages[kp.first] = kp.second;
+      } else {
+        s->pages.push_back(kp.second);
+      }
+    }
+    if (!s->alive.empty() && s->alive.back().b == old) s->alive.back().b = old + cm.n;
+    else s->alive.push_back({old, old + cm.n});
+    if (!s->runs.empty() && s->runs.back().slot0 + s->runs.back().len == old &&
+        s->runs.back().log0 + s->runs.back().len == s->n_logical)
+      s->runs.back().len += cm.n;
+    else
+      s->runs.push_back({old, s->n_logical, cm.n});
+    for (int64_t t = 0; t < cm.n; ++t) {
+      s->key.absorb(kRecAppend);
+      s->key.absorb(token_ids ? (uint64_t)(uint32_t)token_ids[ti + t] : kNoToken);
+    }
+    ti += cm.n;
+    s->n_slots += cm.n;
+    s->n_logical += cm.n;
+    s->n_alive += cm.n;
+    s->n_active_pages += cm.n_act_new;
+  }
+  ++c->epoch;
+
+  if (!cow.empty())
+    CK(launch_copy_pages(c->g, reinterpret_cast<const PagePair*>(d + o_cow), (int)cow.size(),
+                         c->d_err, c->stream));
+  CK(launch_append(c->g, c->sa, reinterpret_cast<const AppendItem*>(d + o_items),
+                   reinterpret_cast<const AppendBlock*>(d + o_blocks), (int)blocks.size(),
+                   reinterpret_cast<const int32_t*>(d + o_ids),
+                   reinterpret_cast<const int32_t*>(d + o_act), k_raw, v, total, c->d_cs,
+                   c->d_err, c->stream));
+  return AKV_OK;
+}
+
+// ---- Eq. (4) ---------------------------------------------------------------
+
+int akv_drop(akv_cache* c, int64_t seq, const int64_t* ranges, int32_t n_ranges) {
+  if (!c || n_ranges < 0 || (n_ranges > 0 && !ranges)) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  std::vector<Interval> logical;
+  for (int i = 0; i < n_ranges; ++i) {
+    const int64_t b = ranges[2 * i], e = ranges[2 * i + 1];
+    if (b < 0 || e < b || e > s->n_logical)
+      return fail(c, AKV_ERANGE, "range [%lld, %lld) outside [0, %lld)", (long long)b,
+                  (long long)e, (long long)s->n_logical);
+    logical.push_back({b, e});
+  }
+  logical = merge(logical);
+  if (logical.empty()) return AKV_OK;     // dropping the empty set is no operation
+
+  const int S = c->cfg.page_size;
+  std::vector<Interval> slots;
+  for (const Interval& iv : logical) logical_to_slots(s->runs, iv.a, iv.b, slots);
+  slots = merge(slots);
+  std::vector<Interval> alive = s->alive, removed;
+  for (const Interval& iv : slots) iv_subtract(alive, iv.a, iv.b, &removed);
+  int64_t n_removed = 0;
+  std::vector<int64_t> dead_pages;
+  for (const Interval& iv : removed) {
+    n_removed += iv.b - iv.a;
+    for (int64_t k = iv.a / S; k <= (iv.b - 1) / S; ++k) {
+      if ((k + 1) * S > s->n_slots || s->pages[k] < 0) continue;
+      if (!dead_pages.empty() && dead_pages.back() == k) continue;
+      if (!iv_any(alive, k * S, (k + 1) * S)) dead_pages.push_back(k);
+    }
+  }
+  const int32_t n_active = iv_count_pages(alive, S);
+
+  std::vector<int32_t> r32;
+  for (const Interval& iv : slots) { r32.push_back((int32_t)iv.a); r32.push_back((int32_t)iv.b); }
+  DropItem it{};
+  it.dslot = s->dslot;
+  it.n_slots = (int32_t)s->n_slots;
+  it.n_pages = (int32_t)s->pages.size();
+  it.range_off = 0;
+  it.n_ranges = (int32_t)slots.size();
+  it.expect_active = n_active;
+  Blob blob;
+  const size_t o_item = blob.put(&it, 1);
+  const size_t o_r = blob.put(r32.data(), r32.size());
+  char* d = nullptr;
+  int rc = upload(c, blob, nullptr, &d);
+  if (rc) return rc;
+
+  // commit
+  s->alive.swap(alive);
+  s->n_alive -= n_removed;
+  s->n_active_pages = n_active;
+  for (int64_t k : dead_pages) { decref(c, s->pages[k]); s->pages[k] = -1; }
+  s->key.absorb(kRecDrop);
+  s->key.absorb(logical.size());
+  for (const Interval& iv : logical) { s->key.absorb((uint64_t)iv.a); s->key.absorb((uint64_t)iv.b); }
+  ++c->epoch;
+  CK(launch_drop(c->g, c->sa, reinterpret_cast<const DropItem*>(d + o_item), 1,
+                 reinterpret_cast<const int32_t*>(d + o_r), c->d_err, c->stream));
+  return AKV_OK;
+}
+
+// ---- Eq. (5) ---------------------------------------------------------------
+
+int akv_reposition(akv_cache* c, const int64_t* seqs, int32_t n_seqs) {
+  if (!c || n_seqs < 0 || (n_seqs > 0 && !seqs)) return AKV_EINVAL;
+  const int S = c->cfg.page_size;
+  std::vector<HostSeq*> hs(n_seqs);
+  size_t need = 0;
+  std::vector<ReposItem> items;
+  std::vector<int32_t> ids;
+  std::vector<char> dense(n_seqs, 0);
+  for (int i = 0; i < n_seqs; ++i) {
+    hs[i] = find(c, seqs[i]);
+    if (!hs[i]) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seqs[i]);
+    for (int j = 0; j < i; ++j)
+      if (hs[j] == hs[i]) return fail(c, AKV_EINVAL, "sequence %lld repeated", (long long)seqs[i]);
+    const HostSeq* s = hs[i];
+    const bool is_dense = s->alive.empty() ? s->n_slots == 0
+                                           : (s->alive.size() == 1 && s->alive[0].a == 0 &&
+                                              s->alive[0].b == s->n_slots);
+    dense[i] = is_dense;
+    if (is_dense) continue;
+    const int64_t r = s->n_alive;
+    const int64_t u = (!s->alive.empty() && s->alive[0].a == 0) ? s->alive[0].b : 0;
+    const int64_t n_kept = u / S;
+    const int64_t new_pages = (r + S - 1) / S;
+    need += (size_t)(new_pages - n_kept);
+  }
+  if (need > c->free_pages.size())
+    return fail(c, AKV_ENOPAGES, "reposition needs %zu pages, %zu free", need, c->free_pages.size());
+  std::vector<int32_t> fresh = peek_pages(c, need);
+  size_t fi = 0;
+  int32_t blocks = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    if (dense[i]) continue;
+    const HostSeq* s = hs[i];
+    const int64_t r = s->n_alive;
+    const int64_t u = (!s->alive.empty() && s->alive[0].a == 0) ? s->alive[0].b : 0;
+    ReposItem it{};
+    it.dslot = s->dslot;
+    it.old_slots = (int32_t)s->n_slots;
+    it.old_pages = (int32_t)s->pages.size();
+    it.r = (int32_t)r;
+    it.n_kept = (int32_t)(u / S);
+    it.new_pages = (int32_t)((r + S - 1) / S);
+    it.fresh_off = (int32_t)ids.size();
+    it.block0 = blocks;
+    for (int32_t k = it.n_kept; k < it.new_pages; ++k) ids.push_back(fresh[fi++]);
+    blocks += it.new_pages - it.n_kept;
+    items.push_back(it);
+  }
+  char* d = nullptr;
+  size_t o_items = 0, o_ids = 0;
+  if (!items.empty()) {
+    Blob blob;
+    o_items = blob.put(items.data(), items.size());
+    o_ids = blob.put(ids.data(), ids.size());
+    int rc = upload(c, blob, nullptr, &d);
+    if (rc) return rc;
+  }
+
+  // commit
+  take_pages(c, need);
+  size_t ii = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    HostSeq* s = hs[i];
+    s->key.absorb(kRecRepos);
+    if (dense[i]) {
+      s->gather_identity = true;
+      s->gather_n = s->n_slots;
+      continue;
+    }
+    const ReposItem& it = items[ii++];
+    // slot -> logical runs of the survivors, now dense
+    std::vector<Run> nr;
+    size_t ri = 0;
+    int64_t j = 0;
+    for (const Interval& iv : s->alive) {
+      while (ri < s->runs.size() && s->runs[ri].slot0 + s->runs[ri].len <= iv.a) ++ri;
+      for (size_t rk = ri; rk < s->runs.size() && s->runs[rk].slot0 < iv.b; ++rk) {
+        const Run& r0 = s->runs[rk];
+        const int64_t a = std::max(iv.a, r0.slot0), b = std::min(iv.b, r0.slot0 + r0.len);
+        if (a >= b) continue;
+        const int64_t lg = r0.log0 + (a - r0.slot0);
+        if (!nr.empty() && nr.back().log0 + nr.back().len == lg) nr.back().len += b - a;
+        else nr.push_back({j, lg, b - a});
+        j += b - a;
+      }
+    }
+    for (int64_t k = it.n_kept; k < (int64_t)s->pages.size(); ++k) decref(c, s->pages[k]);
+    s->pages.resize(it.n_kept);
+    for (int32_t k = 0; k < it.new_pages - it.n_kept; ++k) s->pages.push_back(ids[it.fresh_off + k]);
+    s->runs.swap(nr);
+    s->alive.clear();
+    if (it.r > 0) s->alive.push_back({0, it.r});
+    s->n_slots = it.r;
+    s->n_alive = it.r;
+    s->n_active_pages = it.new_pages;
+    s->gather_identity = false;
+    s->gather_n = it.r;
+  }
+  ++c->epoch;
+  if (!items.empty()) {
+    CK(launch_compact(c->g, c->sa, reinterpret_cast<const ReposItem*>(d + o_items),
+                      (int)items.size(), reinterpret_cast<const int32_t*>(d + o_ids), c->d_err,
+                      c->stream));
+    CK(launch_gather(c->g, c->sa, reinterpret_cast<const ReposItem*>(d + o_items),
+                     (int)items.size(), blocks, c->d_cs, c->d_err, c->stream));
+  }
+  return AKV_OK;
+}
+
+// ---- decode ------------------------------------------------------------------
+
+int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64_t* seqs,
+                         int32_t n_seqs, float* out) {
+  if (!c || n_seqs < 0 || (n_seqs > 0 && (!seqs || !q || !out))) return AKV_EINVAL;
+  if (layer < 0 || layer >= c->cfg.layers) return fail(c, AKV_EINVAL, "layer %d out of range", layer);
+  if (n_seqs == 0) return AKV_OK;
+  const bool same = c->plan_epoch == c->epoch && (int)c->plan_seqs.size() == n_seqs &&
+                    std::equal(c->plan_seqs.begin(), c->plan_seqs.end(), seqs);
+  if (!same) {
+    std::vector<const HostSeq*> hs(n_seqs);
+    int64_t total = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+      hs[i] = find(c, seqs[i]);
+      if (!hs[i]) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seqs[i]);
+      total += hs[i]->n_active_pages;
+    }
+    // split so that the (item, kv head) blocks fill the GPU a few times over
+    const int64_t target = (int64_t)c->sm_count * 8;
+    int64_t pps = std::max<int64_t>(4, (total * c->cfg.hkv + target - 1) / target);
+    for (;;) {
+      int64_t items = 0;
+      for (int i = 0; i < n_seqs; ++i) items += std::max<int64_t>(1, (hs[i]->n_active_pages + pps - 1) / pps);
+      if (items <= kMaxItems) break;
+      pps *= 2;
+    }
+    std::vector<DecodeItem> items;
+    std::vector<int32_t> item0(n_seqs), splits(n_seqs);
+    bool combine = false;
+    for (int i = 0; i < n_seqs; ++i) {
+      const HostSeq* s = hs[i];
+      const int32_t na = s->n_active_pages;
+      const int32_t ns = (int32_t)std::max<int64_t>(1, (na + pps - 1) / pps);
+      item0[i] = (int32_t)items.size();
+      splits[i] = ns;
+      combine |= ns > 1;
+      for (int32_t k = 0; k < ns; ++k) {
+        DecodeItem it{};
+        it.dslot = s->dslot;
+        it.row = i;
+        it.p0 = (int32_t)std::min<int64_t>(na, (int64_t)k * pps);
+        it.p1 = (int32_t)std::min<int64_t>(na, (int64_t)(k + 1) * pps);
+        it.pos_q = (int32_t)(s->n_slots - 1);
+        it.n_splits = ns;
+        it.item0 = item0[i];
+        items.push_back(it);
+      }
+    }
+    Blob blob;
+    blob.put(items.data(), items.size());
+    blob.put(item0.data(), item0.size());
+    blob.put(splits.data(), splits.size());
+    if (blob.b.size() > c->plan_cap) return fail(c, AKV_ECAPACITY, "decode plan too large");
+    char* d = nullptr;
+    int rc = upload(c, blob, c->d_plan, &d);
+    if (rc) return rc;
+    c->plan_epoch = c->epoch;
+    c->plan_seqs.assign(seqs, seqs + n_seqs);
+    c->plan_items = (int)items.size();
+    c->plan_combine = combine;
+  }
+  const size_t n_items = (size_t)c->plan_items;
+  const size_t o_item0 = (n_items * sizeof(DecodeItem) + 15) & ~size_t(15);
+  const size_t o_splits = (o_item0 + n_seqs * sizeof(int32_t) + 15) & ~size_t(15);
+  DecodeArgs a{};
+  a.g = c->g;
+  a.sa = c->sa;
+  a.items = reinterpret_cast<const DecodeItem*>(c->d_plan);
+  a.n_items = c->plan_items;
+  a.layer = layer;
+  a.q = q;
+  a.out = out;
+  a.part_acc = c->d_part_acc;
+  a.part_ml = c->d_part_ml;
+  a.cs = c->d_cs;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+  a.err = c->d_err;
+  a.wait_limit = c->wait_limit;
+  CK(launch_decode(a, c->plan_combine, n_seqs,
+                   reinterpret_cast<const int32_t*>(c->d_plan + o_item0),
+                   reinterpret_cast<const int32_t*>(c->d_plan + o_splits), c->stream));
+  return AKV_OK;
+}
+
+// ---- introspection -------------------------------------------------------------
+
+int akv_seq_info(akv_cache* c, int64_t seq, akv_seq_info_t* info) {
+  if (!c || !info) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  info->n_logical = s->n_logical;
+  info->n_held = s->n_slots;
+  info->n_active = s->n_alive;
+  info->next_pos = s->n_slots;
+  info->n_pages = (int32_t)s->pages.size();
+  info->n_active_pages = s->n_active_pages;
+  int32_t own = 0, shared = 0;
+  for (int32_t p : s->pages) {
+    if (p < 0) continue;
+    if (c->refcnt[p] > 1) ++shared; else ++own;
+  }
+  info->n_owned_pages = own;
+  info->n_shared_pages = shared;
+  return AKV_OK;
+}
+
+int akv_seq_positions(akv_cache* c, int64_t seq, int32_t* pos) {
+  if (!c || !pos) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  for (int64_t i = 0; i < s->n_slots; ++i) pos[i] = (int32_t)i;   // slot s is position s
+  return AKV_OK;
+}
+
+int akv_seq_keep_mask(akv_cache* c, int64_t seq, uint8_t* keep) {
+  if (!c || !keep) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  const size_t nw = (size_t)((s->n_slots + 31) / 32);
+  std::vector<uint32_t> w(nw);
+  if (nw) {
+    CK(cudaMemcpyAsync(w.data(), c->sa.keep + (int64_t)s->dslot * c->sa.keep_words,
+                       nw * sizeof(uint32_t), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+  }
+  for (int64_t i = 0; i < s->n_slots; ++i) keep[i] = (w[i / 32] >> (i % 32)) & 1u;
+  return AKV_OK;
+}
+
+int akv_seq_logical(akv_cache* c, int64_t seq, int64_t* logical) {
+  if (!c || !logical) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  for (const Run& r : s->runs)
+    for (int64_t t = 0; t < r.len; ++t) logical[r.slot0 + t] = r.log0 + t;
+  return AKV_OK;
+}
+
+int akv_seq_gather_map(akv_cache* c, int64_t seq, int32_t* map, int64_t* n) {
+  if (!c || !n) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  *n = s->gather_n;
+  if (!map || !s->gather_n) return AKV_OK;
+  if (s->gather_identity) {
+    for (int64_t i = 0; i < s->gather_n; ++i) map[i] = (int32_t)i;
+    return AKV_OK;
+  }
+  CK(cudaMemcpyAsync(map, c->sa.gather + (int64_t)s->dslot * c->sa.max_slots,
+                     (size_t)s->gather_n * sizeof(int32_t), cudaMemcpyDeviceToHost, c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  return AKV_OK;
+}
+
+int akv_seq_page_table(akv_cache* c, int64_t seq, int32_t* pages, int32_t* n_pages,
+                       int32_t* active, int32_t* n_active) {
+  if (!c) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  if (n_pages) *n_pages = (int32_t)s->pages.size();
+  if (n_active) *n_active = s->n_active_pages;
+  const int64_t row = (int64_t)s->dslot * c->sa.seq_pages;
+  if (pages && !s->pages.empty())
+    CK(cudaMemcpyAsync(pages, c->sa.pages + row, s->pages.size() * sizeof(int32_t),
+                       cudaMemcpyDeviceToHost, c->stream));
+  if (active && s->n_active_pages)
+    CK(cudaMemcpyAsync(active, c->sa.active + row, (size_t)s->n_active_pages * sizeof(int32_t),
+                       cudaMemcpyDeviceToHost, c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  return AKV_OK;
+}
+
+int akv_history_key(akv_cache* c, int64_t seq, uint64_t key[2]) {
+  if (!c || !key) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  key[0] = s->key.a;
+  key[1] = s->key.b;
+  return AKV_OK;
+}
+
+int akv_page_refcount(akv_cache* c, int32_t page, int32_t* refcount) {
+  if (!c || !refcount || page < 0 || page >= c->cfg.max_pages) return AKV_EINVAL;
+  *refcount = c->refcnt[page];
+  return AKV_OK;
+}
+
+int akv_pool_stats(akv_cache* c, int32_t* free_pages, int32_t* used_pages) {
+  if (!c) return AKV_EINVAL;
+  if (free_pages) *free_pages = (int32_t)c->free_pages.size();
+  if (used_pages) *used_pages = c->cfg.max_pages - (int32_t)c->free_pages.size();
+  return AKV_OK;
+}
+
+const char* akv_last_error(akv_cache* c) { return c ? c->err.c_str() : "null cache"; }
+
+int akv_sync_errors(akv_cache* c, uint32_t* word) {
+  if (!c) return AKV_EINVAL;
+  uint32_t w = 0;
+  CK(cudaStreamSynchronize(c->stream));
+  CK(cudaMemcpy(&w, c->d_err, sizeof(w), cudaMemcpyDeviceToHost));
+  CK(cudaMemset(c->d_err, 0, sizeof(w)));
+  if (word) *word = w;
+  return w ? fail(c, AKV_EDEVICE, "device error word 0x%x", w) : AKV_OK;
+}
+
+int akv_set_wait_limit(akv_cache* c, uint32_t polls) {
+  if (!c || polls == 0) return AKV_EINVAL;
+  c->wait_limit = polls;
+  return AKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// Internal interface between the host planner (akv_host.cpp) and the CUDA
+// kernels (akv_kernels.cu, akv_decode.cu).  Not part of the public ABI.
+//
+// Every operation is planned on the host (which owns page allocation and the
+// per-sequence counts), packed into one small descriptor blob, copied to the
+// device once, and executed by one to three kernels on the cache's stream.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace akv {
+
+// Pool geometry.  Layout: [phys_layer][page][kv_head][slot_in_page][head_dim].
+struct Geom {
+  void* k;
+  void* v;
+  int64_t layer_stride;  // elements between physical layers
+  int64_t page_stride;   // elements between pages (hkv * S * D)
+  int64_t head_stride;   // elements between heads (S * D)
+  int32_t layers, phys_layers, hq, hkv, d, s, dtype, max_pages;
+};
+
+// Per-sequence device arrays, one fixed-size row per device sequence slot
+// ("dslot"); row i of `keep` starts at i * keep_words, and so on.
+struct SeqArrays {
+  uint32_t* keep;       // keep bit per held slot
+  int32_t* pages;       // pool page id per slot page (-1 once released)
+  int32_t* active;      // slot-page indices holding an active token, ascending
+  int32_t* gather;      // last reposition's gather map (new slot -> old slot)
+  int32_t* old_pages;   // snapshot of replaced page ids during a reposition
+  int32_t keep_words;   // ceil(max_slots / 32)
+  int32_t seq_pages;    // ceil(max_slots / S)
+  int32_t max_slots;
+};
+
+// ---- append (Eq. 3) -------------------------------------------------------
+struct AppendItem {
+  int32_t dslot;
+  int32_t slot0;     // first new slot (== old n_held == position)
+  int32_t n;         // tokens appended
+  int32_t tok0;      // row of the first token in k_raw / v
+  int32_t k0;        // first slot page touched
+  int32_t nk;        // slot pages touched (page ids in ids[ids_off..])
+  int32_t ids_off;
+  int32_t act0;      // first active-list entry written
+  int32_t n_act;     // active-list entries written (from act[act_off..])
+  int32_t act_off;
+};
+struct AppendBlock { int32_t item, t0; };   // block -> (item, first token)
+constexpr int kAppendTokens = 16;           // tokens per append block
+
+// ---- copy-on-write page copy ----------------------------------------------
+struct PagePair { int32_t src, dst; };
+
+// ---- drop (Eq. 4) -----------------------------------------------------------
+struct DropItem {
+  int32_t dslot;
+  int32_t n_slots;      // held slots
+  int32_t n_pages;      // slot pages
+  int32_t range_off;    // slot ranges (pairs) in ranges[range_off..]
+  int32_t n_ranges;
+  int32_t expect_active;  // host's count of active pages afterwards
+};
+
+// ---- reposition (Eq. 5) -------------------------------------------------------
+struct ReposItem {
+  int32_t dslot;
+  int32_t old_slots;    // held slots before
+  int32_t old_pages;    // slot pages before
+  int32_t r;            // survivors (host count)
+  int32_t n_kept;       // leading pages that keep their id
+  int32_t new_pages;    // ceil(r / S)
+  int32_t fresh_off;    // fresh page ids in ids[fresh_off..], new_pages - n_kept
+  int32_t block0;       // first gather block of this item (prefix sum)
+};
+
+// ---- decode ---------------------------------------------------------------------
+struct DecodeItem {
+  int32_t dslot;
+  int32_t row;          // row of q / out
+  int32_t p0, p1;       // active-list range [p0, p1) of this split
+  int32_t pos_q;        // query position (next_pos - 1), -1 if no token held
+  int32_t n_splits;     // splits of this row
+  int32_t item0;        // first item of this row
+  int32_t pad;
+};
+
+struct DecodeArgs {
+  Geom g;
+  SeqArrays sa;
+  const DecodeItem* items;
+  int32_t n_items;
+  int32_t layer;        // logical layer (slab = layer % phys_layers)
+  const void* q;
+  float* out;
+  float* part_acc;      // [item][hkv][group][D]
+  float2* part_ml;      // [item][hkv][group] (max, sum) in log2 units
+  const float2* cs;     // RoPE table [max_slots][D/2] (cos, sin)
+  float scale_log2;     // log2(e) / sqrt(D)
+  uint32_t* err;
+  uint32_t wait_limit;
+};
+
+// Launchers (akv_kernels.cu / akv_decode.cu).  All enqueue on `st`.
+cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* items,
+                          const AppendBlock* blocks, int n_blocks, const int32_t* ids,
+                          const int32_t* act, const void* k_raw, const void* v,
+                          int64_t total_tokens, const float2* cs, uint32_t* err,
+                          cudaStream_t st);
+cudaError_t launch_copy_pages(const Geom& g, const PagePair* pairs, int n_pairs,
+                              uint32_t* err, cudaStream_t st);
+cudaError_t launch_drop(const Geom& g, const SeqArrays& sa, const DropItem* items,
+                        int n_items, const int32_t* ranges, uint32_t* err, cudaStream_t st);
+cudaError_t launch_compact(const Geom& g, const SeqArrays& sa, const ReposItem* items,
+                           int n_items, const int32_t* ids, uint32_t* err, cudaStream_t st);
+cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* items,
+                          int n_items, int n_blocks, const float2* cs, uint32_t* err,
+                          cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, bool need_combine, int n_rows,
+                          const int32_t* row_item0, const int32_t* row_splits,
+                          cudaStream_t st);
+
+}  // namespace akv

@@ -1,0 +1,500 @@
+// Cache-maintenance kernels: append (Eq. 3), drop (Eq. 4), reposition
+// (Eq. 5: compaction + gather/rotate/store), and the copy-on-write page copy.
+//
+// Sources: "Cache Engineering for Agents" paper review, 3.3 Cache Operations
+// (Eqs. 3-5); "[Repo Review] AKV", 5.5 (the reposition kernel un-rotates the
+// old position and rotates the new one in FP32, copies V and non-RoPE parts,
+// copies raw values when the position is unchanged, and writes to a separate
+// destination slot).
+//
+// Every kernel validates the indices it takes from metadata and, instead of
+// touching memory out of bounds, sets a bit in the device error word and
+// skips the access.
+#include <cuda_bf16.h>
+
+#include "akv.h"
+#include "akv_internal.h"
+
+namespace akv {
+namespace {
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of the pool dtype
+// ---------------------------------------------------------------------------
+
+template <typename T> struct Vec;
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int E = 8;
+  __device__ static void unpack(uint4 u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static uint4 pack(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <> struct Vec<float> {
+  static constexpr int E = 4;
+  __device__ static void unpack(uint4 u, float* f) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+  __device__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+};
+
+__device__ __forceinline__ uint4 ld16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// One rotation unit: E consecutive pairs (i, i + D/2) starting at i = c*E.
+// (x, y) -> (x cos - y sin, x sin + y cos), fp32, rounded once to T.
+template <typename T>
+__device__ __forceinline__ void rotate_unit(const T* src, T* dst, int c, int half,
+                                            const float2* cs_row) {
+  constexpr int E = Vec<T>::E;
+  const uint4 lo = ld16(src + c * E);
+  const uint4 hi = ld16(src + half + c * E);
+  float x[E], y[E], xo[E], yo[E];
+  Vec<T>::unpack(lo, x);
+  Vec<T>::unpack(hi, y);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float2 t = cs_row[c * E + e];
+    xo[e] = fmaf(x[e], t.x, -y[e] * t.y);
+    yo[e] = fmaf(x[e], t.y, y[e] * t.x);
+  }
+  st16(dst + c * E, Vec<T>::pack(xo));
+  st16(dst + half + c * E, Vec<T>::pack(yo));
+}
+
+template <typename T>
+__device__ __forceinline__ void copy_unit(const T* src, T* dst, int c, int half) {
+  constexpr int E = Vec<T>::E;
+  st16(dst + c * E, ld16(src + c * E));
+  st16(dst + half + c * E, ld16(src + half + c * E));
+}
+
+__device__ __forceinline__ void flag(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
+
+// ---------------------------------------------------------------------------
+// append: K = R(pos) K_raw, V copied; pages/active/keep metadata updated
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
+         const AppendBlock* __restrict__ blocks, const int32_t* __restrict__ ids,
+         const int32_t* __restrict__ act, const T* __restrict__ k_raw,
+         const T* __restrict__ v_raw, int64_t total_tokens,
+         const float2* __restrict__ cs, uint32_t* err) {
+  extern __shared__ float2 s_cs[];   // [kAppendTokens][D/2]
+  __shared__ int s_page[kAppendTokens];
+  __shared__ int s_off[kAppendTokens];
+  const AppendBlock blk = blocks[blockIdx.x];
+  const AppendItem it = items[blk.item];
+  const int nt = min(kAppendTokens, it.n - blk.t0);
+  const int D = g.d, H = D / 2, S = g.s;
+  const int tid = threadIdx.x, bs = blockDim.x;
+  const int64_t row_base = (int64_t)it.dslot;
+
+  if (blk.t0 == 0) {
+    for (int i = tid; i < it.nk; i += bs) {
+      const int k = it.k0 + i;
+      if (k >= 0 && k < sa.seq_pages) sa.pages[row_base * sa.seq_pages + k] = ids[it.ids_off + i];
+      else flag(err, AKV_DERR_INDEX);
+    }
+    for (int i = tid; i < it.n_act; i += bs) {
+      const int a = it.act0 + i;
+      if (a >= 0 && a < sa.seq_pages) sa.active[row_base * sa.seq_pages + a] = act[it.act_off + i];
+      else flag(err, AKV_DERR_INDEX);
+    }
+  }
+  for (int t = tid; t < nt; t += bs) {
+    const int slot = it.slot0 + blk.t0 + t;
+    int pid = -1;
+    if (slot >= 0 && slot < sa.max_slots) {
+      atomicOr(&sa.keep[row_base * sa.keep_words + slot / 32], 1u << (slot % 32));
+      const int pk = slot / S - it.k0;
+      if (pk >= 0 && pk < it.nk) pid = ids[it.ids_off + pk];
+    }
+    if (pid < 0 || pid >= g.max_pages) { flag(err, AKV_DERR_PAGE); pid = -1; }
+    s_page[t] = pid;
+    s_off[t] = slot % S;
+  }
+  for (int i = tid; i < nt * H; i += bs) {
+    const int slot = it.slot0 + blk.t0 + i / H;
+    s_cs[i] = (slot >= 0 && slot < sa.max_slots) ? cs[(int64_t)slot * H + i % H]
+                                                  : make_float2(1.f, 0.f);
+  }
+  __syncthreads();
+
+  constexpr int E = Vec<T>::E;
+  const int ku = H / E, vu = D / E, per_row = ku + vu;
+  const int units = g.hkv * nt * per_row;
+  const T* kb = k_raw;
+  const T* vb = v_raw;
+  T* kp = static_cast<T*>(g.k);
+  T* vp = static_cast<T*>(g.v);
+  for (int u = tid; u < units; u += bs) {
+    const int r = u % per_row;
+    const int t = (u / per_row) % nt;
+    const int h = u / (per_row * nt);
+    const int pid = s_page[t];
+    if (pid < 0) continue;
+    const int64_t tok = it.tok0 + blk.t0 + t;
+    const int64_t dst_off = (int64_t)pid * g.page_stride + (int64_t)h * g.head_stride +
+                            (int64_t)s_off[t] * D;
+    // logical layers in order, so aliased slabs keep the last layer's data
+    for (int l = 0; l < g.layers; ++l) {
+      const int64_t src_off = ((int64_t)l * total_tokens + tok) * g.hkv * D + (int64_t)h * D;
+      const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
+      if (r < ku) {
+        rotate_unit<T>(kb + src_off, kp + slab + dst_off, r, H, s_cs + t * H);
+      } else {
+        const int c = r - ku;
+        st16(vp + slab + dst_off + c * E, ld16(vb + src_off + c * E));
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// copy-on-write: copy whole pages (every physical layer, K and V)
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_copy_pages(Geom g, const PagePair* __restrict__ pairs, uint32_t* err) {
+  const PagePair pp = pairs[blockIdx.x];
+  if (pp.src < 0 || pp.src >= g.max_pages || pp.dst < 0 || pp.dst >= g.max_pages) {
+    if (threadIdx.x == 0) flag(err, AKV_DERR_PAGE);
+    return;
+  }
+  constexpr int E = Vec<T>::E;
+  const int64_t slab = (int64_t)blockIdx.y * g.layer_stride;
+  const int n = (int)(g.page_stride / E);
+  const T* ks = static_cast<const T*>(g.k) + slab + pp.src * g.page_stride;
+  const T* vs = static_cast<const T*>(g.v) + slab + pp.src * g.page_stride;
+  T* kd = static_cast<T*>(g.k) + slab + pp.dst * g.page_stride;
+  T* vd = static_cast<T*>(g.v) + slab + pp.dst * g.page_stride;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    st16(kd + i * E, ld16(ks + i * E));
+    st16(vd + i * E, ld16(vs + i * E));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// block-wide exclusive scan of one int per thread (blockDim.x == 1024)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int block_exclusive_scan(int x, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < nw) s_warp[lane] = wi - w;   // exclusive warp offsets
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const int r = s_warp[warp] + incl - x;
+  __syncthreads();   // s_warp is reused by the next call
+  return r;
+}
+
+// keep bits of slot page k (S slots starting at k*S), S in {1,...,64}
+__device__ __forceinline__ int page_popc(const uint32_t* keep, int k, int S) {
+  const int64_t first = (int64_t)k * S;
+  if (S >= 32) {
+    int c = 0;
+    for (int w = 0; w < S / 32; ++w) c += __popc(keep[first / 32 + w]);
+    return c;
+  }
+  const uint32_t word = keep[first / 32];
+  const uint32_t m = (S == 32) ? 0xffffffffu : ((1u << S) - 1u);
+  return __popc((word >> (first % 32)) & m);
+}
+
+// ---------------------------------------------------------------------------
+// drop: clear keep bits of slot ranges, rebuild the active page list,
+// release (mark -1) full pages left with no active token
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(1024)
+k_drop(Geom g, SeqArrays sa, const DropItem* __restrict__ items,
+       const int32_t* __restrict__ ranges, uint32_t* err) {
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  const DropItem it = items[blockIdx.x];
+  uint32_t* keep = sa.keep + (int64_t)it.dslot * sa.keep_words;
+  int32_t* pages = sa.pages + (int64_t)it.dslot * sa.seq_pages;
+  int32_t* active = sa.active + (int64_t)it.dslot * sa.seq_pages;
+  const int S = g.s;
+
+  for (int r = 0; r < it.n_ranges; ++r) {
+    const int a = ranges[it.range_off + 2 * r];
+    const int b = ranges[it.range_off + 2 * r + 1];
+    if (a < 0 || b > it.n_slots || a > b) {
+      if (threadIdx.x == 0) flag(err, AKV_DERR_INDEX);
+      continue;
+    }
+    if (a == b) continue;
+    const int w0 = a / 32, w1 = (b - 1) / 32;
+    for (int w = w0 + (int)threadIdx.x; w <= w1; w += blockDim.x) {
+      const int lo = max(a - w * 32, 0), hi = min(b - w * 32, 32);
+      const uint32_t m = (hi == 32 ? 0xffffffffu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+      atomicAnd(&keep[w], ~m);
+    }
+  }
+  __syncthreads();
+
+  int carry = 0;
+  for (int base = 0; base < it.n_pages; base += blockDim.x) {
+    const int k = base + threadIdx.x;
+    int live = 0;
+    if (k < it.n_pages) {
+      live = page_popc(keep, k, S) > 0;
+      if (!live && (int64_t)(k + 1) * S <= it.n_slots) pages[k] = -1;
+    }
+    const int pos = block_exclusive_scan(live, s_warp, &s_total);
+    if (live) active[carry + pos] = k;
+    carry += s_total;
+  }
+  if (threadIdx.x == 0 && carry != it.expect_active) flag(err, AKV_DERR_COUNT);
+}
+
+// ---------------------------------------------------------------------------
+// reposition, part 1: compaction.  Exclusive prefix sum of the keep bits
+// (ballot-free: each thread owns one 32-slot word, popc + block scan) gives
+// the gather map; the new page table, keep bits and active list follow.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(1024)
+k_compact(Geom g, SeqArrays sa, const ReposItem* __restrict__ items,
+          const int32_t* __restrict__ ids, uint32_t* err) {
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  const ReposItem it = items[blockIdx.x];
+  uint32_t* keep = sa.keep + (int64_t)it.dslot * sa.keep_words;
+  int32_t* pages = sa.pages + (int64_t)it.dslot * sa.seq_pages;
+  int32_t* active = sa.active + (int64_t)it.dslot * sa.seq_pages;
+  int32_t* oldp = sa.old_pages + (int64_t)it.dslot * sa.seq_pages;
+  int32_t* gather = sa.gather + (int64_t)it.dslot * sa.max_slots;
+  const int S = g.s;
+
+  // snapshot the page ids the gather will read from
+  for (int k = it.n_kept + (int)threadIdx.x; k < it.old_pages; k += blockDim.x)
+    oldp[k] = pages[k];
+
+  // gather map: new slot j <- old slot of the j-th set keep bit
+  const int nw = (it.old_slots + 31) / 32;
+  int carry = 0;
+  for (int base = 0; base < nw; base += blockDim.x) {
+    const int w = base + threadIdx.x;
+    uint32_t bits = 0;
+    if (w < nw) {
+      bits = keep[w];
+      const int tail = it.old_slots - w * 32;
+      if (tail < 32) bits &= (1u << tail) - 1u;
+    }
+    const int pos = block_exclusive_scan(__popc(bits), s_warp, &s_total);
+    int j = carry + pos;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      if (j < sa.max_slots) gather[j] = w * 32 + b;
+      else flag(err, AKV_DERR_INDEX);
+      ++j;
+    }
+    carry += s_total;
+  }
+  if (threadIdx.x == 0 && carry != it.r) flag(err, AKV_DERR_COUNT);
+  __syncthreads();
+
+  // new page table: kept prefix unchanged, fresh ids after, released tail
+  for (int k = it.n_kept + (int)threadIdx.x; k < max(it.new_pages, it.old_pages); k += blockDim.x)
+    pages[k] = k < it.new_pages ? ids[it.fresh_off + (k - it.n_kept)] : -1;
+  // keep bits: exactly slots [0, r)
+  for (int w = threadIdx.x; w < nw; w += blockDim.x) {
+    const int n = it.r - w * 32;
+    keep[w] = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+  }
+  for (int k = threadIdx.x; k < it.new_pages; k += blockDim.x) active[k] = k;
+}
+
+// ---------------------------------------------------------------------------
+// reposition, part 2: gather + delta rotation + store, one block per fresh
+// destination page, all layers and KV heads.  Survivor j moves from old slot
+// src_j to j: K' = R(j - src_j) K (bit copy when j == src_j), V copied.
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
+         const float2* __restrict__ cs, uint32_t* err) {
+  extern __shared__ float2 s_cs[];   // [S][D/2], angle -(src - j) f
+  __shared__ int s_src_page[64];
+  __shared__ int s_src_off[64];
+  __shared__ int s_copy[64];
+  __shared__ int s_dst_page;
+  int lo = 0, hi = n_items - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (items[mid].block0 <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+  }
+  const ReposItem it = items[lo];
+  const int S = g.s, D = g.d, H = D / 2;
+  const int k = it.n_kept + ((int)blockIdx.x - it.block0);
+  const int j0 = k * S;
+  const int nj = min(S, it.r - j0);
+  const int32_t* gather = sa.gather + (int64_t)it.dslot * sa.max_slots;
+  const int32_t* oldp = sa.old_pages + (int64_t)it.dslot * sa.seq_pages;
+  const int tid = threadIdx.x, bs = blockDim.x;
+
+  if (tid == 0) {
+    int p = (k >= 0 && k < sa.seq_pages) ? sa.pages[(int64_t)it.dslot * sa.seq_pages + k] : -1;
+    if (p < 0 || p >= g.max_pages) { flag(err, AKV_DERR_PAGE); p = -1; }
+    s_dst_page = p;
+  }
+  for (int t = tid; t < nj; t += bs) {
+    const int j = j0 + t;
+    const int src = gather[j];
+    int sp = -1;
+    if (src >= j && src < it.old_slots) sp = oldp[src / S];
+    if (sp < 0 || sp >= g.max_pages) { flag(err, AKV_DERR_PAGE); sp = -1; }
+    s_src_page[t] = sp;
+    s_src_off[t] = src % S;
+    s_copy[t] = (src == j);
+  }
+  for (int i = tid; i < nj * H; i += bs) {
+    const int t = i / H;
+    const int delta = gather[j0 + t] - (j0 + t);
+    float2 c = make_float2(1.f, 0.f);
+    if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * H + i % H];
+    s_cs[i] = make_float2(c.x, -c.y);
+  }
+  __syncthreads();
+  const int dpage = s_dst_page;
+  if (dpage < 0) return;
+
+  constexpr int E = Vec<T>::E;
+  const int ku = H / E, vu = D / E, per_row = ku + vu;
+  const int units = g.hkv * nj * per_row;
+  T* kp = static_cast<T*>(g.k);
+  T* vp = static_cast<T*>(g.v);
+  for (int u = tid; u < units; u += bs) {
+    const int r = u % per_row;
+    const int t = (u / per_row) % nj;
+    const int h = u / (per_row * nj);
+    const int sp = s_src_page[t];
+    if (sp < 0) continue;
+    const int64_t src_off = (int64_t)sp * g.page_stride + (int64_t)h * g.head_stride +
+                            (int64_t)s_src_off[t] * D;
+    const int64_t dst_off = (int64_t)dpage * g.page_stride + (int64_t)h * g.head_stride +
+                            (int64_t)t * D;
+    const bool cp = s_copy[t];
+#pragma unroll 4
+    for (int l = 0; l < g.layers; ++l) {
+      const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
+      if (r < ku) {
+        if (cp) copy_unit<T>(kp + slab + src_off, kp + slab + dst_off, r, H);
+        else rotate_unit<T>(kp + slab + src_off, kp + slab + dst_off, r, H, s_cs + t * H);
+      } else {
+        const int c = r - ku;
+        st16(vp + slab + dst_off + c * E, ld16(vp + slab + src_off + c * E));
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* items,
+                          const AppendBlock* blocks, int n_blocks, const int32_t* ids,
+                          const int32_t* act, const void* k_raw, const void* v,
+                          int64_t total_tokens, const float2* cs, uint32_t* err,
+                          cudaStream_t st) {
+  if (n_blocks <= 0) return cudaSuccess;
+  const size_t smem = (size_t)kAppendTokens * (g.d / 2) * sizeof(float2);
+  if (g.dtype == AKV_DTYPE_BF16)
+    k_append<__nv_bfloat16><<<n_blocks, 256, smem, st>>>(
+        g, sa, items, blocks, ids, act, static_cast<const __nv_bfloat16*>(k_raw),
+        static_cast<const __nv_bfloat16*>(v), total_tokens, cs, err);
+  else
+    k_append<float><<<n_blocks, 256, smem, st>>>(
+        g, sa, items, blocks, ids, act, static_cast<const float*>(k_raw),
+        static_cast<const float*>(v), total_tokens, cs, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_pages(const Geom& g, const PagePair* pairs, int n_pairs,
+                              uint32_t* err, cudaStream_t st) {
+  if (n_pairs <= 0) return cudaSuccess;
+  dim3 grid(n_pairs, g.phys_layers);
+  if (g.dtype == AKV_DTYPE_BF16)
+    k_copy_pages<__nv_bfloat16><<<grid, 256, 0, st>>>(g, pairs, err);
+  else
+    k_copy_pages<float><<<grid, 256, 0, st>>>(g, pairs, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_drop(const Geom& g, const SeqArrays& sa, const DropItem* items,
+                        int n_items, const int32_t* ranges, uint32_t* err, cudaStream_t st) {
+  if (n_items <= 0) return cudaSuccess;
+  k_drop<<<n_items, 1024, 0, st>>>(g, sa, items, ranges, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact(const Geom& g, const SeqArrays& sa, const ReposItem* items,
+                           int n_items, const int32_t* ids, uint32_t* err, cudaStream_t st) {
+  if (n_items <= 0) return cudaSuccess;
+  k_compact<<<n_items, 1024, 0, st>>>(g, sa, items, ids, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* items,
+                          int n_items, int n_blocks, const float2* cs, uint32_t* err,
+                          cudaStream_t st) {
+  if (n_blocks <= 0) return cudaSuccess;
+  const size_t smem = (size_t)g.s * (g.d / 2) * sizeof(float2);
+  if (g.dtype == AKV_DTYPE_BF16)
+    k_gather<__nv_bfloat16><<<n_blocks, 256, smem, st>>>(g, sa, items, n_items, cs, err);
+  else
+    k_gather<float><<<n_blocks, 256, smem, st>>>(g, sa, items, n_items, cs, err);
+  return cudaGetLastError();
+}
+
+}  // namespace akv

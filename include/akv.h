@@ -1,0 +1,220 @@
+/*
+ * akv.h -- C ABI of the active-KV cache library (GB300, sm_103a).
+ *
+ * The library keeps, for many sequences, a paged K/V cache in which a set of
+ * logical tokens can be dropped from attention, the survivors repositioned
+ * to dense positions with their keys re-rotated, and decode attention read
+ * only the active tokens.  Sources ("Cache Engineering for Agents" paper
+ * review; "[Repo Review] AKV" code review):
+ *
+ *   append      -- paper review, 3.3 Cache Operations, Eq. (3)
+ *   drop        -- paper review, 3.3, Eq. (4); AKV review, 1 (Drop)
+ *   reposition  -- paper review, 3.3, Eq. (5); AKV review, 5.5 (kernel)
+ *   history     -- paper review, 3.4 Cache Operation Sequence, Eq. (6)
+ *   copy-on-write of shared pages -- paper review, 4.2.3 Reposition-aware
+ *                  Cache Management; AKV review, 5.4 (OccurrenceState)
+ *   decode      -- attention over the active KV only; paper review, A.4.1
+ *
+ * Conventions (all calls):
+ *   - Every function returns AKV_OK (0) or a negative AKV_E* code.  On an
+ *     error the cache state is unchanged (each call plans on the host, checks
+ *     every limit, then commits).  akv_last_error() gives a message.
+ *   - "device" pointers are CUDA device memory; "host" pointers are host
+ *     memory read (or written) before the call returns.
+ *   - All GPU work of a cache is enqueued on the cache's stream (set at
+ *     creation, changeable with akv_set_stream) and is asynchronous: no call
+ *     on the append/drop/reposition/decode path waits for the GPU.  Device
+ *     buffers passed in must stay valid until that work has run.  Calls on
+ *     one cache must not run concurrently from several host threads.
+ *   - Positions: a sequence's held tokens (everything since its last
+ *     reposition, dropped or not) sit in slots 0..n_held-1; the RoPE position
+ *     of slot s is s, and the next append lands at n_held.  Drop does not
+ *     move anything, so it never lowers the next position (paper review,
+ *     Appendix A.1.1, Figure 10: E lands at 3 after D is dropped).
+ *   - RoPE is the half-split form (pairs (i, i+D/2), f_i = theta^(-2i/D)).
+ */
+#ifndef AKV_H
+#define AKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AKV_OK 0
+#define AKV_EINVAL (-1)    /* invalid argument or configuration */
+#define AKV_ERANGE (-2)    /* token range outside [0, n_logical) */
+#define AKV_ENOSEQ (-3)    /* unknown or freed sequence id */
+#define AKV_ENOPAGES (-4)  /* the page pool has too few free pages */
+#define AKV_ECAPACITY (-5) /* a per-sequence or per-call capacity is exceeded */
+#define AKV_ECUDA (-6)     /* a CUDA runtime call failed */
+#define AKV_EDEVICE (-7)   /* a kernel reported an inconsistency */
+
+#define AKV_DTYPE_BF16 0
+#define AKV_DTYPE_FP32 1
+
+/* Device error word bits (akv_sync_errors). */
+#define AKV_DERR_PAGE 0x1u     /* a page id outside the pool was met */
+#define AKV_DERR_INDEX 0x2u    /* a slot/index outside its array was met */
+#define AKV_DERR_WAIT 0x4u     /* a bounded wait gave up (pipeline stalled) */
+#define AKV_DERR_COUNT 0x8u    /* a device count disagreed with the host plan */
+
+typedef struct akv_config {
+  int32_t layers;      /* logical transformer layers (>= 1) */
+  int32_t phys_layers; /* K/V slabs held in the pool; logical layer l uses
+                          slab l % phys_layers.  0 means == layers. */
+  int32_t hq;          /* query heads (multiple of hkv; hq/hkv <= 16) */
+  int32_t hkv;         /* key/value heads */
+  int32_t head_dim;    /* 64 or 128 */
+  int32_t page_size;   /* tokens per page: 1, 2, 4, 8, 16, 32 or 64 */
+  int32_t dtype;       /* AKV_DTYPE_BF16 or AKV_DTYPE_FP32 (pool and inputs) */
+  int32_t max_pages;   /* pages in the pool */
+  int32_t max_seqs;    /* sequences alive at the same time */
+  int32_t max_slots;   /* held tokens per sequence (positions stay below) */
+  double rope_theta;   /* RoPE base */
+} akv_config;
+
+typedef struct akv_cache akv_cache;
+
+typedef struct akv_seq_info_t {
+  int64_t n_logical;      /* tokens ever appended (logical indices 0..n-1) */
+  int64_t n_held;         /* tokens held since the last reposition */
+  int64_t n_active;       /* held tokens not dropped */
+  int64_t next_pos;       /* position of the next append (== n_held) */
+  int32_t n_pages;        /* pages spanned by the held slots */
+  int32_t n_active_pages; /* pages holding at least one active token */
+  int32_t n_owned_pages;  /* pages referenced only by this sequence */
+  int32_t n_shared_pages; /* pages also referenced by another sequence */
+} akv_seq_info_t;
+
+/* Bytes of ONE pool (the K pool and the V pool have the same size):
+ * phys_layers * max_pages * hkv * page_size * head_dim * sizeof(dtype).
+ * Pool layout: [phys_layer][page][kv_head][slot_in_page][head_dim],
+ * so one (page, head) tile is page_size*head_dim contiguous elements.
+ * Returns 0 for an invalid configuration. */
+size_t akv_pool_bytes(const akv_config* cfg);
+
+/* Creates a cache over caller-owned K and V pools (device, akv_pool_bytes
+ * each, 256-byte aligned; contents need not be initialised).  The library
+ * allocates its own metadata, RoPE table and workspace on the device and
+ * keeps host state; the pools stay the caller's and must outlive the cache.
+ * `stream` is a cudaStream_t (NULL = legacy default stream).  Validates the
+ * configuration (AKV_EINVAL) and allocations (AKV_ECUDA). */
+int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool,
+                     size_t pool_bytes, void* stream, akv_cache** out);
+
+/* Waits for the cache's stream, then frees what the library allocated. */
+int akv_cache_destroy(akv_cache* cache);
+
+/* Later calls enqueue on `stream`.  The caller orders it after the old one. */
+int akv_set_stream(akv_cache* cache, void* stream);
+
+/* A new, empty sequence.  AKV_ECAPACITY when max_seqs are alive. */
+int akv_seq_create(akv_cache* cache, int64_t* seq);
+
+/* A branch of `parent`: same tokens, positions, drops and history; every
+ * page is shared (reference counted).  Pages are copied only when a branch
+ * writes into a shared partly filled page (append) -- reposition always
+ * writes fresh pages, so a shared page is never written (paper review,
+ * 4.2.3: a reposition by one request makes a new version; others keep the
+ * old one). */
+int akv_seq_fork(akv_cache* cache, int64_t parent, int64_t* child);
+
+/* Releases the sequence's page references (pages are reused at zero). */
+int akv_seq_free(akv_cache* cache, int64_t seq);
+
+/* Eq. (3), append: for each i < n_seqs, appends n_tokens[i] tokens to
+ * seqs[i] at positions next_pos.. (K is rotated to its position here).
+ *   k_raw, v : device, [layers][T][hkv][head_dim] in the pool dtype, with
+ *              T = sum(n_tokens) and the tokens of seqs[0], seqs[1], ... in
+ *              order; k_raw is the key BEFORE RoPE.  Logical layer l is
+ *              written to slab l % phys_layers (aliased layers: the last
+ *              logical layer of a slab wins).
+ *   token_ids: host, [T] or NULL; only enters the history key.
+ * Keys are computed in fp32 from the table cos/sin(p f_i) (fp64 -> fp32)
+ * and stored rounded to nearest even.  A sequence may appear once per call.
+ * Errors: AKV_ENOSEQ, AKV_ECAPACITY (max_slots), AKV_ENOPAGES. */
+int akv_append(akv_cache* cache, const int64_t* seqs, const int32_t* n_tokens,
+               int32_t n_seqs, const void* k_raw, const void* v,
+               const int32_t* token_ids);
+
+/* Eq. (4), drop: removes logical indices in the half-open ranges
+ * ranges[2i]..ranges[2i+1] (host, n_ranges pairs) from all later attention.
+ * Overlapping, repeated or already dropped indices are allowed (P is a
+ * set).  Nothing moves: positions and next_pos are unchanged.  A full page
+ * left with no active token loses this sequence's reference.
+ * Errors: AKV_ERANGE (begin < 0, end < begin or end > n_logical). */
+int akv_drop(akv_cache* cache, int64_t seq, const int64_t* ranges,
+             int32_t n_ranges);
+
+/* Eq. (5), reposition, batched over n_seqs sequences (host ids): the r
+ * active tokens of each move, in logical order, to slots/positions 0..r-1;
+ * each key is re-rotated by K' = R(q) R(p)^-1 K = R(q - p) K in fp32 (a key
+ * whose position does not change is copied bit for bit) and V is copied;
+ * next_pos becomes r.  The gather map is the exclusive prefix sum of the
+ * keep mask.  Leading pages whose every slot stays put keep their page id
+ * (and stay shared); all other survivors are written to fresh pages, and
+ * the old pages lose this sequence's reference.  A sequence with nothing
+ * dropped since it was last dense only gets a history record.
+ * Errors: AKV_ENOSEQ, AKV_EINVAL (repeated id), AKV_ENOPAGES. */
+int akv_reposition(akv_cache* cache, const int64_t* seqs, int32_t n_seqs);
+
+/* Decode attention of one layer over the active tokens only:
+ *   q   : device, [n_seqs][hq][head_dim] pool dtype, BEFORE RoPE; it is
+ *         rotated to next_pos - 1 (the position of the last appended token).
+ *   seqs: host, [n_seqs] sequence ids.
+ *   out : device, [n_seqs][hq][head_dim] fp32,
+ *         out = softmax(q' K^T / sqrt(D)) V over active tokens; query head h
+ *         reads KV head h / (hq/hkv).  A sequence with no active token gets 0.
+ * Split-KV over pages with a library-owned partial workspace, then a merge.
+ * Errors: AKV_ENOSEQ, AKV_EINVAL (layer), AKV_ECAPACITY (work items). */
+int akv_decode_attention(akv_cache* cache, int32_t layer, const void* q,
+                         const int64_t* seqs, int32_t n_seqs, float* out);
+
+/* ---- introspection (tests, tools): these wait for the cache's stream ---- */
+
+int akv_seq_info(akv_cache* cache, int64_t seq, akv_seq_info_t* info);
+
+/* Host outputs of n_held entries: position of each held slot, whether it is
+ * active (device keep mask), and its logical index. */
+int akv_seq_positions(akv_cache* cache, int64_t seq, int32_t* pos);
+int akv_seq_keep_mask(akv_cache* cache, int64_t seq, uint8_t* keep);
+int akv_seq_logical(akv_cache* cache, int64_t seq, int64_t* logical);
+
+/* Gather map of the sequence's last reposition: map[j] = old slot of the
+ * token now in slot j (host, n entries; *n is set even if map is NULL). */
+int akv_seq_gather_map(akv_cache* cache, int64_t seq, int32_t* map, int64_t* n);
+
+/* Device page table (pool page id per slot page, -1 once released) and the
+ * device active page list (slot-page indices, ascending).  Host outputs; a
+ * NULL output is skipped; counts are always set. */
+int akv_seq_page_table(akv_cache* cache, int64_t seq, int32_t* pages,
+                       int32_t* n_pages, int32_t* active, int32_t* n_active);
+
+/* 128-bit key of the sequence's operation history (Eq. 6): equal histories
+ * give equal keys; different ones differ (with overwhelming probability).
+ * One record per appended token (its id, or none), one per non-empty drop
+ * (its sorted, merged ranges), one per reposition. */
+int akv_history_key(akv_cache* cache, int64_t seq, uint64_t key[2]);
+
+/* Reference count of a pool page (0 = free) and pool occupancy. */
+int akv_page_refcount(akv_cache* cache, int32_t page, int32_t* refcount);
+int akv_pool_stats(akv_cache* cache, int32_t* free_pages, int32_t* used_pages);
+
+/* Message of the last error on this cache (static storage of the cache). */
+const char* akv_last_error(akv_cache* cache);
+
+/* Waits for the stream and returns (then clears) the device error word
+ * (AKV_DERR_* bits).  Returns AKV_EDEVICE when it was non-zero. */
+int akv_sync_errors(akv_cache* cache, uint32_t* word);
+
+/* Iteration limit of every bounded device wait (default 1<<22 polls). */
+int akv_set_wait_limit(akv_cache* cache, uint32_t polls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AKV_H */

@@ -1,0 +1,275 @@
+"""CUDA library vs the CPU oracle, element by element, through the C ABI.
+
+Sizes are ones the oracle finishes in seconds while still spanning several
+pages/tiles with ragged tails; the full-size workloads are covered by
+``test_gpu_fullsize.py``.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from agent_kv_cache_gb300 import abi, build
+from workloads import traces
+from twin import Twin
+
+pytestmark = pytest.mark.gpu
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build()
+    abi.lib()
+
+
+def test_tiny_workload():
+    """1 layer, 8/2 heads, D 64, fp32, 512 tokens, 3 seeded spans dropped,
+    reposition, then one decode step."""
+    spans = traces.tiny_spans(traces.seed_for(0))
+    t = Twin(layers=1, hq=8, hkv=2, head_dim=64, page_size=16, dtype="fp32",
+             rope_theta=1e4, max_pages=96, max_seqs=2, max_slots=1024,
+             seed=traces.seed_for(0))
+    s = t.create()
+    t.append([s], [512])
+    t.check(s)
+    t.drop(s, spans)
+    t.check(s)
+    t.reposition([s])
+    t.check(s)
+    t.append([s], [1])
+    t.check(s)
+    t.decode([s], 0)
+
+
+def test_fig10_positions_through_library():
+    g = json.load(open(os.path.join(GOLD, "fig10_positions.json")))
+    t = Twin(page_size=1, max_pages=64, max_slots=64)
+    s = t.create()
+    name_of = {}
+    for op in g["ops"]:
+        if op[0] == "append":
+            name_of[t.gpu.info(s)["n_logical"]] = op[1]
+            t.append([s], [1])
+        elif op[0] == "drop":
+            idx = {n: i for i, n in name_of.items()}
+            t.drop(s, [(idx[n], idx[n] + 1) for n in op[1]])
+        elif op[0] == "repos":
+            t.reposition([s])
+        else:
+            keep = t.gpu.keep_mask(s)
+            seen = {name_of[int(l)]: int(p) for l, p, a in
+                    zip(t.gpu.logical(s), t.gpu.positions(s), keep) if a}
+            assert seen == op[2]
+            assert t.gpu.info(s)["next_pos"] - 1 == op[2][op[1]]
+        t.check(s)
+    t.decode([s], 0)
+
+
+CONFIGS = [
+    # dtype, page, G, D
+    ("bf16", 16, 4, 128),
+    ("bf16", 16, 8, 64),
+    ("bf16", 16, 1, 128),
+    ("bf16", 1, 4, 64),
+    ("bf16", 64, 2, 128),
+    ("fp32", 16, 4, 64),
+    ("fp32", 4, 16, 128),
+]
+
+
+@pytest.mark.parametrize("dtype,page,G,D", CONFIGS)
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_random_operation_sequences(dtype, page, G, D, seed):
+    rng = np.random.default_rng(1000 * seed + page + G + D)
+    hkv = 2
+    t = Twin(layers=2, hq=hkv * G, hkv=hkv, head_dim=D, page_size=page, dtype=dtype,
+             rope_theta=1e4 if D == 64 else 5e5, max_pages=2048, max_seqs=8,
+             max_slots=1024, seed=seed)
+    seqs = [t.create()]
+    t.append(seqs, [int(rng.integers(1, 200))])
+    step = 0
+    for _ in range(10):
+        g = seqs[int(rng.integers(0, len(seqs)))]
+        op = rng.choice(["append", "drop", "drop", "repos", "fork", "decode"])
+        n = t.gpu.info(g)["n_logical"]
+        if op == "append":
+            t.append([g], [int(rng.integers(1, 120))])
+        elif op == "drop" and n:
+            rs = []
+            for _ in range(int(rng.integers(1, 4))):
+                b = int(rng.integers(0, n))
+                rs.append((b, int(rng.integers(b, min(n, b + 90) + 1))))
+            t.drop(g, rs)
+        elif op == "repos":
+            t.reposition([g])
+        elif op == "fork" and len(seqs) < 6:
+            seqs.append(t.fork(g))
+        elif op == "decode":
+            t.append(seqs, [1] * len(seqs))
+            t.decode(seqs, step)
+            step += 1
+        for s in seqs:
+            t.check(s)
+    t.append(seqs, [1] * len(seqs))
+    t.decode(seqs, step)
+
+
+def test_batched_reposition_and_decode():
+    t = Twin(layers=3, hq=16, hkv=4, head_dim=128, page_size=16, dtype="bf16",
+             rope_theta=5e5, max_pages=4096, max_seqs=8, max_slots=4096)
+    seqs = [t.create() for _ in range(5)]
+    t.append(seqs, [700, 1, 16, 333, 1500])
+    t.drop(seqs[0], [(0, 100), (300, 500)])
+    t.drop(seqs[1], [(0, 1)])
+    t.drop(seqs[3], [(5, 6), (40, 41), (100, 332)])
+    t.drop(seqs[4], [(1024, 1500)])
+    t.reposition(seqs)
+    for s in seqs:
+        t.check(s)
+    t.append(seqs, [1] * 5)
+    t.decode(seqs, 0)
+    t.drop(seqs[2], [(0, 17)])           # every token of seq 2 dropped
+    t.append(seqs[:2] + seqs[3:], [1] * 4)
+    for s in seqs:
+        t.check(s)
+    t.decode(seqs, 1)                    # seq 2 has nothing active: zeros
+
+
+def _history(t, ops, toks):
+    s = t.create()
+    names = {}
+    for op in ops:
+        if op[0] == "append":
+            names[op[1]] = t.gpu.info(s)["n_logical"]
+            t.append([s], [1], token_ids=[toks[op[1]]])
+        elif op[0] == "drop":
+            t.drop(s, [(names[n], names[n] + 1) for n in op[1]])
+        else:
+            t.reposition([s])
+    return s
+
+
+def test_history_keys_figure5_and_figure11():
+    g = json.load(open(os.path.join(GOLD, "fig5_histories.json")))
+    t = Twin(page_size=1, max_pages=256, max_seqs=16, max_slots=64)
+    seqs = {name: _history(t, ops, g["tokens"]) for name, ops in g["paths"].items()}
+    keys = {name: t.gpu.history_key(s) for name, s in seqs.items()}
+    assert len(set(keys.values())) == len(keys), keys
+    again = _history(t, g["paths"]["fig5_2"], g["tokens"])
+    assert t.gpu.history_key(again) == keys["fig5_2"]
+
+
+def test_history_key_equality_matches_operation_logs():
+    rng = np.random.default_rng(7)
+    t = Twin(page_size=4, max_pages=4096, max_seqs=64, max_slots=256)
+    seqs = []
+    for i in range(40):
+        s = t.create()
+        for _ in range(int(rng.integers(1, 5))):
+            op = int(rng.integers(0, 3))
+            n = t.gpu.info(s)["n_logical"]
+            if op == 0 or n == 0:
+                k = int(rng.integers(1, 3))
+                t.append([s], [k], token_ids=list(rng.integers(0, 2, size=k)))
+            elif op == 1:
+                b = int(rng.integers(0, n))
+                t.drop(s, [(b, b + 1)])
+            else:
+                t.reposition([s])
+        seqs.append(s)
+    for a in seqs:
+        for b in seqs:
+            same_log = t.orc.history(t.o[a]) == t.orc.history(t.o[b])
+            assert t.history_equal(a, b) == same_log
+    # appending n tokens at once == n appends of one
+    a, b = t.create(), t.create()
+    t.append([a], [5], token_ids=[1, 2, 3, 4, 5])
+    t.append([b], [2], token_ids=[1, 2])
+    t.append([b], [3], token_ids=[3, 4, 5])
+    assert t.history_equal(a, b)
+
+
+def test_copy_on_write_isolation():
+    t = Twin(layers=2, hq=8, hkv=2, head_dim=64, page_size=16, dtype="bf16",
+             rope_theta=1e4, max_pages=512, max_seqs=8, max_slots=2048)
+    base = t.create()
+    t.append([base], [203])                     # ragged: tail page partly filled
+    pages0, _ = t.gpu.page_table(base)
+    snap_k = t.gpu.k_pool[:, torch.from_numpy(pages0.astype(np.int64)).cuda()].clone()
+    snap_v = t.gpu.v_pool[:, torch.from_numpy(pages0.astype(np.int64)).cuda()].clone()
+    kids = [t.fork(base) for _ in range(3)]
+    for p in pages0:
+        assert t.gpu.refcount(int(p)) == 4
+    t.drop(kids[0], [(40, 90)])
+    t.reposition([kids[0]])
+    t.append([kids[1]], [30])                   # writes into the shared tail: copy-on-write
+    t.drop(kids[2], [(0, 5)])
+    t.reposition([kids[2]])
+    t.append(kids, [1, 1, 1])
+    for s in [base] + kids:
+        t.check(s)
+    idx = torch.from_numpy(pages0.astype(np.int64)).cuda()
+    assert torch.equal(t.gpu.k_pool[:, idx], snap_k)
+    assert torch.equal(t.gpu.v_pool[:, idx], snap_v)
+    # kept prefix of kids[0] (pages before the first drop) is still shared
+    p0, _ = t.gpu.page_table(kids[0])
+    assert list(p0[:2]) == list(pages0[:2])
+    t.decode([base] + kids, 0)
+    for s in kids + [base]:
+        t.free(s)
+    free, used = t.gpu.pool_stats()
+    assert used == 0 and free == 512
+
+
+def test_errors_leave_state_unchanged():
+    t = Twin(layers=1, hq=4, hkv=2, head_dim=64, page_size=16, dtype="bf16",
+             rope_theta=1e4, max_pages=10, max_seqs=2, max_slots=200)
+    s = t.create()
+    t.append([s], [100])
+
+    def snapshot():
+        return (t.gpu.info(s), t.gpu.keep_mask(s).tolist(), t.gpu.page_table(s)[0].tolist(),
+                t.gpu.history_key(s), t.gpu.pool_stats())
+
+    before = snapshot()
+    for bad in ([(0, 101)], [(-1, 3)], [(7, 3)]):
+        with pytest.raises(abi.AkvError) as e:
+            t.gpu.drop(s, bad)
+        assert e.value.code == abi.AKV_ERANGE
+    with pytest.raises(abi.AkvError) as e:
+        t.gpu.drop(12345, [(0, 1)])
+    assert e.value.code == abi.AKV_ENOSEQ
+    k = torch.zeros((1, 120, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(abi.AkvError) as e:        # 100 + 120 > max_slots
+        t.gpu.append([s], [120], k, k)
+    assert e.value.code == abi.AKV_ECAPACITY
+    k = torch.zeros((1, 90, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(abi.AkvError) as e:        # needs 5 more pages, 3 free
+        t.gpu.append([s], [90], k, k)
+    assert e.value.code == abi.AKV_ENOPAGES
+    t2 = t.create()
+    with pytest.raises(abi.AkvError) as e:        # max_seqs == 2
+        t.gpu.seq_create()
+    assert e.value.code == abi.AKV_ECAPACITY
+    t.free(t2)
+    with pytest.raises(abi.AkvError) as e:
+        t.gpu.reposition([s, s])
+    assert e.value.code == abi.AKV_EINVAL
+    # reposition needing more pages than are free is refused as a whole
+    t.drop(s, [(0, 1)])
+    before = snapshot()
+    other = t.create()
+    t.append([other], [40])                      # leaves 10 - 7 - 3 = 0 free
+    with pytest.raises(abi.AkvError) as e:
+        t.gpu.reposition([s])
+    assert e.value.code == abi.AKV_ENOPAGES
+    assert snapshot()[:4] == before[:4]
+    t.check(s)
+    t.free(other)
+    t.reposition([s])
+    t.check(s)
+

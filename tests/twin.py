@@ -1,0 +1,174 @@
+"""Drive the CUDA library and the CPU oracle with the same seeded inputs.
+
+Inputs come from ``workloads.synth`` only (values exact in the pool dtype);
+the oracle never sees anything produced by the CUDA path.
+
+Tolerances (derived from the arithmetic):
+
+* indices, keep masks, positions, gather maps, active page lists: bit-exact;
+* V: bit-exact (it is only copied);
+* K: every stored key went through r rotations (the append plus each
+  reposition that moved it).  The library rotates in fp32 with cos/sin
+  table entries rounded once from fp64, so one rotation of a pair (x, y)
+  is off the exact value by at most about 4 * 2^-24 * |(x, y)| before the
+  final rounding to the pool dtype.  The oracle rounds the exact value to
+  the pool dtype.  Per element the test allows
+      r * (ulp(ref) + 8 * 2^-24 * |(x, y)|),
+  which is the "within 1 ulp of the oracle rounded to bf16" bound for each
+  rounding step, widened only where a component is tiny next to its pair's
+  norm (there fp32 cancellation decides the last bits).
+* attention output (fp32): max abs error <= 1e-2 and mean abs error <= 1e-3
+  for bf16 pools; 1e-4 / 1e-5 for fp32 pools.
+"""
+import numpy as np
+import torch
+
+from agent_kv_cache_gb300 import Cache
+from oracle.akv_oracle import OracleCache
+from workloads import synth
+
+ATTN_TOL = {"bf16": (1e-2, 1e-3), "fp32": (1e-4, 1e-5)}
+
+
+def ulp(x, dtype):
+    """Spacing of the pool dtype at |x| (x float64)."""
+    bits = 8 if dtype == "bf16" else 24
+    ax = np.maximum(np.abs(x), 2.0 ** -100)
+    return 2.0 ** (np.floor(np.log2(ax)) - (bits - 1))
+
+
+def key_tolerance(ref, dtype, n_rot):
+    d = ref.shape[-1]
+    h = d // 2
+    norm = np.sqrt(ref[..., :h] ** 2 + ref[..., h:] ** 2)
+    norm = np.concatenate([norm, norm], axis=-1)
+    return max(n_rot, 1) * (ulp(ref, dtype) + 8 * 2.0 ** -24 * norm)
+
+
+class Twin:
+    def __init__(self, layers=1, hq=8, hkv=2, head_dim=64, page_size=16, dtype="fp32",
+                 rope_theta=1e4, max_pages=256, max_seqs=8, max_slots=2048, seed=1,
+                 phys_layers=0):
+        self.gpu = Cache(layers, hq, hkv, head_dim, page_size, dtype, max_pages, max_seqs,
+                         max_slots, rope_theta, phys_layers=phys_layers)
+        self.orc = OracleCache(hq, hkv, head_dim, rope_theta, dtype, layers=range(layers),
+                               page_size=page_size)
+        self.L, self.hq, self.hkv, self.d, self.S = layers, hq, hkv, head_dim, page_size
+        self.dtype = dtype
+        self.width = synth.width_for(dtype)
+        self.seed = seed
+        self.o = {}        # gpu seq id -> oracle seq id
+        self.tag = {}      # gpu seq id -> input stream tag
+        self.rot = {}      # gpu seq id -> rotations a key may have gone through
+        self.next_tag = 1
+        self.tdtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+
+    # -- operations on both sides -----------------------------------------
+    def create(self):
+        g = self.gpu.seq_create()
+        self.o[g] = self.orc.create()
+        self.tag[g] = self.next_tag
+        self.next_tag += 1
+        self.rot[g] = 1
+        return g
+
+    def fork(self, parent):
+        g = self.gpu.seq_fork(parent)
+        self.o[g] = self.orc.fork(self.o[parent])
+        self.tag[g] = self.next_tag
+        self.next_tag += 1
+        self.rot[g] = self.rot[parent]
+        return g
+
+    def free(self, g):
+        self.gpu.seq_free(g)
+        self.orc.free(self.o.pop(g))
+
+    def _kv(self, g, n):
+        t0 = self.orc.seqs[self.o[g]].n_logical
+        k = synth.kv_tokens(self.seed, self.tag[g], synth.KIND_K, range(self.L), t0, n,
+                            self.hkv, self.d, self.width)
+        v = synth.kv_tokens(self.seed, self.tag[g], synth.KIND_V, range(self.L), t0, n,
+                            self.hkv, self.d, self.width)
+        return k, v
+
+    def append(self, seqs, ns, token_ids=None):
+        ks, vs = [], []
+        for g, n in zip(seqs, ns):
+            k, v = self._kv(g, n)
+            ks.append(k)
+            vs.append(v)
+        tok = 0
+        for g, n, k, v in zip(seqs, ns, ks, vs):
+            ids = None if token_ids is None else token_ids[tok:tok + n]
+            self.orc.append(self.o[g], k, v, ids)
+            tok += n
+        kt = torch.from_numpy(np.concatenate(ks, axis=1)).to(self.tdtype).cuda().contiguous()
+        vt = torch.from_numpy(np.concatenate(vs, axis=1)).to(self.tdtype).cuda().contiguous()
+        self.gpu.append(list(seqs), list(ns), kt, vt, token_ids)
+        torch.cuda.synchronize()
+
+    def drop(self, g, ranges):
+        self.gpu.drop(g, ranges)
+        self.orc.drop(self.o[g], ranges)
+
+    def reposition(self, seqs):
+        self.gpu.reposition(list(seqs))
+        for g in seqs:
+            st = self.orc.seqs[self.o[g]]
+            if not (st.alive.all() and np.array_equal(st.pos, np.arange(st.alive.size))):
+                self.rot[g] += 1
+            self.orc.reposition(self.o[g])
+
+    def decode(self, seqs, step, layers=None):
+        """Decode attention for every layer; returns the max/mean abs errors."""
+        layers = range(self.L) if layers is None else layers
+        worst = (0.0, 0.0)
+        for l in layers:
+            q = np.stack([synth.query(self.seed, self.tag[g], l, step, self.hq, self.d,
+                                      self.width) for g in seqs])
+            out = self.gpu.decode_attention(l, torch.from_numpy(q).to(self.tdtype).cuda(),
+                                            list(seqs))
+            got = out.double().cpu().numpy()
+            want = self.orc.attention(l, q, [self.o[g] for g in seqs])
+            err = np.abs(got - want)
+            worst = (max(worst[0], err.max()), max(worst[1], err.mean()))
+            tmax, tmean = ATTN_TOL[self.dtype]
+            assert err.max() <= tmax and err.mean() <= tmean, (l, err.max(), err.mean())
+        return worst
+
+    # -- comparison --------------------------------------------------------
+    def check(self, g, kv=True):
+        o = self.orc.seqs[self.o[g]]
+        info = self.gpu.info(g)
+        want = self.orc.info(self.o[g])
+        for k in ("n_logical", "n_held", "next_pos", "n_pages", "n_active_pages"):
+            assert info[k] == want[k], (k, info[k], want[k])
+        assert info["n_active"] == want["n_alive"]
+        n = info["n_held"]
+        np.testing.assert_array_equal(self.gpu.keep_mask(g), o.alive)
+        np.testing.assert_array_equal(self.gpu.logical(g), o.logical)
+        np.testing.assert_array_equal(self.gpu.positions(g), o.pos)
+        pages, act = self.gpu.page_table(g)
+        np.testing.assert_array_equal(act, self.orc.active_pages(self.o[g]))
+        assert len(pages) == -(-n // self.S)
+        # every page with an active token is a valid pool page
+        for k in act:
+            assert 0 <= pages[k] < self.gpu.cfg.max_pages
+            assert self.gpu.refcount(int(pages[k])) >= 1
+        if o.last_gather is not None:
+            np.testing.assert_array_equal(self.gpu.gather_map(g), o.last_gather)
+        if kv and n:
+            live = np.array([pages[s // self.S] >= 0 for s in range(n)])
+            for l in range(self.L):
+                k, v = self.gpu.read_kv(g, l)
+                ref_k = o.K[l][live]
+                tol = key_tolerance(ref_k, self.dtype, self.rot[g])
+                err = np.abs(k[live] - ref_k)
+                bad = err > tol
+                assert not bad.any(), (l, err[bad][:5], ref_k[bad][:5], tol[bad][:5])
+                np.testing.assert_array_equal(v[live], o.V[l][live])
+        assert self.gpu.sync_errors() == 0
+
+    def history_equal(self, a, b):
+        return self.gpu.history_key(a) == self.gpu.history_key(b)
