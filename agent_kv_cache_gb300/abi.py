@@ -90,6 +90,7 @@ SIGNATURES = {
     "akv_pool_stats": (ctypes.c_int, [_P, _PI32, _PI32]),
     "akv_last_error": (ctypes.c_char_p, [_P]),
     "akv_sync_errors": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "akv_kernel_launches": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "akv_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint32]),
 }
 
@@ -266,6 +267,12 @@ def akv_sync_errors(cache):
     if rc not in (AKV_OK, AKV_EDEVICE):
         _check(rc, cache)
     return w.value
+
+
+def akv_kernel_launches(cache):
+    n = ctypes.c_uint64()
+    _check(lib().akv_kernel_launches(cache, ctypes.byref(n)), cache)
+    return n.value
 
 
 def akv_set_wait_limit(cache, polls):

@@ -102,6 +102,9 @@ class Cache:
     def pool_stats(self):
         return abi.akv_pool_stats(self.handle)
 
+    def kernel_launches(self):
+        return abi.akv_kernel_launches(self.handle)
+
     def sync_errors(self):
         return abi.akv_sync_errors(self.handle)
 

@@ -162,6 +162,7 @@ struct akv_cache {
   std::string err;
   uint32_t wait_limit = 1u << 22;
   int sm_count = 148;
+  uint64_t launches = 0;
 };
 
 namespace {
@@ -562,9 +563,12 @@ int akv_append(akv_cache* c, const int64_t* seqs, const int32_t* n_tokens, int32
   }
   ++c->epoch;
 
-  if (!cow.empty())
+  if (!cow.empty()) {
     CK(launch_copy_pages(c->g, reinterpret_cast<const PagePair*>(d + o_cow), (int)cow.size(),
                          c->d_err, c->stream));
+    ++c->launches;
+  }
+  ++c->launches;
   CK(launch_append(c->g, c->sa, reinterpret_cast<const AppendItem*>(d + o_items),
                    reinterpret_cast<const AppendBlock*>(d + o_blocks), (int)blocks.size(),
                    reinterpret_cast<const int32_t*>(d + o_ids),
@@ -635,6 +639,7 @@ int akv_drop(akv_cache* c, int64_t seq, const int64_t* ranges, int32_t n_ranges)
   ++c->epoch;
   CK(launch_drop(c->g, c->sa, reinterpret_cast<const DropItem*>(d + o_item), 1,
                  reinterpret_cast<const int32_t*>(d + o_r), c->d_err, c->stream));
+  ++c->launches;
   return AKV_OK;
 }
 
@@ -745,6 +750,7 @@ int akv_reposition(akv_cache* c, const int64_t* seqs, int32_t n_seqs) {
                       c->stream));
     CK(launch_gather(c->g, c->sa, reinterpret_cast<const ReposItem*>(d + o_items),
                      (int)items.size(), blocks, c->d_cs, c->d_err, c->stream));
+    c->launches += blocks > 0 ? 2 : 1;
   }
   return AKV_OK;
 }
@@ -830,6 +836,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   CK(launch_decode(a, c->plan_combine, n_seqs,
                    reinterpret_cast<const int32_t*>(c->d_plan + o_item0),
                    reinterpret_cast<const int32_t*>(c->d_plan + o_splits), c->stream));
+  c->launches += c->plan_combine ? 2 : 1;
   return AKV_OK;
 }
 
@@ -953,6 +960,12 @@ int akv_sync_errors(akv_cache* c, uint32_t* word) {
   CK(cudaMemset(c->d_err, 0, sizeof(w)));
   if (word) *word = w;
   return w ? fail(c, AKV_EDEVICE, "device error word 0x%x", w) : AKV_OK;
+}
+
+int akv_kernel_launches(akv_cache* c, uint64_t* count) {
+  if (!c || !count) return AKV_EINVAL;
+  *count = c->launches;
+  return AKV_OK;
 }
 
 int akv_set_wait_limit(akv_cache* c, uint32_t polls) {

@@ -210,6 +210,9 @@ const char* akv_last_error(akv_cache* cache);
  * (AKV_DERR_* bits).  Returns AKV_EDEVICE when it was non-zero. */
 int akv_sync_errors(akv_cache* cache, uint32_t* word);
 
+/* Number of kernels this cache has launched since creation. */
+int akv_kernel_launches(akv_cache* cache, uint64_t* count);
+
 /* Iteration limit of every bounded device wait (default 1<<22 polls). */
 int akv_set_wait_limit(akv_cache* cache, uint32_t polls);
 

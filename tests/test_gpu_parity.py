@@ -227,9 +227,9 @@ def test_copy_on_write_isolation():
 
 def test_errors_leave_state_unchanged():
     t = Twin(layers=1, hq=4, hkv=2, head_dim=64, page_size=16, dtype="bf16",
-             rope_theta=1e4, max_pages=10, max_seqs=2, max_slots=200)
+             rope_theta=1e4, max_pages=16, max_seqs=2, max_slots=400)
     s = t.create()
-    t.append([s], [100])
+    t.append([s], [100])                          # 7 pages, 9 free
 
     def snapshot():
         return (t.gpu.info(s), t.gpu.keep_mask(s).tolist(), t.gpu.page_table(s)[0].tolist(),
@@ -243,13 +243,13 @@ def test_errors_leave_state_unchanged():
     with pytest.raises(abi.AkvError) as e:
         t.gpu.drop(12345, [(0, 1)])
     assert e.value.code == abi.AKV_ENOSEQ
-    k = torch.zeros((1, 120, 2, 64), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(abi.AkvError) as e:        # 100 + 120 > max_slots
-        t.gpu.append([s], [120], k, k)
+    k = torch.zeros((1, 320, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(abi.AkvError) as e:        # 100 + 320 > max_slots
+        t.gpu.append([s], [320], k, k)
     assert e.value.code == abi.AKV_ECAPACITY
-    k = torch.zeros((1, 90, 2, 64), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(abi.AkvError) as e:        # needs 5 more pages, 3 free
-        t.gpu.append([s], [90], k, k)
+    k = torch.zeros((1, 200, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(abi.AkvError) as e:        # needs 12 more pages, 9 free
+        t.gpu.append([s], [200], k, k)
     assert e.value.code == abi.AKV_ENOPAGES
     t2 = t.create()
     with pytest.raises(abi.AkvError) as e:        # max_seqs == 2
@@ -259,17 +259,21 @@ def test_errors_leave_state_unchanged():
     with pytest.raises(abi.AkvError) as e:
         t.gpu.reposition([s, s])
     assert e.value.code == abi.AKV_EINVAL
-    # reposition needing more pages than are free is refused as a whole
+    assert snapshot() == before
+    t.check(s)
+    # a reposition needing more fresh pages than are free is refused as a whole
+    # (the fresh pages are taken before the old ones are released)
     t.drop(s, [(0, 1)])
     before = snapshot()
     other = t.create()
-    t.append([other], [40])                      # leaves 10 - 7 - 3 = 0 free
+    t.append([other], [96])                       # 6 pages: 3 left free
     with pytest.raises(abi.AkvError) as e:
-        t.gpu.reposition([s])
+        t.gpu.reposition([s])                     # needs 7
     assert e.value.code == abi.AKV_ENOPAGES
     assert snapshot()[:4] == before[:4]
     t.check(s)
     t.free(other)
     t.reposition([s])
     t.check(s)
-
+    t.free(s)
+    assert t.gpu.pool_stats() == (16, 0)

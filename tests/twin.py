@@ -7,16 +7,19 @@ Tolerances (derived from the arithmetic):
 
 * indices, keep masks, positions, gather maps, active page lists: bit-exact;
 * V: bit-exact (it is only copied);
-* K: every stored key went through r rotations (the append plus each
-  reposition that moved it).  The library rotates in fp32 with cos/sin
-  table entries rounded once from fp64, so one rotation of a pair (x, y)
-  is off the exact value by at most about 4 * 2^-24 * |(x, y)| before the
-  final rounding to the pool dtype.  The oracle rounds the exact value to
-  the pool dtype.  Per element the test allows
-      r * (ulp(ref) + 8 * 2^-24 * |(x, y)|),
-  which is the "within 1 ulp of the oracle rounded to bf16" bound for each
-  rounding step, widened only where a component is tiny next to its pair's
-  norm (there fp32 cancellation decides the last bits).
+* K: every stored key went through r roundings to the pool dtype (the
+  append plus each reposition that moved it).  One rotation of a pair
+  (x, y) in fp32 with table cos/sin rounded once from fp64 is off the exact
+  value by at most about 4 * 2^-24 * |(x, y)| before the final rounding, so
+  a single step lands within 1 ulp of the oracle's RNE(exact) (the bound the
+  method states).  Over a chain, the two sides start each later rotation
+  from inputs that may differ by 1 ulp per component; a rotation preserves
+  the norm of that difference and spreads it over both components, so the
+  bound per element is
+      ulp(ref) + (r - 1) * sqrt(2) * 2^(1-p) * |(x, y)| + r * 8 * 2^-24 * |(x, y)|
+  (p = 8 significant bits for bf16, 24 for fp32; ulp(v) <= 2^(1-p) |v|).
+  Every element must meet it, and at least 99% of the elements must lie
+  within r ulp of the oracle (the per-step bound applied r times).
 * attention output (fp32): max abs error <= 1e-2 and mean abs error <= 1e-3
   for bf16 pools; 1e-4 / 1e-5 for fp32 pools.
 """
@@ -37,12 +40,26 @@ def ulp(x, dtype):
     return 2.0 ** (np.floor(np.log2(ax)) - (bits - 1))
 
 
-def key_tolerance(ref, dtype, n_rot):
-    d = ref.shape[-1]
-    h = d // 2
+def _pair_norm(ref):
+    h = ref.shape[-1] // 2
     norm = np.sqrt(ref[..., :h] ** 2 + ref[..., h:] ** 2)
-    norm = np.concatenate([norm, norm], axis=-1)
-    return max(n_rot, 1) * (ulp(ref, dtype) + 8 * 2.0 ** -24 * norm)
+    return np.concatenate([norm, norm], axis=-1)
+
+
+def key_tolerance(ref, dtype, n_rot):
+    """Per-element bound of a key that went through n_rot roundings."""
+    p = 8 if dtype == "bf16" else 24
+    r = max(n_rot, 1)
+    norm = _pair_norm(ref)
+    return (ulp(ref, dtype) + (r - 1) * np.sqrt(2.0) * 2.0 ** (1 - p) * norm
+            + r * 8 * 2.0 ** -24 * norm)
+
+
+def key_ulp_fraction(err, ref, dtype, n_rot):
+    """Fraction of elements within n_rot ulp of the oracle."""
+    r = max(n_rot, 1)
+    ok = err <= r * (ulp(ref, dtype) + 8 * 2.0 ** -24 * _pair_norm(ref))
+    return float(ok.mean()) if ok.size else 1.0
 
 
 class Twin:
@@ -167,6 +184,8 @@ class Twin:
                 err = np.abs(k[live] - ref_k)
                 bad = err > tol
                 assert not bad.any(), (l, err[bad][:5], ref_k[bad][:5], tol[bad][:5])
+                frac = key_ulp_fraction(err, ref_k, self.dtype, self.rot[g])
+                assert frac >= 0.99, (l, frac)
                 np.testing.assert_array_equal(v[live], o.V[l][live])
         assert self.gpu.sync_errors() == 0
 
