@@ -91,6 +91,9 @@ SIGNATURES = {
     "akv_last_error": (ctypes.c_char_p, [_P]),
     "akv_sync_errors": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "akv_kernel_launches": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
+    "akv_decode_attention_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                                    ctypes.c_double, _P, _P, _P, _I32, _I32,
+                                                    _PI32, _PI32, _P, _P, _I32, _P]),
     "akv_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint32]),
 }
 
@@ -273,6 +276,20 @@ def akv_kernel_launches(cache):
     n = ctypes.c_uint64()
     _check(lib().akv_kernel_launches(cache, ctypes.byref(n)), cache)
     return n.value
+
+
+def akv_decode_attention_noalloc(k_slab, v_slab, max_pages, hq, hkv, head_dim, page_size,
+                                 dtype, rope_theta, page_table, active_pages, keep_bits,
+                                 row_stride, keep_stride, n_active_pages, n_held, q, out,
+                                 stream=0):
+    """Decode attention over caller-owned metadata; allocates nothing (see akv.h)."""
+    na, pna = _arr(n_active_pages, np.int32, ctypes.c_int32)
+    nh, pnh = _arr(n_held, np.int32, ctypes.c_int32)
+    dt = AKV_DTYPE_BF16 if dtype in ("bf16", AKV_DTYPE_BF16) else AKV_DTYPE_FP32
+    _check(lib().akv_decode_attention_noalloc(
+        k_slab, v_slab, max_pages, hq, hkv, head_dim, page_size, dt, float(rope_theta),
+        page_table, active_pages, keep_bits, row_stride, keep_stride, pna, pnh, q, out,
+        len(na), stream or None))
 
 
 def akv_set_wait_limit(cache, polls):

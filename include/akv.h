@@ -173,6 +173,47 @@ int akv_reposition(akv_cache* cache, const int64_t* seqs, int32_t n_seqs);
 int akv_decode_attention(akv_cache* cache, int32_t layer, const void* q,
                          const int64_t* seqs, int32_t n_seqs, float* out);
 
+/* ---- decode attention that allocates nothing (no counterpart in the paper) ----
+ *
+ * For callers that cannot allocate device memory: applications that reserve
+ * all of their GPU memory once at start-up and forbid cudaMalloc/cudaFree
+ * while serving (those calls synchronise the device, can fail mid-request
+ * and fragment memory already planned), for example a plugin running inside
+ * another runtime's memory pool.  Such a caller cannot create an akv_cache,
+ * so this call takes only its own pointers and computes the same decode
+ * attention as akv_decode_attention() over metadata in the same layout:
+ *
+ *   k_slab, v_slab : device, one layer's slab [max_pages][hkv][page_size][D]
+ *   page_table     : device int32 [n_seqs][row_stride], pool page per slot page
+ *   active_pages   : device int32 [n_seqs][row_stride], ascending slot-page
+ *                    indices that hold an active token (first n_active_pages)
+ *   keep_bits      : device uint32 [n_seqs][keep_stride], bit s = slot s active
+ *   n_active_pages : host int32 [n_seqs]
+ *   n_held         : host int32 [n_seqs]; the query is rotated to n_held - 1
+ *   q, out         : device [n_seqs][hq][D] (pool dtype) / fp32
+ *
+ * The split-KV partial sums live in one file-scope device array of
+ * AKV_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading this library
+ * holds until the process exits; the call calls no cudaMalloc, cudaFree or
+ * other allocating routine.  Its first call on each device (with that device
+ * current) looks up the array's device address with cudaGetSymbolAddress;
+ * make that first call before any stream capture.  All calls share the
+ * array and it keeps the last call's contents (nothing in it needs to start
+ * at zero: a call writes every partial it reads), so calls that overlap on
+ * the GPU -- on different streams, or from several host threads -- race and
+ * must be serialised by the caller.  Splits are sized so the partials fit.
+ * Errors: AKV_ECAPACITY when n_seqs > AKV_NOALLOC_MAX_SEQS; AKV_EINVAL for
+ * a bad shape or pointer; AKV_ECUDA when a launch fails. */
+#define AKV_NOALLOC_SCRATCH_BYTES (8 << 20)
+#define AKV_NOALLOC_MAX_SEQS 256
+int akv_decode_attention_noalloc(
+    const void* k_slab, const void* v_slab, int32_t max_pages, int32_t hq,
+    int32_t hkv, int32_t head_dim, int32_t page_size, int32_t dtype,
+    double rope_theta, const int32_t* page_table, const int32_t* active_pages,
+    const uint32_t* keep_bits, int32_t row_stride, int32_t keep_stride,
+    const int32_t* n_active_pages, const int32_t* n_held, const void* q,
+    float* out, int32_t n_seqs, void* stream);
+
 /* ---- introspection (tests, tools): these wait for the cache's stream ---- */
 
 int akv_seq_info(akv_cache* cache, int64_t seq, akv_seq_info_t* info);
