@@ -175,7 +175,9 @@ cudaError_t launch_decode(const DecodeArgs& a, bool need_combine, int n_rows,
   if (a.n_items <= 0) return cudaSuccess;
   const int G = a.g.hq / a.g.hkv;
   cudaError_t e;
-  if (a.g.dtype == AKV_DTYPE_BF16)
+  if (a.use_mma)
+    e = launch_decode_mma(a, st);
+  else if (a.g.dtype == AKV_DTYPE_BF16)
     e = a.g.d == 64 ? launch_simple_g<__nv_bfloat16, 64>(a, G, st)
                     : launch_simple_g<__nv_bfloat16, 128>(a, G, st);
   else

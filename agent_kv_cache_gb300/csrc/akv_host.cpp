@@ -19,6 +19,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <queue>
 #include <string>
 #include <unordered_map>
 #include <vector>
@@ -163,6 +164,10 @@ struct akv_cache {
   uint32_t wait_limit = 1u << 22;
   int sm_count = 148;
   uint64_t launches = 0;
+  CUtensorMap tm_k{}, tm_v{};
+  bool use_mma = false;
+  int mma_blocks_per_sm = 0;
+  int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
 };
 
 namespace {
@@ -254,6 +259,7 @@ void destroy(akv_cache* c) {
   cudaFree(c->d_part_ml);
   cudaFree(c->d_err);
   cudaFree(c->d_plan);
+  cudaFree(c->d_counters);
   for (Stage& s : c->stages) {
     if (s.h) cudaFreeHost(s.h);
     if (s.d) cudaFree(s.d);
@@ -355,6 +361,13 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
     CKC(cudaMallocHost(&s.h, c->stage_bytes));
     CKC(cudaMalloc(&s.d, c->stage_bytes));
     CKC(cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming));
+  }
+  CKC(cudaMalloc(&c->d_counters, (size_t)kMaxItems * f.hkv * sizeof(int32_t)));
+  CKC(cudaMemset(c->d_counters, 0, (size_t)kMaxItems * f.hkv * sizeof(int32_t)));
+  c->use_mma = make_pool_tensor_maps(g, &c->tm_k, &c->tm_v);
+  if (c->use_mma) {
+    c->mma_blocks_per_sm = decode_mma_blocks_per_sm(f.head_dim);
+    if (c->mma_blocks_per_sm < 1) c->use_mma = false;
   }
   CKC(cudaDeviceSynchronize());
 #undef CKC
@@ -573,7 +586,10 @@ int akv_append(akv_cache* c, const int64_t* seqs, const int32_t* n_tokens, int32
                    reinterpret_cast<const AppendBlock*>(d + o_blocks), (int)blocks.size(),
                    reinterpret_cast<const int32_t*>(d + o_ids),
                    reinterpret_cast<const int32_t*>(d + o_act), k_raw, v, total, c->d_cs,
-                   c->d_err, c->stream));
+                   c->d_err,
+                   AppendLimits{(int32_t)items.size(), (int32_t)ids.size(), (int32_t)act.size(),
+                                c->cfg.max_seqs},
+                   c->stream));
   return AKV_OK;
 }
 
@@ -772,36 +788,73 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       if (!hs[i]) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seqs[i]);
       total += hs[i]->n_active_pages;
     }
-    // split so that the (item, kv head) blocks fill the GPU a few times over
-    const int64_t target = (int64_t)c->sm_count * 8;
-    int64_t pps = std::max<int64_t>(4, (total * c->cfg.hkv + target - 1) / target);
-    for (;;) {
-      int64_t items = 0;
-      for (int i = 0; i < n_seqs; ++i) items += std::max<int64_t>(1, (hs[i]->n_active_pages + pps - 1) / pps);
-      if (items <= kMaxItems) break;
-      pps *= 2;
-    }
     std::vector<DecodeItem> items;
     std::vector<int32_t> item0(n_seqs), splits(n_seqs);
     bool combine = false;
-    for (int i = 0; i < n_seqs; ++i) {
-      const HostSeq* s = hs[i];
-      const int32_t na = s->n_active_pages;
-      const int32_t ns = (int32_t)std::max<int64_t>(1, (na + pps - 1) / pps);
+    auto emit = [&](int i, int32_t ns, bool even) {
+      const HostSeq* sq = hs[i];
+      const int64_t na = sq->n_active_pages;
       item0[i] = (int32_t)items.size();
       splits[i] = ns;
       combine |= ns > 1;
       for (int32_t k = 0; k < ns; ++k) {
         DecodeItem it{};
-        it.dslot = s->dslot;
+        it.dslot = sq->dslot;
         it.row = i;
-        it.p0 = (int32_t)std::min<int64_t>(na, (int64_t)k * pps);
-        it.p1 = (int32_t)std::min<int64_t>(na, (int64_t)(k + 1) * pps);
-        it.pos_q = (int32_t)(s->n_slots - 1);
+        it.p0 = (int32_t)(even ? na * k / ns : std::min<int64_t>(na, k * ((na + ns - 1) / ns)));
+        it.p1 = (int32_t)(even ? na * (k + 1) / ns : std::min<int64_t>(na, (k + 1) * ((na + ns - 1) / ns)));
+        it.pos_q = (int32_t)(sq->n_slots - 1);
         it.n_splits = ns;
         it.item0 = item0[i];
         items.push_back(it);
       }
+    };
+    if (c->use_mma) {
+      // Tensor-core path: as many blocks as fit the GPU in whole waves, the
+      // splits of each sequence proportional to its active pages and equal
+      // within it; one split holds at most kDecodeMaxTiles tiles.
+      const int64_t tpp = c->cfg.page_size / 16;
+      const int64_t resident = (int64_t)c->sm_count * c->mma_blocks_per_sm;
+      const int64_t pairs = (int64_t)n_seqs * c->cfg.hkv;
+      const int64_t waves = std::max<int64_t>(1, (pairs + resident - 1) / resident);
+      int64_t target = std::max<int64_t>(n_seqs, waves * resident / c->cfg.hkv);
+      std::vector<int32_t> ns(n_seqs);
+      int64_t sum = 0;
+      using Entry = std::pair<int64_t, int>;        // (pages per split, seq)
+      std::priority_queue<Entry> pq;
+      for (int i = 0; i < n_seqs; ++i) {
+        const int64_t na = hs[i]->n_active_pages;
+        ns[i] = (int32_t)std::max<int64_t>(1, (na * tpp + kDecodeMaxTiles - 1) / kDecodeMaxTiles);
+        sum += ns[i];
+        pq.push({(na + ns[i] - 1) / ns[i], i});
+      }
+      target = std::min<int64_t>(std::max(target, sum), kMaxItems);
+      while (sum < target && !pq.empty()) {
+        Entry e = pq.top();
+        pq.pop();
+        if (e.first <= 2) break;                      // splits of 1-2 pages gain nothing
+        const int i = e.second;
+        ++ns[i];
+        ++sum;
+        const int64_t na = hs[i]->n_active_pages;
+        pq.push({(na + ns[i] - 1) / ns[i], i});
+      }
+      if (sum > kMaxItems) return fail(c, AKV_ECAPACITY, "decode needs %lld work items", (long long)sum);
+      for (int i = 0; i < n_seqs; ++i) emit(i, ns[i], true);
+      combine = false;                                 // merged inside the kernel
+    } else {
+      // split so that the (item, kv head) blocks fill the GPU a few times over
+      const int64_t target = (int64_t)c->sm_count * 8;
+      int64_t pps = std::max<int64_t>(4, (total * c->cfg.hkv + target - 1) / target);
+      for (;;) {
+        int64_t n_it = 0;
+        for (int i = 0; i < n_seqs; ++i)
+          n_it += std::max<int64_t>(1, (hs[i]->n_active_pages + pps - 1) / pps);
+        if (n_it <= kMaxItems) break;
+        pps *= 2;
+      }
+      for (int i = 0; i < n_seqs; ++i)
+        emit(i, (int32_t)std::max<int64_t>(1, (hs[i]->n_active_pages + pps - 1) / pps), false);
     }
     Blob blob;
     blob.put(items.data(), items.size());
@@ -820,6 +873,9 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   const size_t o_item0 = (n_items * sizeof(DecodeItem) + 15) & ~size_t(15);
   const size_t o_splits = (o_item0 + n_seqs * sizeof(int32_t) + 15) & ~size_t(15);
   DecodeArgs a{};
+  a.tm_k = c->tm_k;
+  a.tm_v = c->tm_v;
+  a.use_mma = c->use_mma;
   a.g = c->g;
   a.sa = c->sa;
   a.items = reinterpret_cast<const DecodeItem*>(c->d_plan);
@@ -833,6 +889,10 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
   a.err = c->d_err;
   a.wait_limit = c->wait_limit;
+  a.counters = c->d_counters;
+  a.n_rows = n_seqs;
+  a.max_seqs = c->cfg.max_seqs;
+  a.counter_rows = kMaxItems;
   CK(launch_decode(a, c->plan_combine, n_seqs,
                    reinterpret_cast<const int32_t*>(c->d_plan + o_item0),
                    reinterpret_cast<const int32_t*>(c->d_plan + o_splits), c->stream));
@@ -958,6 +1018,8 @@ int akv_sync_errors(akv_cache* c, uint32_t* word) {
   CK(cudaStreamSynchronize(c->stream));
   CK(cudaMemcpy(&w, c->d_err, sizeof(w), cudaMemcpyDeviceToHost));
   CK(cudaMemset(c->d_err, 0, sizeof(w)));
+  // a kernel that gave up may have left split counters behind
+  if (w) CK(cudaMemset(c->d_counters, 0, (size_t)kMaxItems * c->cfg.hkv * sizeof(int32_t)));
   if (word) *word = w;
   return w ? fail(c, AKV_EDEVICE, "device error word 0x%x", w) : AKV_OK;
 }

@@ -9,6 +9,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace akv {
@@ -89,6 +90,8 @@ struct DecodeItem {
 };
 
 struct DecodeArgs {
+  CUtensorMap tm_k;     // TMA maps over the pools (tensor-core path only)
+  CUtensorMap tm_v;
   Geom g;
   SeqArrays sa;
   const DecodeItem* items;
@@ -102,14 +105,21 @@ struct DecodeArgs {
   float scale_log2;     // log2(e) / sqrt(D)
   uint32_t* err;
   uint32_t wait_limit;
+  int32_t use_mma;      // tensor-core kernel (bf16 pools, page % 16 == 0, group <= 8)
+  int32_t* counters;    // [row][hkv] finished splits (tensor-core path; reset by the last)
+  int32_t n_rows;       // rows of q / out in this call
+  int32_t max_seqs;     // device rows of the per-sequence arrays
+  int32_t counter_rows; // rows of `counters`
 };
+constexpr int kDecodeMaxTiles = 512;   // 16-token tiles in one split of the tensor-core path
 
 // Launchers (akv_kernels.cu / akv_decode.cu).  All enqueue on `st`.
+struct AppendLimits { int32_t n_items, n_ids, n_act, max_seqs; };
 cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* items,
                           const AppendBlock* blocks, int n_blocks, const int32_t* ids,
                           const int32_t* act, const void* k_raw, const void* v,
                           int64_t total_tokens, const float2* cs, uint32_t* err,
-                          cudaStream_t st);
+                          AppendLimits lim, cudaStream_t st);
 cudaError_t launch_copy_pages(const Geom& g, const PagePair* pairs, int n_pairs,
                               uint32_t* err, cudaStream_t st);
 cudaError_t launch_drop(const Geom& g, const SeqArrays& sa, const DropItem* items,
@@ -122,5 +132,10 @@ cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* i
 cudaError_t launch_decode(const DecodeArgs& a, bool need_combine, int n_rows,
                           const int32_t* row_item0, const int32_t* row_splits,
                           cudaStream_t st);
+// Tensor-core decode (akv_decode_mma.cu).
+bool decode_mma_supported(const Geom& g);
+bool make_pool_tensor_maps(const Geom& g, CUtensorMap* tk, CUtensorMap* tv);
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st);
+int decode_mma_blocks_per_sm(int head_dim);
 
 }  // namespace akv

@@ -102,18 +102,36 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
          const AppendBlock* __restrict__ blocks, const int32_t* __restrict__ ids,
          const int32_t* __restrict__ act, const T* __restrict__ k_raw,
          const T* __restrict__ v_raw, int64_t total_tokens,
-         const float2* __restrict__ cs, uint32_t* err) {
+         const float2* __restrict__ cs, uint32_t* err, AppendLimits lim) {
   extern __shared__ float2 s_cs[];   // [kAppendTokens][D/2]
   __shared__ int s_page[kAppendTokens];
   __shared__ int s_off[kAppendTokens];
   const AppendBlock blk = blocks[blockIdx.x];
+  if (blk.item < 0 || blk.item >= lim.n_items) {
+    if (threadIdx.x == 0) flag(err, AKV_DERR_INDEX);
+    return;
+  }
   const AppendItem it = items[blk.item];
+  // the item must describe memory this call owns (uniform per block)
+  if (it.dslot < 0 || it.dslot >= lim.max_seqs || it.ids_off < 0 || it.nk < 0 ||
+      it.ids_off + it.nk > lim.n_ids || it.act_off < 0 || it.n_act < 0 ||
+      it.act_off + it.n_act > lim.n_act || it.tok0 < 0 || it.n < 0 || blk.t0 < 0 ||
+      blk.t0 >= it.n || (int64_t)it.tok0 + it.n > total_tokens) {
+    if (threadIdx.x == 0) flag(err, AKV_DERR_INDEX);
+    return;
+  }
   const int nt = min(kAppendTokens, it.n - blk.t0);
   const int D = g.d, H = D / 2, S = g.s;
   const int tid = threadIdx.x, bs = blockDim.x;
   const int64_t row_base = (int64_t)it.dslot;
 
-  if (blk.t0 == 0) {
+  // blockIdx.y picks the layer when every logical layer has its own slab;
+  // with aliased slabs one block walks all layers in order (last one wins)
+  const int l_begin = gridDim.y > 1 ? (int)blockIdx.y : 0;
+  const int l_end = gridDim.y > 1 ? (int)blockIdx.y + 1 : g.layers;
+  const bool meta = blockIdx.y == 0;
+
+  if (blk.t0 == 0 && meta) {
     for (int i = tid; i < it.nk; i += bs) {
       const int k = it.k0 + i;
       if (k >= 0 && k < sa.seq_pages) sa.pages[row_base * sa.seq_pages + k] = ids[it.ids_off + i];
@@ -129,11 +147,11 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     const int slot = it.slot0 + blk.t0 + t;
     int pid = -1;
     if (slot >= 0 && slot < sa.max_slots) {
-      atomicOr(&sa.keep[row_base * sa.keep_words + slot / 32], 1u << (slot % 32));
+      if (meta) atomicOr(&sa.keep[row_base * sa.keep_words + slot / 32], 1u << (slot % 32));
       const int pk = slot / S - it.k0;
       if (pk >= 0 && pk < it.nk) pid = ids[it.ids_off + pk];
     }
-    if (pid < 0 || pid >= g.max_pages) { flag(err, AKV_DERR_PAGE); pid = -1; }
+    if (pid < 0 || pid >= g.max_pages) { if (meta) flag(err, AKV_DERR_PAGE); pid = -1; }
     s_page[t] = pid;
     s_off[t] = slot % S;
   }
@@ -160,8 +178,7 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     const int64_t tok = it.tok0 + blk.t0 + t;
     const int64_t dst_off = (int64_t)pid * g.page_stride + (int64_t)h * g.head_stride +
                             (int64_t)s_off[t] * D;
-    // logical layers in order, so aliased slabs keep the last layer's data
-    for (int l = 0; l < g.layers; ++l) {
+    for (int l = l_begin; l < l_end; ++l) {
       const int64_t src_off = ((int64_t)l * total_tokens + tok) * g.hkv * D + (int64_t)h * D;
       const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
       if (r < ku) {
@@ -446,17 +463,18 @@ cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* 
                           const AppendBlock* blocks, int n_blocks, const int32_t* ids,
                           const int32_t* act, const void* k_raw, const void* v,
                           int64_t total_tokens, const float2* cs, uint32_t* err,
-                          cudaStream_t st) {
+                          AppendLimits lim, cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
   const size_t smem = (size_t)kAppendTokens * (g.d / 2) * sizeof(float2);
+  const dim3 grid(n_blocks, g.phys_layers == g.layers ? g.layers : 1);
   if (g.dtype == AKV_DTYPE_BF16)
-    k_append<__nv_bfloat16><<<n_blocks, 256, smem, st>>>(
+    k_append<__nv_bfloat16><<<grid, 256, smem, st>>>(
         g, sa, items, blocks, ids, act, static_cast<const __nv_bfloat16*>(k_raw),
-        static_cast<const __nv_bfloat16*>(v), total_tokens, cs, err);
+        static_cast<const __nv_bfloat16*>(v), total_tokens, cs, err, lim);
   else
-    k_append<float><<<n_blocks, 256, smem, st>>>(
+    k_append<float><<<grid, 256, smem, st>>>(
         g, sa, items, blocks, ids, act, static_cast<const float*>(k_raw),
-        static_cast<const float*>(v), total_tokens, cs, err);
+        static_cast<const float*>(v), total_tokens, cs, err, lim);
   return cudaGetLastError();
 }
 

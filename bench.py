@@ -51,7 +51,7 @@ def workload_name():
 
 
 def trajectories():
-    return traces.llama8b_batch(SEED, batch=BATCH, n_total=N_TOKENS)
+    return traces.llama8b_batch(SEED, batch=16, n_total=N_TOKENS)[:BATCH]
 
 
 # ---------------------------------------------------------------------------
@@ -313,7 +313,8 @@ def gpu_arm(args):
     for _ in range(args.warmup):
         b.step()
     torch.cuda.synchronize()
-    assert b.cache.sync_errors() == 0
+    w = b.cache.sync_errors()
+    assert w == 0, f"device error word 0x{w:x} after the warm-up steps"
 
     evs = [b.events() for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -410,6 +411,9 @@ def gpu_arm(args):
             "gpu_launches": int(launches),
             "clocks": clk.summary(),
         }
+        if args.profiling_case:
+            line["config"]["profiling_case"] = (f"reduced for a profiler capture: batch {BATCH}, "
+                                                f"{SHAPE.layers} layers, {DECODE_STEPS} decode steps")
         if cpu:
             line["cpu_baseline"] = {"value": round(cpu["bytes"] / cpu["seconds"] / 1e9, 4),
                                     "unit": "GB/s", "cores": cpu["workers"], "kind": "oracle",
@@ -447,6 +451,7 @@ def reference_arm(args):
 
 
 def main():
+    global BATCH, DECODE_STEPS, SHAPE
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3)
@@ -454,7 +459,20 @@ def main():
     ap.add_argument("--impl", choices=["akv", "reference"], default="akv")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # smaller cases for profiler captures only; a line printed with any of
+    # these is marked "profiling case" and is not the benchmark's number
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--decode-steps", type=int, default=None)
     args = ap.parse_args()
+    if args.batch or args.layers or args.decode_steps:
+        import dataclasses
+        BATCH = args.batch or BATCH
+        DECODE_STEPS = args.decode_steps or DECODE_STEPS
+        SHAPE = dataclasses.replace(SHAPE, layers=args.layers or SHAPE.layers)
+        args.profiling_case = True
+    else:
+        args.profiling_case = False
     if args.impl == "reference":
         reference_arm(args)
     else:

@@ -139,6 +139,44 @@ def test_batched_reposition_and_decode():
     t.decode(seqs, 1)                    # seq 2 has nothing active: zeros
 
 
+@pytest.mark.parametrize("dtype,page,G", [("bf16", 16, 4), ("bf16", 16, 8), ("bf16", 4, 4),
+                                          ("fp32", 16, 4)])
+def test_poisoned_pool_memory_does_not_leak_into_attention(dtype, page, G):
+    """Slots that are not active (dropped, or never written) may hold any bit
+    pattern; attention must ignore them.  The pools start filled with NaN."""
+    t = Twin(layers=2, hq=2 * G, hkv=2, head_dim=128, page_size=page, dtype=dtype,
+             rope_theta=5e5, max_pages=512, max_seqs=4, max_slots=2048, seed=5)
+    t.gpu.k_pool.fill_(float("nan"))
+    t.gpu.v_pool.fill_(float("nan"))
+    a, b = t.create(), t.create()
+    t.append([a, b], [37, 301])                 # ragged tails: never-written slots
+    t.drop(b, [(3, 40), (100, 101)])
+    t.append([a, b], [1, 1])
+    t.decode([a, b], 0)
+    t.reposition([b])
+    t.append([a, b], [1, 1])
+    for s in (a, b):
+        t.check(s)
+    t.decode([a, b], 1)
+
+
+def test_long_splits_wrap_the_stage_ring():
+    """Splits of ~50 tiles: every shared-memory stage is refilled many times."""
+    t = Twin(layers=1, hq=32, hkv=8, head_dim=128, page_size=16, dtype="bf16",
+             rope_theta=5e5, max_pages=6000, max_seqs=4, max_slots=17000, seed=9)
+    seqs = [t.create() for _ in range(4)]
+    t.append(seqs, [16000, 15000, 16383, 9000])
+    t.drop(seqs[0], [(1000, 5000)])
+    t.drop(seqs[2], [(0, 16), (300, 301)])
+    t.append(seqs, [1, 1, 1, 1])
+    t.decode(seqs, 0)
+    t.reposition(seqs[:3])
+    t.append(seqs, [1, 1, 1, 1])
+    for s in seqs:
+        t.check(s, kv=False)
+    t.decode(seqs, 1)
+
+
 def _history(t, ops, toks):
     s = t.create()
     names = {}
@@ -213,8 +251,9 @@ def test_copy_on_write_isolation():
     for s in [base] + kids:
         t.check(s)
     idx = torch.from_numpy(pages0.astype(np.int64)).cuda()
-    assert torch.equal(t.gpu.k_pool[:, idx], snap_k)
-    assert torch.equal(t.gpu.v_pool[:, idx], snap_v)
+    # bit patterns, so never-written slots (any bits, NaN included) compare too
+    assert torch.equal(t.gpu.k_pool[:, idx].view(torch.int16), snap_k.view(torch.int16))
+    assert torch.equal(t.gpu.v_pool[:, idx].view(torch.int16), snap_v.view(torch.int16))
     # kept prefix of kids[0] (pages before the first drop) is still shared
     p0, _ = t.gpu.page_table(kids[0])
     assert list(p0[:2]) == list(pages0[:2])
