@@ -83,6 +83,24 @@ __device__ __forceinline__ void rotate_unit(const T* src, T* dst, int c, int hal
   st16(dst + half + c * E, Vec<T>::pack(yo));
 }
 
+// The same rotation on a unit already loaded into registers.
+template <typename T>
+__device__ __forceinline__ void rotate_regs(uint4 lo, uint4 hi, T* dst, int c, int half,
+                                            const float2* cs_row) {
+  constexpr int E = Vec<T>::E;
+  float x[E], y[E], xo[E], yo[E];
+  Vec<T>::unpack(lo, x);
+  Vec<T>::unpack(hi, y);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float2 t = cs_row[c * E + e];
+    xo[e] = fmaf(x[e], t.x, -y[e] * t.y);
+    yo[e] = fmaf(x[e], t.y, y[e] * t.x);
+  }
+  st16(dst + c * E, Vec<T>::pack(xo));
+  st16(dst + half + c * E, Vec<T>::pack(yo));
+}
+
 template <typename T>
 __device__ __forceinline__ void copy_unit(const T* src, T* dst, int c, int half) {
   constexpr int E = Vec<T>::E;
@@ -375,7 +393,7 @@ k_compact(Geom g, SeqArrays sa, const ReposItem* __restrict__ items,
 // ---------------------------------------------------------------------------
 
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
          const float2* __restrict__ cs, uint32_t* err) {
   extern __shared__ float2 s_cs[];   // [S][D/2], angle -(src - j) f
@@ -439,15 +457,47 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
     const int64_t dst_off = (int64_t)dpage * g.page_stride + (int64_t)h * g.head_stride +
                             (int64_t)t * D;
     const bool cp = s_copy[t];
-#pragma unroll 4
-    for (int l = 0; l < g.layers; ++l) {
-      const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
-      if (r < ku) {
-        if (cp) copy_unit<T>(kp + slab + src_off, kp + slab + dst_off, r, H);
-        else rotate_unit<T>(kp + slab + src_off, kp + slab + dst_off, r, H, s_cs + t * H);
-      } else {
-        const int c = r - ku;
-        st16(vp + slab + dst_off + c * E, ld16(vp + slab + src_off + c * E));
+    // Source and destination both live in the pool, so the compiler cannot
+    // move a later layer's loads above an earlier layer's stores: batch the
+    // loads of several layers explicitly to keep enough bytes in flight.
+    if (r < ku) {
+      constexpr int B = 2;
+      for (int l0 = 0; l0 < g.layers; l0 += B) {
+        uint4 lo[B], hi[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+          if (l0 + j < g.layers) {
+            const T* src = kp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + src_off;
+            lo[j] = ld16(src + r * E);
+            hi[j] = ld16(src + H + r * E);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+          if (l0 + j >= g.layers) break;
+          T* dst = kp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + dst_off;
+          if (cp) {
+            st16(dst + r * E, lo[j]);
+            st16(dst + H + r * E, hi[j]);
+          } else {
+            rotate_regs<T>(lo[j], hi[j], dst, r, H, s_cs + t * H);
+          }
+        }
+      }
+    } else {
+      constexpr int B = 4;
+      const int c = r - ku;
+      for (int l0 = 0; l0 < g.layers; l0 += B) {
+        uint4 x[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+          if (l0 + j < g.layers)
+            x[j] = ld16(vp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + src_off + c * E);
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+          if (l0 + j >= g.layers) break;
+          st16(vp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + dst_off + c * E, x[j]);
+        }
       }
     }
   }

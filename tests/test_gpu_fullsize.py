@@ -1,0 +1,155 @@
+"""Full-size workloads: every sequence's metadata bit-exact against the
+oracle, sampled keys/values/attention element by element.
+
+The four large workloads run at their full shapes and batch sizes, through
+the same batched calls as the benchmark (so the same decode launch plan).
+The long-running 70B-shaped workload runs 6 turns instead of 100 (with the
+active-token cap lowered to 4096 so that its drop/reposition cycle still
+fires); its shapes, batch and layer aliasing are the full ones.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from agent_kv_cache_gb300 import abi, build
+from fullsize import FullSize
+from workloads import traces
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean():
+    build()
+    gc.collect()
+    torch.cuda.empty_cache()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _pages(lengths, S, extra):
+    return sum(-(-n // S) for n in lengths) + extra
+
+
+def test_llama8b_trace_fullsize():
+    """16 x 32768 tokens, ~60% dropped, reposition of forks, 2 decode steps x 32 layers."""
+    sh, seed, B, N = traces.LLAMA8B, traces.seed_for(1), 16, 32768
+    trajs = traces.llama8b_batch(seed, batch=B, n_total=N)
+    rs = [N - sum(e - b for b, e in t.drop_ranges) for t in trajs]
+    max_pages = B * (N // 16) + _pages([r + 8 for r in rs], 16, 2 * B + 64)
+    fs = FullSize(sh, seed, 2 * B, max_pages, N + 64, sample_seqs=[0, 9], sample_layers=[0, 31])
+    base = [fs.create(b, b + 1) for b in range(B)]
+    fs.append_tokens(base, N)
+    forks = [fs.fork(s, i, fs.tags[s]) for i, s in enumerate(base)]
+    for f, tr in zip(forks, trajs):
+        fs.drop(f, tr.drop_ranges)
+    fs.check_metadata()
+    fs.reposition(forks)
+    fs.check_metadata()
+    fs.check_kv()
+    for step in range(2):
+        fs.append_tokens(forks, 1)
+        fs.decode(forks, step, range(sh.layers), check_layers=[0, 31])
+    fs.check_metadata()
+    fs.check_kv()
+    fs.close()
+
+
+def test_gptoss120b_trace_fullsize():
+    """4 x 131072 tokens, ~80% dropped, D = 64, group 8, 2 decode steps x 36 layers."""
+    sh, seed, B, N = traces.GPTOSS120B, traces.seed_for(2), 4, 131072
+    trajs = traces.gptoss_batch(seed, batch=B, n_total=N)
+    rs = [N - sum(e - b for b, e in t.drop_ranges) for t in trajs]
+    max_pages = _pages([N] * B, 16, 0) + _pages([r + 8 for r in rs], 16, 64)
+    fs = FullSize(sh, seed, B, max_pages, N + 64, sample_seqs=[1, 3], sample_layers=[0, 35])
+    seqs = [fs.create(b, b + 1) for b in range(B)]
+    fs.append_tokens(seqs, N)
+    for s, tr in zip(seqs, trajs):
+        fs.drop(s, tr.drop_ranges)
+    fs.reposition(seqs)
+    fs.check_metadata()
+    fs.check_kv()
+    for step in range(2):
+        fs.append_tokens(seqs, 1)
+        fs.decode(seqs, step, range(sh.layers), check_layers=[0, 35])
+    fs.check_metadata()
+    fs.close()
+
+
+def test_branching_histories_fullsize():
+    """A 16384-token prefix forked into 64 branches with 1-6 drop/reposition
+    operations each; batched decode over all 64 branches.  Shared prefix
+    pages stay shared and unchanged; repositioned pages are private."""
+    sh, seed, P = traces.LLAMA8B, traces.seed_for(3), 16384
+    segs, branches = traces.branching(seed, n_branches=64, prefix_len=P)
+    max_pages = P // 16 + 64 * (P // 16 + 4) + 256
+    fs = FullSize(sh, seed, 66, max_pages, P + 64, sample_seqs=[-1, 0, 13, 40],
+                  sample_layers=[0, 31])
+    root = fs.create(-1, 1)
+    fs.append_tokens([root], P)
+    pages0, _ = fs.gpu.page_table(root)
+    idx = torch.from_numpy(pages0.astype(np.int64)).cuda()
+    snap = fs.gpu.k_pool[:, idx].view(torch.int16).sum(dtype=torch.int64).item()
+    kids = [fs.fork(root, i, 1) for i in range(64)]
+    for k, br in zip(kids, branches):
+        for op in br.ops:
+            if op[0] == "drop":
+                fs.drop(k, op[1])
+            else:
+                fs.reposition([k])
+    fs.check_metadata()
+    fs.check_kv()
+    # the root's pages were never written by any branch
+    assert fs.gpu.k_pool[:, idx].view(torch.int16).sum(dtype=torch.int64).item() == snap
+    # every branch shares the pages before its first dropped slot
+    for k in kids:
+        pk, _ = fs.gpu.page_table(k)
+        info = fs.gpu.info(k)
+        assert info["n_shared_pages"] >= 0 and info["n_owned_pages"] >= 0
+        shared = [p for p in pk if p >= 0 and fs.gpu.refcount(int(p)) > 1]
+        assert set(shared) <= set(pages0.tolist())
+    for step in range(2):
+        fs.append_tokens(kids, 1)
+        fs.decode(kids, step, range(sh.layers), check_layers=[0, 31])
+    fs.check_metadata()
+    for k in kids:
+        fs.free(k)
+    fs.free(root)
+    assert fs.gpu.pool_stats()[1] == 0
+    fs.close()
+
+
+def test_llama70b_steady_state_fullsize():
+    """64 sequences, 80 logical layers on 16 aliased slabs, 64/8 heads, D 128:
+    6 turns of (tool response append, decode), drop oldest tool responses and
+    reposition every 3 turns."""
+    sh, seed, B = traces.LLAMA70B, traces.seed_for(4), 64
+    turns = traces.steady_state(seed, n_seqs=B, n_turns=6, decode_per_turn=2, active_cap=4096)
+    longest = max(1024 + sum(t.tool_len + 2 for t in ts) for ts in turns)
+    max_pages = B * (-(-longest // 16) + 8) * 2
+    fs = FullSize(sh, seed, B, max_pages, longest + 64, sample_seqs=[5, 50],
+                  sample_layers=[3, 15], phys_layers=16)
+    seqs = [fs.create(b, b + 1) for b in range(B)]
+    fs.append_tokens(seqs, 1024)
+    step = 0
+    for k in range(6):
+        for s, ts in zip(seqs, turns):
+            fs.append_tokens([s], ts[k].tool_len)
+        for _ in range(2):
+            fs.append_tokens(seqs, 1)
+            fs.decode(seqs, step, range(sh.layers), check_layers=[3, 79])
+            step += 1
+        did = []
+        for s, ts in zip(seqs, turns):
+            if ts[k].drop_ranges:
+                fs.drop(s, ts[k].drop_ranges)
+            if ts[k].repos:
+                did.append(s)
+        if did:
+            fs.reposition(did)
+    fs.check_metadata()
+    fs.check_kv()
+    fs.close()
