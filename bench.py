@@ -89,6 +89,24 @@ def step_bytes(trajs):
                 decode_per_call=decode_calls, total=repos + decode + append + drop)
 
 
+def decode_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if that
+    summary was taken on the decode kernel as it is now (else None)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "decode_mma_llama8b.md")
+    src = os.path.join(ROOT, "agent_kv_cache_gb300", "csrc", "akv_decode_mma.cu")
+    try:
+        text = open(prof).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = dict(l.split(":", 1) for l in text.splitlines()
+                  if l.startswith(("kernel_source_sha256:", "traffic_bytes_per_launch:")))
+    if fields.get("kernel_source_sha256", "").strip() != digest:
+        return None
+    return int(fields["traffic_bytes_per_launch"].strip())
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
@@ -350,6 +368,7 @@ def gpu_arm(args):
     achieved = float(np.sum(per_call) / (np.sum(dec_ms) * 1e-3) / 1e9)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    traffic = decode_traffic() if not args.profiling_case else None
     peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     value = world * by["total"] / (ms * 1e-3) / 1e9
@@ -400,10 +419,11 @@ def gpu_arm(args):
                        "l2": "inputs larger than L2 (each decode call reads ~0.9 GB); no flush",
                        "bytes_per_step": by["total"]},
             "decode_tok_s": round(tok_s, 1),
-            "roofline": {"kernel": "decode attention call (split-KV kernel + split merge)",
+            "roofline": {"kernel": "k_decode_mma (one launch per decode-attention call, "
+                                   "split merge fused)",
                          "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": None,
+                         "traffic": traffic,
                          "avg_call_us": round(float(np.mean(dec_ms)) * 1e3, 2),
                          "algorithmic_bytes_per_call": int(np.mean(per_call))},
             "repos_ms": round(float(np.mean(repos_ms)), 3),
