@@ -83,17 +83,19 @@ __device__ __forceinline__ void rotate_unit(const T* src, T* dst, int c, int hal
   st16(dst + half + c * E, Vec<T>::pack(yo));
 }
 
-// The same rotation on a unit already loaded into registers.
+// The same rotation on a unit already loaded into registers, with the row's
+// cos/sin stored unit-minor: pair c*E + e at cs_t[e * n_units + c], so the
+// lanes rotating one row read consecutive words (no bank conflicts).
 template <typename T>
 __device__ __forceinline__ void rotate_regs(uint4 lo, uint4 hi, T* dst, int c, int half,
-                                            const float2* cs_row) {
+                                            const float2* cs_t, int n_units) {
   constexpr int E = Vec<T>::E;
   float x[E], y[E], xo[E], yo[E];
   Vec<T>::unpack(lo, x);
   Vec<T>::unpack(hi, y);
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const float2 t = cs_row[c * E + e];
+    const float2 t = cs_t[e * n_units + c];
     xo[e] = fmaf(x[e], t.x, -y[e] * t.y);
     yo[e] = fmaf(x[e], t.y, y[e] * t.x);
   }
@@ -396,7 +398,7 @@ template <typename T>
 __global__ void __launch_bounds__(256, 4)
 k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
          const float2* __restrict__ cs, uint32_t* err) {
-  extern __shared__ float2 s_cs[];   // [S][D/2], angle -(src - j) f
+  extern __shared__ float2 s_cs[];   // [S][D/2] (unit-minor), angle -(src - j) f
   __shared__ int s_src_page[64];
   __shared__ int s_src_off[64];
   __shared__ int s_copy[64];
@@ -430,12 +432,16 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
     s_src_off[t] = src % S;
     s_copy[t] = (src == j);
   }
-  for (int i = tid; i < nj * H; i += bs) {
-    const int t = i / H;
-    const int delta = gather[j0 + t] - (j0 + t);
-    float2 c = make_float2(1.f, 0.f);
-    if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * H + i % H];
-    s_cs[i] = make_float2(c.x, -c.y);
+  {
+    constexpr int E = Vec<T>::E;
+    const int ku = H / E;
+    for (int i = tid; i < nj * H; i += bs) {
+      const int t = i / H, j = i % H;                 // pair j = c*E + e of row t
+      const int delta = gather[j0 + t] - (j0 + t);
+      float2 c = make_float2(1.f, 0.f);
+      if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * H + j];
+      s_cs[t * H + (j % E) * ku + j / E] = make_float2(c.x, -c.y);
+    }
   }
   __syncthreads();
   const int dpage = s_dst_page;
@@ -480,7 +486,7 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
             st16(dst + r * E, lo[j]);
             st16(dst + H + r * E, hi[j]);
           } else {
-            rotate_regs<T>(lo[j], hi[j], dst, r, H, s_cs + t * H);
+            rotate_regs<T>(lo[j], hi[j], dst, r, H, s_cs + t * H, ku);
           }
         }
       }

@@ -108,6 +108,25 @@ def decode_traffic():
 
 
 # ---------------------------------------------------------------------------
+# ranks: one replica per GPU, sequences partitioned, no data-path collective
+# ---------------------------------------------------------------------------
+
+def rank_tags(rank, batch):
+    """Input-stream tags of the sequences a rank owns (disjoint across ranks)."""
+    return [rank * 1000 + b + 1 for b in range(batch)]
+
+
+def reduce_max(value, dist, device):
+    """Max over ranks of a per-rank time (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
 
@@ -233,7 +252,7 @@ class Bench:
                            self.max_pages, 2 * BATCH + 2, N_TOKENS + DECODE_STEPS + S,
                            SHAPE.rope_theta)
         self.stream = self.cache.stream
-        self.tags = [rank * 1000 + b + 1 for b in range(BATCH)]
+        self.tags = rank_tags(rank, BATCH)
         self.width = synth.width_for(SHAPE.dtype)
         self._build_base()
         self._make_inputs()
@@ -352,11 +371,7 @@ def gpu_arm(args):
         torch.cuda.synchronize()
     barrier()
     launches = (b.cache.kernel_launches() - n0) // args.steps
-    ms = start.elapsed_time(stop) / args.steps
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(start.elapsed_time(stop) / args.steps, dist, "cuda")
     assert b.cache.sync_errors() == 0
 
     by = b.bytes
@@ -393,11 +408,7 @@ def gpu_arm(args):
         e2.record(b.stream)
         torch.cuda.synchronize()
         barrier()
-        ms2 = s2.elapsed_time(e2) / args.steps
-        if dist:
-            t = torch.tensor([ms2], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms2 = float(t.item())
+        ms2 = reduce_max(s2.elapsed_time(e2) / args.steps, dist, "cuda")
         h2d = (b.q.numel() + b.knew.numel() + b.vnew.numel()) * BYTES_EL
         d2h = host["out"].numel() * 4
         e2e = {"value": world * by["total"] / (ms2 * 1e-3) / 1e9, "unit": "GB/s",
