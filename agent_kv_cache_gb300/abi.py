@@ -91,6 +91,7 @@ SIGNATURES = {
     "akv_last_error": (ctypes.c_char_p, [_P]),
     "akv_sync_errors": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "akv_kernel_launches": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
+    "akv_set_decode_waves": (ctypes.c_int, [_P, _I32]),
     "akv_decode_attention_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                     ctypes.c_double, _P, _P, _P, _I32, _I32,
                                                     _PI32, _PI32, _P, _P, _I32, _P]),
@@ -270,6 +271,10 @@ def akv_sync_errors(cache):
     if rc not in (AKV_OK, AKV_EDEVICE):
         _check(rc, cache)
     return w.value
+
+
+def akv_set_decode_waves(cache, waves):
+    _check(lib().akv_set_decode_waves(cache, waves), cache)
 
 
 def akv_kernel_launches(cache):

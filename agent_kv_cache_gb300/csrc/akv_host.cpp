@@ -167,6 +167,7 @@ struct akv_cache {
   CUtensorMap tm_k{}, tm_v{};
   bool use_mma = false;
   int mma_blocks_per_sm = 0;
+  int32_t decode_waves = 1;
   int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
 };
 
@@ -816,7 +817,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       const int64_t tpp = c->cfg.page_size / 16;
       const int64_t resident = (int64_t)c->sm_count * c->mma_blocks_per_sm;
       const int64_t pairs = (int64_t)n_seqs * c->cfg.hkv;
-      const int64_t waves = std::max<int64_t>(1, (pairs + resident - 1) / resident);
+      const int64_t waves = std::max<int64_t>(c->decode_waves, (pairs + resident - 1) / resident);
       int64_t target = std::max<int64_t>(n_seqs, waves * resident / c->cfg.hkv);
       std::vector<int32_t> ns(n_seqs);
       int64_t sum = 0;
@@ -1022,6 +1023,13 @@ int akv_sync_errors(akv_cache* c, uint32_t* word) {
   if (w) CK(cudaMemset(c->d_counters, 0, (size_t)kMaxItems * c->cfg.hkv * sizeof(int32_t)));
   if (word) *word = w;
   return w ? fail(c, AKV_EDEVICE, "device error word 0x%x", w) : AKV_OK;
+}
+
+int akv_set_decode_waves(akv_cache* c, int32_t waves) {
+  if (!c || waves < 1 || waves > 64) return AKV_EINVAL;
+  c->decode_waves = waves;
+  c->plan_epoch = ~0ULL;   // re-plan on the next call
+  return AKV_OK;
 }
 
 int akv_kernel_launches(akv_cache* c, uint64_t* count) {
