@@ -28,9 +28,15 @@ AKV" = page 2):
 Readings where the pages are silent or garbled (the display formulas of
 Eqs. 3-6 did not survive extraction):
 
-* RoPE is the half-split form: the pairs are (i, i + D/2), i < D/2, with
-  frequency f_i = theta^(-2 i / D); R(p) maps (x, y) to
-  (x cos(p f_i) - y sin(p f_i), x sin(p f_i) + y cos(p f_i)).
+* RoPE is the half-split form: the pairs are (i, i + R/2), i < R/2, with
+  frequency f_i = theta^(-2 i / R); R(p) maps (x, y) to
+  (x cos(p f_i) - y sin(p f_i), x sin(p f_i) + y cos(p f_i)).  R is the
+  rotary width: the full head dim, or the first R dims for partial RoPE,
+  whose other dims are not rotated and are copied by a reposition
+  ("[Repo Review] AKV", 5.5).
+* Sliding-window attention counts positions, not active tokens: with
+  position gaps left by a drop, the read range of a query is still the
+  window of positions ending at the query ("[Repo Review] AKV", 5.5).
 * P is a set of logical (trajectory) indices, assigned at append and never
   renumbered; dropping an index already dropped is a no-op.
 * The keys are stored in the pool's dtype: every write of a key (append,
@@ -62,33 +68,35 @@ import numpy as np
 # rotary position embedding
 # ---------------------------------------------------------------------------
 
-def inv_freq(head_dim, theta):
-    """f_i = theta^(-2 i / D) for i in [0, D/2), in fp64."""
-    i = np.arange(head_dim // 2, dtype=np.float64)
-    return np.power(float(theta), -2.0 * i / float(head_dim))
+def inv_freq(rope_dim, theta):
+    """f_i = theta^(-2 i / R) for i in [0, R/2), in fp64 (R = rotary dims)."""
+    i = np.arange(rope_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / float(rope_dim))
 
 
 def rope(x, pos, freq):
-    """R(pos) x on the last axis (half-split pairs).
+    """R(pos) x on the last axis.
 
-    ``x`` is [..., D]; ``pos`` broadcasts against ``x[..., 0]``.
+    The rotary part is the first R = 2 len(freq) dims, in half-split pairs
+    (i, i + R/2); dims R.. pass through (partial RoPE).  ``x`` is [..., D];
+    ``pos`` broadcasts against ``x[..., 0]``.
     """
     x = np.asarray(x, dtype=np.float64)
-    h = x.shape[-1] // 2
+    h = len(freq)
     ang = np.asarray(pos, dtype=np.float64)[..., None] * freq
     c, s = np.cos(ang), np.sin(ang)
-    a, b = x[..., :h], x[..., h:]
-    return np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
+    a, b = x[..., :h], x[..., h:2 * h]
+    return np.concatenate([a * c - b * s, a * s + b * c, x[..., 2 * h:]], axis=-1)
 
 
 def rope_inverse(x, pos, freq):
     """R(pos)^-1 x = R(pos)^T x."""
     x = np.asarray(x, dtype=np.float64)
-    h = x.shape[-1] // 2
+    h = len(freq)
     ang = np.asarray(pos, dtype=np.float64)[..., None] * freq
     c, s = np.cos(ang), np.sin(ang)
-    a, b = x[..., :h], x[..., h:]
-    return np.concatenate([a * c + b * s, -a * s + b * c], axis=-1)
+    a, b = x[..., :h], x[..., h:2 * h]
+    return np.concatenate([a * c + b * s, -a * s + b * c, x[..., 2 * h:]], axis=-1)
 
 
 def reposition_key(k, p, q, freq):
@@ -169,13 +177,14 @@ class OracleCache:
     """
 
     def __init__(self, hq, hkv, head_dim, rope_theta, pool_dtype, layers=(0,),
-                 page_size=16):
+                 page_size=16, rope_dim=0):
         if hq % hkv:
             raise OracleError("hq must be a multiple of hkv")
         self.hq, self.hkv, self.d = hq, hkv, head_dim
         self.group = hq // hkv
         self.layers = list(layers)
-        self.freq = inv_freq(head_dim, rope_theta)
+        self.rope_dim = rope_dim or head_dim
+        self.freq = inv_freq(self.rope_dim, rope_theta)
         self.dtype = pool_dtype
         self.page_size = page_size
         self.seqs = {}
@@ -262,14 +271,21 @@ class OracleCache:
         s.log.append(("repos",))
 
     # -- attention -------------------------------------------------------------
-    def attention(self, layer_index, q, sids):
-        """Decode attention for each sequence: ``q`` is [n][Hq][D] (pre-RoPE)."""
+    def attention(self, layer_index, q, sids, window=0):
+        """Decode attention for each sequence: ``q`` is [n][Hq][D] (pre-RoPE).
+
+        ``window`` > 0: sliding window over positions -- the query at
+        position p reads the active keys whose position lies in (p - window, p]
+        (with positions left sparse by a drop, fewer than ``window`` keys).
+        """
         q = np.asarray(q, dtype=np.float64)
         out = np.zeros(q.shape, dtype=np.float64)
         for i, sid in enumerate(sids):
             s = self.seqs[sid]
-            qr = rope(q[i], np.full(self.hq, s.next_pos - 1), self.freq)
-            act = np.flatnonzero(s.alive)
+            p = s.next_pos - 1
+            qr = rope(q[i], np.full(self.hq, p), self.freq)
+            visible = s.alive if window <= 0 else s.alive & (s.pos > p - window)
+            act = np.flatnonzero(visible)
             if act.size == 0:
                 continue
             for h in range(self.hq):

@@ -367,7 +367,65 @@ def pin_input_values_exact():
         assert abs(x.mean()) < 0.02 and abs(x.var() - 1) < 0.03
 
 
-PINS = [pin_inv_freq, pin_rope_complex_form, pin_rope_matrix_identities,
+def pin_partial_rope():
+    """Partial RoPE: the first R dims rotate with frequencies over R (complex
+    form), the other D - R dims are untouched; a reposition copies them."""
+    rng = np.random.default_rng(14)
+    d, r, theta = 128, 64, 1.0e4
+    f = O.inv_freq(r, theta)
+    assert f.shape == (32,) and abs(f[8] - theta ** -0.25) < 1e-15
+    x = _rand(rng, 5, d)
+    pos = np.array([0, 3, 100, 4095, 70000])
+    got = O.rope(x, pos, f)
+    z = (x[:, : r // 2] + 1j * x[:, r // 2: r]) * np.exp(1j * pos[:, None] * f)
+    np.testing.assert_allclose(got[:, :r], np.concatenate([z.real, z.imag], axis=1), atol=1e-12)
+    np.testing.assert_array_equal(got[:, r:], x[:, r:])
+    np.testing.assert_allclose(O.reposition_key(x, 900, 17, f), O.rope(x, 17 - 900, f), atol=1e-12)
+    c64 = O.OracleCache(4, 2, d, theta, "f64", layers=(0,), page_size=16, rope_dim=r)
+    sid = c64.create()
+    k = _rand(rng, 1, 9, 2, d)
+    c64.append(sid, k, k)
+    ang = np.arange(9)[:, None, None] * (theta ** (-2.0 * np.arange(r // 2) / r))
+    z = (k[0, ..., : r // 2] + 1j * k[0, ..., r // 2: r]) * np.exp(1j * ang)
+    np.testing.assert_allclose(c64.seqs[sid].K[0, ..., :r],
+                               np.concatenate([z.real, z.imag], axis=-1), atol=1e-12)
+    c = O.OracleCache(4, 2, d, theta, "bf16", layers=(0,), page_size=16, rope_dim=r)
+    sid = c.create()
+    k, v = _rand(rng, 1, 40, 2, d), _rand(rng, 1, 40, 2, d)
+    c.append(sid, k, v)
+    before = c.seqs[sid].K.copy()
+    c.drop(sid, [(0, 7)])
+    c.reposition(sid)
+    np.testing.assert_array_equal(c.seqs[sid].K[..., r:], before[:, 7:, :, r:])
+
+
+def pin_sliding_window():
+    """A window covers positions (p - W, p]: W larger than the sequence is
+    full attention; W = 1 reads only the query's own token; with position
+    gaps left by a drop the window holds fewer keys; any W equals textbook
+    attention over exactly the keys whose positions fall in the window."""
+    rng = np.random.default_rng(15)
+    c = _tiny_cache(dtype="f64", d=16, hq=4, hkv=2, theta=1.0e4)
+    s = c.create()
+    n = 60
+    k, v = _tokens(rng, c, n)
+    c.append(s, k, v)
+    q = _rand(rng, 1, 4, 16)
+    full = c.attention(0, q, [s])
+    np.testing.assert_allclose(c.attention(0, q, [s], window=n + 5), full, atol=1e-14)
+    one = c.attention(0, q, [s], window=1)
+    for h in range(4):
+        np.testing.assert_allclose(one[0, h], v[0, n - 1, h // 2], atol=1e-14)
+    c.drop(s, [(30, 55)])                         # gap: positions 30..54 inactive
+    for w in (3, 8, 20, 31, 40):
+        got = c.attention(0, q, [s], window=w)
+        keep = [t for t in range(n) if not (30 <= t < 55) and t > n - 1 - w]
+        want = _dense_attention(q[0], k[0][keep], v[0][keep], n - 1, np.array(keep),
+                                c.freq, 2)
+        np.testing.assert_allclose(got[0], want, atol=1e-12)
+
+
+PINS = [pin_inv_freq, pin_partial_rope, pin_sliding_window, pin_rope_complex_form, pin_rope_matrix_identities,
         pin_rope_relative, pin_bf16_rounding, pin_fig10_positions,
         pin_fig5_histories, pin_drop_semantics,
         pin_reposition_positions_and_gather, pin_no_drop_unchanged,
@@ -465,8 +523,30 @@ def _mutant_history_drops_merged_away(self, sid, ranges):
         log.pop()
 
 
+def _mutant_window_counts_tokens(self, layer_index, q, sids, window=0):
+    if window <= 0:
+        return _orig_attention(self, layer_index, q, sids)
+    out = np.zeros(np.asarray(q).shape)
+    for i, sid in enumerate(sids):
+        s = self.seqs[sid]
+        qr = O.rope(q[i], np.full(self.hq, s.next_pos - 1), self.freq)
+        act = np.flatnonzero(s.alive)[-window:]       # the last W active tokens
+        for h in range(self.hq):
+            kvh = h // self.group
+            sc = s.K[layer_index, act, kvh] @ qr[h] / np.sqrt(self.d)
+            w = np.exp(sc - sc.max())
+            out[i, h] = (w @ s.V[layer_index, act, kvh]) / w.sum()
+    return out
+
+
 _orig_drop = O.OracleCache.drop
 _orig_attention = O.OracleCache.attention
+_orig_init = O.OracleCache.__init__
+
+
+def _mutant_partial_freq_over_d(self, *a, **kw):
+    _orig_init(self, *a, **kw)
+    self.freq = O.inv_freq(self.d, 1.0e4)[: self.rope_dim // 2]
 
 MUTANTS = {
     "rope_sign": ("rope", _bad_rope_sign, None),
@@ -480,6 +560,8 @@ MUTANTS = {
     "gqa_head_modulo": (None, None, ("attention", _mutant_gqa_modulo)),
     "query_position_off_by_one": (None, None, ("attention", _mutant_query_at_next_pos)),
     "history_forgets_drop": (None, None, ("drop", _mutant_history_drops_merged_away)),
+    "window_counts_tokens": (None, None, ("attention", _mutant_window_counts_tokens)),
+    "partial_rope_freq_over_d": (None, None, ("__init__", _mutant_partial_freq_over_d)),
 }
 
 
