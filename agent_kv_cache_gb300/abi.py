@@ -45,7 +45,7 @@ class AkvConfig(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("max_pages", ctypes.c_int32),
                 ("max_seqs", ctypes.c_int32), ("max_slots", ctypes.c_int32),
-                ("rope_theta", ctypes.c_double)]
+                ("rope_theta", ctypes.c_double), ("rope_dim", ctypes.c_int32)]
 
 
 class AkvSeqInfo(ctypes.Structure):
@@ -92,6 +92,7 @@ SIGNATURES = {
     "akv_sync_errors": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "akv_kernel_launches": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "akv_set_decode_waves": (ctypes.c_int, [_P, _I32]),
+    "akv_set_layer_window": (ctypes.c_int, [_P, _I32, _I32]),
     "akv_decode_attention_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                     ctypes.c_double, _P, _P, _P, _I32, _I32,
                                                     _PI32, _PI32, _P, _P, _I32, _P]),
@@ -133,10 +134,10 @@ def _arr(a, dtype, ctype):
 
 
 def make_config(layers, hq, hkv, head_dim, page_size, dtype, max_pages, max_seqs, max_slots,
-                rope_theta, phys_layers=0):
+                rope_theta, phys_layers=0, rope_dim=0):
     return AkvConfig(layers, phys_layers, hq, hkv, head_dim, page_size,
-                      AKV_DTYPE_BF16 if dtype in ("bf16", AKV_DTYPE_BF16) else AKV_DTYPE_FP32,
-                      max_pages, max_seqs, max_slots, float(rope_theta))
+                     AKV_DTYPE_BF16 if dtype in ("bf16", AKV_DTYPE_BF16) else AKV_DTYPE_FP32,
+                     max_pages, max_seqs, max_slots, float(rope_theta), rope_dim)
 
 
 def akv_pool_bytes(cfg):
@@ -271,6 +272,10 @@ def akv_sync_errors(cache):
     if rc not in (AKV_OK, AKV_EDEVICE):
         _check(rc, cache)
     return w.value
+
+
+def akv_set_layer_window(cache, layer, window):
+    _check(lib().akv_set_layer_window(cache, layer, window), cache)
 
 
 def akv_set_decode_waves(cache, waves):

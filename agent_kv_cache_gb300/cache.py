@@ -13,11 +13,11 @@ class Cache:
     """
 
     def __init__(self, layers, hq, hkv, head_dim, page_size, dtype, max_pages, max_seqs,
-                 max_slots, rope_theta, phys_layers=0, stream=None):
+                 max_slots, rope_theta, phys_layers=0, stream=None, rope_dim=0):
         import torch
         self.torch = torch
         self.cfg = abi.make_config(layers, hq, hkv, head_dim, page_size, dtype, max_pages,
-                                   max_seqs, max_slots, rope_theta, phys_layers)
+                                   max_seqs, max_slots, rope_theta, phys_layers, rope_dim)
         self.layers, self.hq, self.hkv, self.d, self.page = layers, hq, hkv, head_dim, page_size
         self.phys = phys_layers or layers
         self.dtype = dtype
@@ -64,6 +64,9 @@ class Cache:
 
     def reposition(self, seqs):
         abi.akv_reposition(self.handle, seqs)
+
+    def set_layer_window(self, layer, window):
+        abi.akv_set_layer_window(self.handle, layer, window)
 
     def decode_attention(self, layer, q, seqs, out=None):
         """q: device [n, hq, D] pool dtype; returns out [n, hq, D] fp32."""

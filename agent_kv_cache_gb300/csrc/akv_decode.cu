@@ -25,7 +25,7 @@ constexpr int kWarps = 4;
 // Generic CUDA-core kernel: any pool dtype, page size, D in {64, 128}, G <= 16.
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kWarps * 32) k_decode_simple(DecodeArgs a) {
-  constexpr int H = D / 2, J = D / 32;
+  constexpr int J = D / 32;
   __shared__ float s_q[G][D];
   __shared__ float s_m[kWarps][G], s_l[kWarps][G];
   __shared__ float s_acc[kWarps][G][D];
@@ -35,14 +35,20 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_simple(DecodeArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (it.pos_q >= 0 && it.pos_q < a.sa.max_slots) {
+    // q' = R(pos_q) q on the first R dims (pairs (d, d + R/2)); the rest as is
+    const int R = g.rope, RH = R / 2;
     const T* q = static_cast<const T*>(a.q) + ((int64_t)it.row * g.hq + (int64_t)kvh * G) * D;
-    const float2* cs = a.cs + (int64_t)it.pos_q * H;
-    for (int i = tid; i < G * H; i += blockDim.x) {
-      const int gq = i / H, d = i % H;
-      const float x = to_f(q[gq * D + d]), y = to_f(q[gq * D + d + H]);
-      const float2 t = cs[d];
-      s_q[gq][d] = fmaf(x, t.x, -y * t.y) * a.scale_log2;
-      s_q[gq][d + H] = fmaf(x, t.y, y * t.x) * a.scale_log2;
+    const float2* cs = a.cs + (int64_t)it.pos_q * RH;
+    for (int i = tid; i < G * D; i += blockDim.x) {
+      const int gq = i / D, d = i % D;
+      if (d < RH) {
+        const float x = to_f(q[gq * D + d]), y = to_f(q[gq * D + d + RH]);
+        const float2 t = cs[d];
+        s_q[gq][d] = fmaf(x, t.x, -y * t.y) * a.scale_log2;
+        s_q[gq][d + RH] = fmaf(x, t.y, y * t.x) * a.scale_log2;
+      } else if (d >= R) {
+        s_q[gq][d] = to_f(q[gq * D + d]) * a.scale_log2;
+      }
     }
   }
   __syncthreads();
@@ -70,7 +76,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_simple(DecodeArgs a) {
     }
     for (int s = 0; s < g.s; ++s) {
       const int slot = kidx * g.s + s;
-      if (!((keep[slot >> 5] >> (slot & 31)) & 1u)) continue;
+      if (slot < it.win_lo || !((keep[slot >> 5] >> (slot & 31)) & 1u)) continue;
       const T* kr = kpool + (int64_t)page * g.page_stride + (int64_t)s * D;
       const T* vr = vpool + (int64_t)page * g.page_stride + (int64_t)s * D;
       float kd[J], vd[J];

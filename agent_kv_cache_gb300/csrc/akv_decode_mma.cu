@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
         row = (page * g.hkv + kvh) * g.s + sub * kTile;
         const int slot0 = (kidx * tpp + sub) * kTile;
         bits = (keep[slot0 >> 5] >> (slot0 & 31)) & 0xffffu;
+        // sliding window: slots below win_lo are not read
+        if (it.win_lo > slot0) bits &= it.win_lo - slot0 >= kTile ? 0u : (0xffffu << (it.win_lo - slot0));
       } else {
         atomicOr(a.err, AKV_DERR_PAGE);
       }
@@ -183,20 +185,29 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
       s_bits[i] = (uint16_t)bits;
     }
   }
-  // rotated, scaled query of the group (heads >= G stay zero)
-  for (int i = tid; i < 8 * (D / 2); i += kThreads) {
-    const int gq = i / (D / 2), d = i % (D / 2);
-    float x = 0.f, y = 0.f;
-    if (gq < G && it.pos_q >= 0 && it.pos_q < a.sa.max_slots) {
+  // rotated, scaled query of the group (heads >= G stay zero); the first R
+  // dims rotate in pairs (d, d + R/2), dims R.. are only scaled
+  {
+    const int R = g.rope, RH = R / 2;
+    const bool have_q = it.pos_q >= 0 && it.pos_q < a.sa.max_slots;
+    for (int i = tid; i < 8 * D; i += kThreads) {
+      const int gq = i / D, d = i % D;
       const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) +
                                ((int64_t)it.row * g.hq + (int64_t)kvh * G + gq) * D;
-      const float qx = __bfloat162float(q[d]), qy = __bfloat162float(q[d + D / 2]);
-      const float2 t = a.cs[(int64_t)it.pos_q * (D / 2) + d];
-      x = fmaf(qx, t.x, -qy * t.y) * a.scale_log2;
-      y = fmaf(qx, t.y, qy * t.x) * a.scale_log2;
+      if (d < RH) {
+        float x = 0.f, y = 0.f;
+        if (gq < G && have_q) {
+          const float qx = __bfloat162float(q[d]), qy = __bfloat162float(q[d + RH]);
+          const float2 t = a.cs[(int64_t)it.pos_q * RH + d];
+          x = fmaf(qx, t.x, -qy * t.y) * a.scale_log2;
+          y = fmaf(qx, t.y, qy * t.x) * a.scale_log2;
+        }
+        s_q[gq * D + d] = x;
+        s_q[gq * D + d + RH] = y;
+      } else if (d >= R) {
+        s_q[gq * D + d] = (gq < G && have_q) ? __bfloat162float(q[d]) * a.scale_log2 : 0.f;
+      }
     }
-    s_q[gq * D + d] = x;
-    s_q[gq * D + d + D / 2] = y;
   }
   __syncthreads();
   // Q^T fragments (B operand of the score MMA): lane holds head lane/4,

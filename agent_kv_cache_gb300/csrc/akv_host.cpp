@@ -112,6 +112,16 @@ int32_t iv_count_pages(const std::vector<Interval>& v, int S) {
   return (int32_t)count;
 }
 
+// Pages with index < k that hold an active slot.
+int32_t iv_count_pages_below(const std::vector<Interval>& v, int S, int64_t k) {
+  std::vector<Interval> clip;
+  for (const Interval& iv : v) {
+    if (iv.a >= k * S) break;
+    clip.push_back({iv.a, std::min(iv.b, k * S)});
+  }
+  return iv_count_pages(clip, S);
+}
+
 void logical_to_slots(const std::vector<Run>& runs, int64_t lb, int64_t le,
                       std::vector<Interval>& out) {
   auto it = std::upper_bound(runs.begin(), runs.end(), lb,
@@ -147,13 +157,22 @@ struct akv_cache {
   Stage stages[kStages];
   size_t stage_bytes = 0;
   int stage_next = 0;
-  // decode plan (device copy kept while the metadata epoch is unchanged)
-  char* d_plan = nullptr;
+  // decode plans (device copies kept while the metadata epoch is unchanged),
+  // one per (sequence list, window) most recently used
+  struct Plan {
+    char* d = nullptr;
+    uint64_t epoch = ~0ULL;
+    std::vector<int64_t> seqs;
+    int32_t window = -1;
+    int items = 0;
+    bool combine = false;
+    uint64_t used = 0;
+  };
+  static constexpr int kPlans = 4;
+  Plan plans[kPlans];
+  uint64_t plan_clock = 0;
   size_t plan_cap = 0;
-  uint64_t plan_epoch = ~0ULL;
-  std::vector<int64_t> plan_seqs;
-  int plan_items = 0;
-  bool plan_combine = false;
+  std::vector<int32_t> windows;     // per logical layer, 0 = full attention
   // host state
   std::vector<int32_t> refcnt, free_pages;
   std::unordered_map<int64_t, HostSeq> seqs;
@@ -203,6 +222,9 @@ int check_config(const akv_config* cfg) {
   if (cfg->max_pages < 1 || cfg->max_seqs < 1) return AKV_EINVAL;
   if (cfg->max_slots < 1 || cfg->max_slots > (1 << 30)) return AKV_EINVAL;
   if (!(cfg->rope_theta > 1.0)) return AKV_EINVAL;
+  if (cfg->rope_dim != 0 &&
+      (cfg->rope_dim < 16 || cfg->rope_dim > cfg->head_dim || cfg->rope_dim % 16))
+    return AKV_EINVAL;
   return AKV_OK;
 }
 
@@ -259,7 +281,7 @@ void destroy(akv_cache* c) {
   cudaFree(c->d_part_acc);
   cudaFree(c->d_part_ml);
   cudaFree(c->d_err);
-  cudaFree(c->d_plan);
+  for (auto& pl : c->plans) cudaFree(pl.d);
   cudaFree(c->d_counters);
   for (Stage& s : c->stages) {
     if (s.h) cudaFreeHost(s.h);
@@ -309,6 +331,9 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   g.s = f.page_size;
   g.dtype = f.dtype;
   g.max_pages = f.max_pages;
+  g.rope = f.rope_dim ? f.rope_dim : f.head_dim;
+  c->cfg.rope_dim = g.rope;
+  c->windows.assign(f.layers, 0);
   g.head_stride = (int64_t)f.page_size * f.head_dim;
   g.page_stride = g.head_stride * f.hkv;
   g.layer_stride = g.page_stride * f.max_pages;
@@ -335,12 +360,13 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   CKC(cudaMalloc(&sa.old_pages, ns * sa.seq_pages * sizeof(int32_t)));
   CKC(cudaMalloc(&sa.gather, ns * (size_t)sa.max_slots * sizeof(int32_t)));
 
-  // RoPE table cos/sin(m f_i), m < max_slots: fp64, rounded once to fp32.
+  // RoPE table cos/sin(m f_i), m < max_slots, f_i = theta^(-2i/R): fp64,
+  // rounded once to fp32.
   {
-    const int H = f.head_dim / 2;
+    const int H = g.rope / 2;
     std::vector<float2> cs((size_t)f.max_slots * H);
     std::vector<double> fr(H);
-    for (int i = 0; i < H; ++i) fr[i] = std::pow(f.rope_theta, -2.0 * i / f.head_dim);
+    for (int i = 0; i < H; ++i) fr[i] = std::pow(f.rope_theta, -2.0 * i / g.rope);
     for (int64_t m = 0; m < f.max_slots; ++m)
       for (int i = 0; i < H; ++i) {
         const double ang = (double)m * fr[i];
@@ -354,7 +380,7 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   CKC(cudaMalloc(&c->d_err, sizeof(uint32_t)));
   CKC(cudaMemset(c->d_err, 0, sizeof(uint32_t)));
   c->plan_cap = kMaxItems * sizeof(DecodeItem) + 2 * ns * sizeof(int32_t) + 64;
-  CKC(cudaMalloc(&c->d_plan, c->plan_cap));
+  for (auto& pl : c->plans) CKC(cudaMalloc(&pl.d, c->plan_cap));
   c->stage_bytes = std::max<size_t>(1 << 20, 8 * (size_t)f.max_pages + 96 * ns +
                                                  kMaxItems * sizeof(DecodeItem) + 65536);
   c->stage_bytes = (c->stage_bytes + 4095) & ~size_t(4095);
@@ -779,22 +805,34 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   if (!c || n_seqs < 0 || (n_seqs > 0 && (!seqs || !q || !out))) return AKV_EINVAL;
   if (layer < 0 || layer >= c->cfg.layers) return fail(c, AKV_EINVAL, "layer %d out of range", layer);
   if (n_seqs == 0) return AKV_OK;
-  const bool same = c->plan_epoch == c->epoch && (int)c->plan_seqs.size() == n_seqs &&
-                    std::equal(c->plan_seqs.begin(), c->plan_seqs.end(), seqs);
-  if (!same) {
+  const int32_t window = c->windows[layer];
+  akv_cache::Plan* plan = nullptr;
+  for (auto& pl : c->plans)
+    if (pl.epoch == c->epoch && pl.window == window && (int)pl.seqs.size() == n_seqs &&
+        std::equal(pl.seqs.begin(), pl.seqs.end(), seqs))
+      plan = &pl;
+  if (!plan) {
     std::vector<const HostSeq*> hs(n_seqs);
+    std::vector<int32_t> first(n_seqs, 0), win_lo(n_seqs, 0);
     int64_t total = 0;
     for (int i = 0; i < n_seqs; ++i) {
       hs[i] = find(c, seqs[i]);
       if (!hs[i]) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seqs[i]);
-      total += hs[i]->n_active_pages;
+      if (window > 0) {
+        // the query at position p reads positions (p - window, p]: slots are
+        // positions, so the read range starts at the page of slot p - window + 1
+        const int64_t lo = std::max<int64_t>(0, hs[i]->n_slots - window);
+        win_lo[i] = (int32_t)lo;
+        first[i] = iv_count_pages_below(hs[i]->alive, c->cfg.page_size, lo / c->cfg.page_size);
+      }
+      total += hs[i]->n_active_pages - first[i];
     }
     std::vector<DecodeItem> items;
     std::vector<int32_t> item0(n_seqs), splits(n_seqs);
     bool combine = false;
     auto emit = [&](int i, int32_t ns, bool even) {
       const HostSeq* sq = hs[i];
-      const int64_t na = sq->n_active_pages;
+      const int64_t f0 = first[i], na = sq->n_active_pages - f0;
       item0[i] = (int32_t)items.size();
       splits[i] = ns;
       combine |= ns > 1;
@@ -802,17 +840,19 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
         DecodeItem it{};
         it.dslot = sq->dslot;
         it.row = i;
-        it.p0 = (int32_t)(even ? na * k / ns : std::min<int64_t>(na, k * ((na + ns - 1) / ns)));
-        it.p1 = (int32_t)(even ? na * (k + 1) / ns : std::min<int64_t>(na, (k + 1) * ((na + ns - 1) / ns)));
+        it.p0 = (int32_t)(f0 + (even ? na * k / ns : std::min<int64_t>(na, k * ((na + ns - 1) / ns))));
+        it.p1 = (int32_t)(f0 + (even ? na * (k + 1) / ns
+                                     : std::min<int64_t>(na, (k + 1) * ((na + ns - 1) / ns))));
         it.pos_q = (int32_t)(sq->n_slots - 1);
         it.n_splits = ns;
         it.item0 = item0[i];
+        it.win_lo = win_lo[i];
         items.push_back(it);
       }
     };
     if (c->use_mma) {
       // Tensor-core path: as many blocks as fit the GPU in whole waves, the
-      // splits of each sequence proportional to its active pages and equal
+      // splits of each sequence proportional to its pages to read and equal
       // within it; one split holds at most kDecodeMaxTiles tiles.
       const int64_t tpp = c->cfg.page_size / 16;
       const int64_t resident = (int64_t)c->sm_count * c->mma_blocks_per_sm;
@@ -824,7 +864,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       using Entry = std::pair<int64_t, int>;        // (pages per split, seq)
       std::priority_queue<Entry> pq;
       for (int i = 0; i < n_seqs; ++i) {
-        const int64_t na = hs[i]->n_active_pages;
+        const int64_t na = hs[i]->n_active_pages - first[i];
         ns[i] = (int32_t)std::max<int64_t>(1, (na * tpp + kDecodeMaxTiles - 1) / kDecodeMaxTiles);
         sum += ns[i];
         pq.push({(na + ns[i] - 1) / ns[i], i});
@@ -837,7 +877,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
         const int i = e.second;
         ++ns[i];
         ++sum;
-        const int64_t na = hs[i]->n_active_pages;
+        const int64_t na = hs[i]->n_active_pages - first[i];
         pq.push({(na + ns[i] - 1) / ns[i], i});
       }
       if (sum > kMaxItems) return fail(c, AKV_ECAPACITY, "decode needs %lld work items", (long long)sum);
@@ -845,32 +885,41 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       combine = false;                                 // merged inside the kernel
     } else {
       // split so that the (item, kv head) blocks fill the GPU a few times over
-      const int64_t target = (int64_t)c->sm_count * 8;
-      int64_t pps = std::max<int64_t>(4, (total * c->cfg.hkv + target - 1) / target);
+      const int64_t tgt = (int64_t)c->sm_count * 8;
+      int64_t pps = std::max<int64_t>(4, (total * c->cfg.hkv + tgt - 1) / tgt);
       for (;;) {
         int64_t n_it = 0;
         for (int i = 0; i < n_seqs; ++i)
-          n_it += std::max<int64_t>(1, (hs[i]->n_active_pages + pps - 1) / pps);
+          n_it += std::max<int64_t>(1, (hs[i]->n_active_pages - first[i] + pps - 1) / pps);
         if (n_it <= kMaxItems) break;
         pps *= 2;
       }
       for (int i = 0; i < n_seqs; ++i)
-        emit(i, (int32_t)std::max<int64_t>(1, (hs[i]->n_active_pages + pps - 1) / pps), false);
+        emit(i, (int32_t)std::max<int64_t>(1, (hs[i]->n_active_pages - first[i] + pps - 1) / pps),
+             false);
     }
     Blob blob;
     blob.put(items.data(), items.size());
     blob.put(item0.data(), item0.size());
     blob.put(splits.data(), splits.size());
     if (blob.b.size() > c->plan_cap) return fail(c, AKV_ECAPACITY, "decode plan too large");
+    plan = &c->plans[0];
+    for (auto& pl : c->plans)
+      if (pl.used < plan->used) plan = &pl;
     char* d = nullptr;
-    int rc = upload(c, blob, c->d_plan, &d);
-    if (rc) return rc;
-    c->plan_epoch = c->epoch;
-    c->plan_seqs.assign(seqs, seqs + n_seqs);
-    c->plan_items = (int)items.size();
-    c->plan_combine = combine;
+    int rc = upload(c, blob, plan->d, &d);
+    if (rc) {
+      plan->epoch = ~0ULL;
+      return rc;
+    }
+    plan->epoch = c->epoch;
+    plan->window = window;
+    plan->seqs.assign(seqs, seqs + n_seqs);
+    plan->items = (int)items.size();
+    plan->combine = combine;
   }
-  const size_t n_items = (size_t)c->plan_items;
+  plan->used = ++c->plan_clock;
+  const size_t n_items = (size_t)plan->items;
   const size_t o_item0 = (n_items * sizeof(DecodeItem) + 15) & ~size_t(15);
   const size_t o_splits = (o_item0 + n_seqs * sizeof(int32_t) + 15) & ~size_t(15);
   DecodeArgs a{};
@@ -879,8 +928,8 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   a.use_mma = c->use_mma;
   a.g = c->g;
   a.sa = c->sa;
-  a.items = reinterpret_cast<const DecodeItem*>(c->d_plan);
-  a.n_items = c->plan_items;
+  a.items = reinterpret_cast<const DecodeItem*>(plan->d);
+  a.n_items = plan->items;
   a.layer = layer;
   a.q = q;
   a.out = out;
@@ -894,10 +943,17 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   a.n_rows = n_seqs;
   a.max_seqs = c->cfg.max_seqs;
   a.counter_rows = kMaxItems;
-  CK(launch_decode(a, c->plan_combine, n_seqs,
-                   reinterpret_cast<const int32_t*>(c->d_plan + o_item0),
-                   reinterpret_cast<const int32_t*>(c->d_plan + o_splits), c->stream));
-  c->launches += c->plan_combine ? 2 : 1;
+  CK(launch_decode(a, plan->combine, n_seqs, reinterpret_cast<const int32_t*>(plan->d + o_item0),
+                   reinterpret_cast<const int32_t*>(plan->d + o_splits), c->stream));
+  c->launches += plan->combine ? 2 : 1;
+  return AKV_OK;
+}
+
+int akv_set_layer_window(akv_cache* c, int32_t layer, int32_t window) {
+  if (!c) return AKV_EINVAL;
+  if (layer < 0 || layer >= c->cfg.layers || window < 0)
+    return fail(c, AKV_EINVAL, "bad layer %d or window %d", layer, window);
+  c->windows[layer] = window;
   return AKV_OK;
 }
 
@@ -1028,7 +1084,7 @@ int akv_sync_errors(akv_cache* c, uint32_t* word) {
 int akv_set_decode_waves(akv_cache* c, int32_t waves) {
   if (!c || waves < 1 || waves > 64) return AKV_EINVAL;
   c->decode_waves = waves;
-  c->plan_epoch = ~0ULL;   // re-plan on the next call
+  for (auto& pl : c->plans) pl.epoch = ~0ULL;   // re-plan on the next call
   return AKV_OK;
 }
 

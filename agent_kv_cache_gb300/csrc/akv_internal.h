@@ -22,6 +22,7 @@ struct Geom {
   int64_t page_stride;   // elements between pages (hkv * S * D)
   int64_t head_stride;   // elements between heads (S * D)
   int32_t layers, phys_layers, hq, hkv, d, s, dtype, max_pages;
+  int32_t rope;          // rotary dims R (first R dims rotate, the rest are copied)
 };
 
 // Per-sequence device arrays, one fixed-size row per device sequence slot
@@ -86,7 +87,7 @@ struct DecodeItem {
   int32_t pos_q;        // query position (next_pos - 1), -1 if no token held
   int32_t n_splits;     // splits of this row
   int32_t item0;        // first item of this row
-  int32_t pad;
+  int32_t win_lo;       // sliding window: slots below are not read (0 = none)
 };
 
 struct DecodeArgs {
@@ -101,7 +102,7 @@ struct DecodeArgs {
   float* out;
   float* part_acc;      // [item][hkv][group][D]
   float2* part_ml;      // [item][hkv][group] (max, sum) in log2 units
-  const float2* cs;     // RoPE table [max_slots][D/2] (cos, sin)
+  const float2* cs;     // RoPE table [max_slots][R/2] (cos, sin)
   float scale_log2;     // log2(e) / sqrt(D)
   uint32_t* err;
   uint32_t wait_limit;

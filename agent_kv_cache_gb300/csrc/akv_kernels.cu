@@ -123,7 +123,7 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
          const int32_t* __restrict__ act, const T* __restrict__ k_raw,
          const T* __restrict__ v_raw, int64_t total_tokens,
          const float2* __restrict__ cs, uint32_t* err, AppendLimits lim) {
-  extern __shared__ float2 s_cs[];   // [kAppendTokens][D/2]
+  extern __shared__ float2 s_cs[];   // [kAppendTokens][R/2]
   __shared__ int s_page[kAppendTokens];
   __shared__ int s_off[kAppendTokens];
   const AppendBlock blk = blocks[blockIdx.x];
@@ -141,7 +141,7 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     return;
   }
   const int nt = min(kAppendTokens, it.n - blk.t0);
-  const int D = g.d, H = D / 2, S = g.s;
+  const int D = g.d, S = g.s;
   const int tid = threadIdx.x, bs = blockDim.x;
   const int64_t row_base = (int64_t)it.dslot;
 
@@ -175,15 +175,18 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     s_page[t] = pid;
     s_off[t] = slot % S;
   }
-  for (int i = tid; i < nt * H; i += bs) {
-    const int slot = it.slot0 + blk.t0 + i / H;
-    s_cs[i] = (slot >= 0 && slot < sa.max_slots) ? cs[(int64_t)slot * H + i % H]
+  const int R = g.rope, RH = R / 2;
+  for (int i = tid; i < nt * RH; i += bs) {
+    const int slot = it.slot0 + blk.t0 + i / RH;
+    s_cs[i] = (slot >= 0 && slot < sa.max_slots) ? cs[(int64_t)slot * RH + i % RH]
                                                   : make_float2(1.f, 0.f);
   }
   __syncthreads();
 
+  // units of a row: rotary (pairs of 16-byte chunks), K dims past the rotary
+  // part (copied), V chunks (copied)
   constexpr int E = Vec<T>::E;
-  const int ku = H / E, vu = D / E, per_row = ku + vu;
+  const int kr = RH / E, kc = (D - R) / E, vu = D / E, per_row = kr + kc + vu;
   const int units = g.hkv * nt * per_row;
   const T* kb = k_raw;
   const T* vb = v_raw;
@@ -201,10 +204,13 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     for (int l = l_begin; l < l_end; ++l) {
       const int64_t src_off = ((int64_t)l * total_tokens + tok) * g.hkv * D + (int64_t)h * D;
       const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
-      if (r < ku) {
-        rotate_unit<T>(kb + src_off, kp + slab + dst_off, r, H, s_cs + t * H);
+      if (r < kr) {
+        rotate_unit<T>(kb + src_off, kp + slab + dst_off, r, RH, s_cs + t * RH);
+      } else if (r < kr + kc) {
+        const int o = R + (r - kr) * E;
+        st16(kp + slab + dst_off + o, ld16(kb + src_off + o));
       } else {
-        const int c = r - ku;
+        const int c = r - kr - kc;
         st16(vp + slab + dst_off + c * E, ld16(vb + src_off + c * E));
       }
     }
@@ -398,7 +404,7 @@ template <typename T>
 __global__ void __launch_bounds__(256, 4)
 k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
          const float2* __restrict__ cs, uint32_t* err) {
-  extern __shared__ float2 s_cs[];   // [S][D/2] (unit-minor), angle -(src - j) f
+  extern __shared__ float2 s_cs[];   // [S][R/2] (unit-minor), angle -(src - j) f
   __shared__ int s_src_page[64];
   __shared__ int s_src_off[64];
   __shared__ int s_copy[64];
@@ -409,7 +415,7 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
     if (items[mid].block0 <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
   }
   const ReposItem it = items[lo];
-  const int S = g.s, D = g.d, H = D / 2;
+  const int S = g.s, D = g.d, R = g.rope, RH = R / 2;
   const int k = it.n_kept + ((int)blockIdx.x - it.block0);
   const int j0 = k * S;
   const int nj = min(S, it.r - j0);
@@ -434,13 +440,13 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
   }
   {
     constexpr int E = Vec<T>::E;
-    const int ku = H / E;
-    for (int i = tid; i < nj * H; i += bs) {
-      const int t = i / H, j = i % H;                 // pair j = c*E + e of row t
+    const int kr = RH / E;
+    for (int i = tid; i < nj * RH; i += bs) {
+      const int t = i / RH, j = i % RH;               // pair j = c*E + e of row t
       const int delta = gather[j0 + t] - (j0 + t);
       float2 c = make_float2(1.f, 0.f);
-      if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * H + j];
-      s_cs[t * H + (j % E) * ku + j / E] = make_float2(c.x, -c.y);
+      if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * RH + j];
+      s_cs[t * RH + (j % E) * kr + j / E] = make_float2(c.x, -c.y);
     }
   }
   __syncthreads();
@@ -448,7 +454,7 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
   if (dpage < 0) return;
 
   constexpr int E = Vec<T>::E;
-  const int ku = H / E, vu = D / E, per_row = ku + vu;
+  const int kr = RH / E, kc = (D - R) / E, vu = D / E, per_row = kr + kc + vu;
   const int units = g.hkv * nj * per_row;
   T* kp = static_cast<T*>(g.k);
   T* vp = static_cast<T*>(g.v);
@@ -466,7 +472,7 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
     // Source and destination both live in the pool, so the compiler cannot
     // move a later layer's loads above an earlier layer's stores: batch the
     // loads of several layers explicitly to keep enough bytes in flight.
-    if (r < ku) {
+    if (r < kr) {
       constexpr int B = 2;
       for (int l0 = 0; l0 < g.layers; l0 += B) {
         uint4 lo[B], hi[B];
@@ -475,7 +481,7 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
           if (l0 + j < g.layers) {
             const T* src = kp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + src_off;
             lo[j] = ld16(src + r * E);
-            hi[j] = ld16(src + H + r * E);
+            hi[j] = ld16(src + RH + r * E);
           }
         }
 #pragma unroll
@@ -484,25 +490,27 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
           T* dst = kp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + dst_off;
           if (cp) {
             st16(dst + r * E, lo[j]);
-            st16(dst + H + r * E, hi[j]);
+            st16(dst + RH + r * E, hi[j]);
           } else {
-            rotate_regs<T>(lo[j], hi[j], dst, r, H, s_cs + t * H, ku);
+            rotate_regs<T>(lo[j], hi[j], dst, r, RH, s_cs + t * RH, kr);
           }
         }
       }
     } else {
+      // a chunk copied as it is: K past the rotary dims, or V
       constexpr int B = 4;
-      const int c = r - ku;
+      T* base = r < kr + kc ? kp : vp;
+      const int o = r < kr + kc ? R + (r - kr) * E : (r - kr - kc) * E;
       for (int l0 = 0; l0 < g.layers; l0 += B) {
         uint4 x[B];
 #pragma unroll
         for (int j = 0; j < B; ++j)
           if (l0 + j < g.layers)
-            x[j] = ld16(vp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + src_off + c * E);
+            x[j] = ld16(base + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + src_off + o);
 #pragma unroll
         for (int j = 0; j < B; ++j) {
           if (l0 + j >= g.layers) break;
-          st16(vp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + dst_off + c * E, x[j]);
+          st16(base + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + dst_off + o, x[j]);
         }
       }
     }
@@ -521,7 +529,7 @@ cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* 
                           int64_t total_tokens, const float2* cs, uint32_t* err,
                           AppendLimits lim, cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
-  const size_t smem = (size_t)kAppendTokens * (g.d / 2) * sizeof(float2);
+  const size_t smem = (size_t)kAppendTokens * (g.rope / 2) * sizeof(float2);
   const dim3 grid(n_blocks, g.phys_layers == g.layers ? g.layers : 1);
   if (g.dtype == AKV_DTYPE_BF16)
     k_append<__nv_bfloat16><<<grid, 256, smem, st>>>(
@@ -563,7 +571,7 @@ cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* i
                           int n_items, int n_blocks, const float2* cs, uint32_t* err,
                           cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
-  const size_t smem = (size_t)g.s * (g.d / 2) * sizeof(float2);
+  const size_t smem = (size_t)g.s * (g.rope / 2) * sizeof(float2);
   if (g.dtype == AKV_DTYPE_BF16)
     k_gather<__nv_bfloat16><<<n_blocks, 256, smem, st>>>(g, sa, items, n_items, cs, err);
   else

@@ -74,6 +74,11 @@ typedef struct akv_config {
   int32_t max_seqs;    /* sequences alive at the same time */
   int32_t max_slots;   /* held tokens per sequence (positions stay below) */
   double rope_theta;   /* RoPE base */
+  int32_t rope_dim;    /* rotary dims R: the first R dims of K and q rotate
+                          (half-split pairs (i, i+R/2), f_i = theta^(-2i/R)),
+                          dims R.. are not rotated (partial RoPE; "[Repo
+                          Review] AKV" 5.5).  0 means R = head_dim; else a
+                          multiple of 16 in [16, head_dim]. */
 } akv_config;
 
 typedef struct akv_cache akv_cache;
@@ -173,6 +178,13 @@ int akv_reposition(akv_cache* cache, const int64_t* seqs, int32_t n_seqs);
 int akv_decode_attention(akv_cache* cache, int32_t layer, const void* q,
                          const int64_t* seqs, int32_t n_seqs, float* out);
 
+/* Sliding-window attention for one layer ("[Repo Review] AKV" 5.5): with
+ * window W > 0, akv_decode_attention on this layer reads, for a query at
+ * position p, only the active tokens whose position lies in (p - W, p] --
+ * a window of positions, so position gaps left by a drop hold fewer keys.
+ * W = 0 (the default) is full attention.  Errors: AKV_EINVAL. */
+int akv_set_layer_window(akv_cache* cache, int32_t layer, int32_t window);
+
 /* ---- decode attention that allocates nothing (no counterpart in the paper) ----
  *
  * For callers that cannot allocate device memory: applications that reserve
@@ -202,6 +214,8 @@ int akv_decode_attention(akv_cache* cache, int32_t layer, const void* q,
  * at zero: a call writes every partial it reads), so calls that overlap on
  * the GPU -- on different streams, or from several host threads -- race and
  * must be serialised by the caller.  Splits are sized so the partials fit.
+ * It covers the plain method: full-width RoPE and full attention (no
+ * rope_dim, no window).
  * Errors: AKV_ECAPACITY when n_seqs > AKV_NOALLOC_MAX_SEQS; AKV_EINVAL for
  * a bad shape or pointer; AKV_ECUDA when a launch fails. */
 #define AKV_NOALLOC_SCRATCH_BYTES (8 << 20)

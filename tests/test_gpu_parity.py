@@ -177,6 +177,71 @@ def test_long_splits_wrap_the_stage_ring():
     t.decode(seqs, 1)
 
 
+PARTIAL = [
+    # dtype, page, G, D, rope_dim
+    ("bf16", 16, 4, 128, 64),
+    ("bf16", 16, 8, 64, 32),
+    ("bf16", 32, 2, 128, 96),
+    ("fp32", 4, 2, 128, 48),
+    ("bf16", 1, 16, 64, 16),
+]
+
+
+@pytest.mark.parametrize("dtype,page,G,D,R", PARTIAL)
+def test_partial_rope_operation_sequences(dtype, page, G, D, R):
+    """Only the first R dims rotate; the rest are copied by append and
+    reposition and read as they are by decode."""
+    rng = np.random.default_rng(R * 7 + D + page)
+    t = Twin(layers=2, hq=2 * G, hkv=2, head_dim=D, page_size=page, dtype=dtype,
+             rope_theta=5e5, max_pages=2048, max_seqs=6, max_slots=1024, seed=R, rope_dim=R)
+    seqs = [t.create(), t.create()]
+    t.append(seqs, [150, 333])
+    for step in range(6):
+        g = seqs[step % 2]
+        n = t.gpu.info(g)["n_logical"]
+        b = int(rng.integers(0, n - 1))
+        t.drop(g, [(b, min(n, b + int(rng.integers(1, 60))))])
+        if step % 2:
+            t.reposition(seqs)
+        t.append(seqs, [1, 1])
+        for s in seqs:
+            t.check(s)
+        t.decode(seqs, step)
+
+
+@pytest.mark.parametrize("dtype,page,G,D", [("bf16", 16, 4, 128), ("bf16", 16, 8, 64),
+                                            ("fp32", 16, 2, 64), ("bf16", 4, 4, 128)])
+def test_sliding_window_over_positions(dtype, page, G, D):
+    """Windows count positions: after a drop without a reposition the window
+    holds fewer keys; windowed and full layers alternate (two plans)."""
+    t = Twin(layers=4, hq=2 * G, hkv=2, head_dim=D, page_size=page, dtype=dtype,
+             rope_theta=1e4, max_pages=4096, max_seqs=6, max_slots=8192, seed=3)
+    seqs = [t.create() for _ in range(3)]
+    t.append(seqs, [2000, 777, 64])
+    t.set_window(1, 128)
+    t.set_window(3, 40)
+    step = 0
+    for w1, w3 in [(128, 40), (1, 5000), (16, 300), (700, 1)]:
+        t.set_window(1, w1)
+        t.set_window(3, w3)
+        t.append(seqs, [1, 1, 1])
+        t.decode(seqs, step)
+        step += 1
+    t.drop(seqs[0], [(1900, 1995), (1500, 1510)])   # gaps inside the windows
+    t.drop(seqs[2], [(0, 64)])
+    t.append(seqs, [1, 1, 1])
+    for w1, w3 in [(128, 40), (10, 200), (3000, 2)]:
+        t.set_window(1, w1)
+        t.set_window(3, w3)
+        t.decode(seqs, step)
+        step += 1
+    t.reposition(seqs)
+    t.append(seqs, [1, 1, 1])
+    t.decode(seqs, step)
+    for s in seqs:
+        t.check(s)
+
+
 def _history(t, ops, toks):
     s = t.create()
     names = {}

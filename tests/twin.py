@@ -40,36 +40,40 @@ def ulp(x, dtype):
     return 2.0 ** (np.floor(np.log2(ax)) - (bits - 1))
 
 
-def _pair_norm(ref):
-    h = ref.shape[-1] // 2
-    norm = np.sqrt(ref[..., :h] ** 2 + ref[..., h:] ** 2)
-    return np.concatenate([norm, norm], axis=-1)
+def _pair_norm(ref, rope_dim=0):
+    """|(x, y)| of each element's rotation pair; 0 on dims that never rotate."""
+    d = ref.shape[-1]
+    r = rope_dim or d
+    h = r // 2
+    norm = np.sqrt(ref[..., :h] ** 2 + ref[..., h:r] ** 2)
+    return np.concatenate([norm, norm, np.zeros(ref.shape[:-1] + (d - r,))], axis=-1)
 
 
-def key_tolerance(ref, dtype, n_rot):
+def key_tolerance(ref, dtype, n_rot, rope_dim=0):
     """Per-element bound of a key that went through n_rot roundings."""
     p = 8 if dtype == "bf16" else 24
     r = max(n_rot, 1)
-    norm = _pair_norm(ref)
+    norm = _pair_norm(ref, rope_dim)
     return (ulp(ref, dtype) + (r - 1) * np.sqrt(2.0) * 2.0 ** (1 - p) * norm
             + r * 8 * 2.0 ** -24 * norm)
 
 
-def key_ulp_fraction(err, ref, dtype, n_rot):
+def key_ulp_fraction(err, ref, dtype, n_rot, rope_dim=0):
     """Fraction of elements within n_rot ulp of the oracle."""
     r = max(n_rot, 1)
-    ok = err <= r * (ulp(ref, dtype) + 8 * 2.0 ** -24 * _pair_norm(ref))
+    ok = err <= r * (ulp(ref, dtype) + 8 * 2.0 ** -24 * _pair_norm(ref, rope_dim))
     return float(ok.mean()) if ok.size else 1.0
 
 
 class Twin:
     def __init__(self, layers=1, hq=8, hkv=2, head_dim=64, page_size=16, dtype="fp32",
                  rope_theta=1e4, max_pages=256, max_seqs=8, max_slots=2048, seed=1,
-                 phys_layers=0):
+                 phys_layers=0, rope_dim=0):
         self.gpu = Cache(layers, hq, hkv, head_dim, page_size, dtype, max_pages, max_seqs,
-                         max_slots, rope_theta, phys_layers=phys_layers)
+                         max_slots, rope_theta, phys_layers=phys_layers, rope_dim=rope_dim)
         self.orc = OracleCache(hq, hkv, head_dim, rope_theta, dtype, layers=range(layers),
-                               page_size=page_size)
+                               page_size=page_size, rope_dim=rope_dim)
+        self.windows = {}
         self.L, self.hq, self.hkv, self.d, self.S = layers, hq, hkv, head_dim, page_size
         self.dtype = dtype
         self.width = synth.width_for(dtype)
@@ -137,6 +141,10 @@ class Twin:
                 self.rot[g] += 1
             self.orc.reposition(self.o[g])
 
+    def set_window(self, layer, window):
+        self.gpu.set_layer_window(layer, window)
+        self.windows[layer] = window
+
     def decode(self, seqs, step, layers=None):
         """Decode attention for every layer; returns the max/mean abs errors."""
         layers = range(self.L) if layers is None else layers
@@ -147,7 +155,8 @@ class Twin:
             out = self.gpu.decode_attention(l, torch.from_numpy(q).to(self.tdtype).cuda(),
                                             list(seqs))
             got = out.double().cpu().numpy()
-            want = self.orc.attention(l, q, [self.o[g] for g in seqs])
+            want = self.orc.attention(l, q, [self.o[g] for g in seqs],
+                                      window=self.windows.get(l, 0))
             err = np.abs(got - want)
             worst = (max(worst[0], err.max()), max(worst[1], err.mean()))
             tmax, tmean = ATTN_TOL[self.dtype]
@@ -180,11 +189,14 @@ class Twin:
             for l in range(self.L):
                 k, v = self.gpu.read_kv(g, l)
                 ref_k = o.K[l][live]
-                tol = key_tolerance(ref_k, self.dtype, self.rot[g])
+                tol = key_tolerance(ref_k, self.dtype, self.rot[g], self.orc.rope_dim)
                 err = np.abs(k[live] - ref_k)
                 bad = err > tol
                 assert not bad.any(), (l, err[bad][:5], ref_k[bad][:5], tol[bad][:5])
-                frac = key_ulp_fraction(err, ref_k, self.dtype, self.rot[g])
+                frac = key_ulp_fraction(err, ref_k, self.dtype, self.rot[g], self.orc.rope_dim)
+                rd = self.orc.rope_dim
+                if rd < self.d:      # dims past the rotary part are copied: bit-exact
+                    np.testing.assert_array_equal(k[live][..., rd:], ref_k[..., rd:])
                 assert frac >= 0.99, (l, frac)
                 np.testing.assert_array_equal(v[live], o.V[l][live])
         assert self.gpu.sync_errors() == 0
