@@ -24,6 +24,13 @@ AKV" = page 2):
   operation sequence replayed from empty; m counts operations.
 * attention -- plain softmax attention of one query over the active keys
   (the pages' decode reads the active KV only; page 1, A.4.1).
+* restore attention -- page 1, 4.2.2, 4.2.3 and A.1.1 (segment-batch
+  attention): a restore recomputes every token of an operation program in
+  one forward and must give each token the attention it had originally --
+  over the keys active when it was appended (including ones dropped later),
+  at the positions of that time.  ``replay_attention`` is the definition:
+  replay the program, and after each appended token take its query's
+  attention over the active cache (the token included).
 
 Readings where the pages are silent or garbled (the display formulas of
 Eqs. 3-6 did not survive extraction):
@@ -296,6 +303,33 @@ class OracleCache:
                 w = np.exp(sc - sc.max())
                 out[i, h] = (w @ vv) / w.sum()
         return out
+
+    # -- restore (segment-batch attention), by replay ------------------------------
+    def replay_attention(self, program, q, k_raw, v, window=0):
+        """Attention output of every appended token of ``program``, as it was
+        when the token was appended.
+
+        ``program`` is a list of ("append", n) | ("drop", ranges) | ("repos",)
+        applied to a fresh sequence; ``q``, ``k_raw``, ``v`` are
+        [layers][T][heads][D] for the T appended tokens in order.  Returns
+        [layers][T][Hq][D].  The sequence is left in its final state.
+        """
+        q = np.asarray(q, dtype=np.float64)
+        sid = self.create()
+        out = np.zeros(q.shape[:2] + (self.hq, self.d))
+        t = 0
+        for op in program:
+            if op[0] == "append":
+                for _ in range(op[1]):
+                    self.append(sid, k_raw[:, t:t + 1], v[:, t:t + 1])
+                    for li in range(len(self.layers)):
+                        out[li, t] = self.attention(li, q[li, t:t + 1], [sid], window)[0]
+                    t += 1
+            elif op[0] == "drop":
+                self.drop(sid, op[1])
+            else:
+                self.reposition(sid)
+        return out, sid
 
     # -- introspection ---------------------------------------------------------
     def info(self, sid):

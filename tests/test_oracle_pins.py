@@ -425,7 +425,48 @@ def pin_sliding_window():
         np.testing.assert_allclose(got[0], want, atol=1e-12)
 
 
-PINS = [pin_inv_freq, pin_partial_rope, pin_sliding_window, pin_rope_complex_form, pin_rope_matrix_identities,
+def pin_replay_attention():
+    """Restore attention: a program of appends alone is plain causal softmax
+    attention (textbook, scipy); the Figure 10 program gives each query the
+    keys and positions the worked example lists."""
+    rng = np.random.default_rng(16)
+    c = _tiny_cache(dtype="f64", d=16, hq=4, hkv=2, theta=1.0e4)
+    n = 25
+    q = _rand(rng, 1, n, 4, 16)
+    k, v = _tokens(rng, c, n)
+    out, _ = c.replay_attention([("append", 10), ("append", 15)], q, k, v)
+    for t in range(n):
+        want = _dense_attention(q[0, t], k[0, : t + 1], v[0, : t + 1], t, np.arange(t + 1),
+                                c.freq, 2)
+        np.testing.assert_allclose(out[0, t], want, atol=1e-12)
+    # Figure 10: A B C | drop B, repos | D | drop D | E | repos | F
+    g = _gold("fig10_positions.json")
+    names = [op[1] for op in g["ops"] if op[0] == "append"]
+    idx = {name: i for i, name in enumerate(names)}
+    program = []
+    for op in g["ops"]:
+        if op[0] == "append":
+            program.append(("append", 1))
+        elif op[0] == "drop":
+            program.append(("drop", [(idx[x], idx[x] + 1) for x in op[1]]))
+        elif op[0] == "repos":
+            program.append(("repos",))
+    m = len(names)
+    q = _rand(rng, 1, m, 4, 16)
+    k, v = _tokens(rng, c, m)
+    out, _ = c.replay_attention(program, q, k, v)
+    for op in g["ops"]:
+        if op[0] != "query":
+            continue
+        x = idx[op[1]]
+        seen = op[2]
+        keys = [idx[nm] for nm in seen]
+        pos = np.array([seen[nm] for nm in seen])
+        want = _dense_attention(q[0, x], k[0][keys], v[0][keys], seen[op[1]], pos, c.freq, 2)
+        np.testing.assert_allclose(out[0, x], want, atol=1e-12)
+
+
+PINS = [pin_inv_freq, pin_partial_rope, pin_sliding_window, pin_replay_attention, pin_rope_complex_form, pin_rope_matrix_identities,
         pin_rope_relative, pin_bf16_rounding, pin_fig10_positions,
         pin_fig5_histories, pin_drop_semantics,
         pin_reposition_positions_and_gather, pin_no_drop_unchanged,
