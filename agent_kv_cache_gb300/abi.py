@@ -48,6 +48,15 @@ class AkvConfig(ctypes.Structure):
                 ("rope_theta", ctypes.c_double), ("rope_dim", ctypes.c_int32)]
 
 
+class AkvOp(ctypes.Structure):
+    """struct akv_op"""
+    _fields_ = [("kind", ctypes.c_int32), ("count", ctypes.c_int32),
+                ("ranges", ctypes.POINTER(ctypes.c_int64))]
+
+
+AKV_OP_APPEND, AKV_OP_DROP, AKV_OP_REPOS = 0, 1, 2
+
+
 class AkvSeqInfo(ctypes.Structure):
     """struct akv_seq_info_t"""
     _fields_ = [("n_logical", ctypes.c_int64), ("n_held", ctypes.c_int64),
@@ -93,6 +102,8 @@ SIGNATURES = {
     "akv_kernel_launches": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "akv_set_decode_waves": (ctypes.c_int, [_P, _I32]),
     "akv_set_layer_window": (ctypes.c_int, [_P, _I32, _I32]),
+    "akv_restore_attention": (ctypes.c_int, [_P, ctypes.POINTER(AkvOp), _I32, _I32, _P, _P, _P,
+                                             _I32, _P]),
     "akv_decode_attention_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                     ctypes.c_double, _P, _P, _P, _I32, _I32,
                                                     _PI32, _PI32, _P, _P, _I32, _P]),
@@ -272,6 +283,33 @@ def akv_sync_errors(cache):
     if rc not in (AKV_OK, AKV_EDEVICE):
         _check(rc, cache)
     return w.value
+
+
+def make_program(program):
+    """Python program [("append", n) | ("drop", ranges) | ("repos",)] -> akv_op array.
+
+    Returns (array, keep-alive list)."""
+    keep = []
+    arr = (AkvOp * max(1, len(program)))()
+    for i, op in enumerate(program):
+        if op[0] == "append":
+            arr[i] = AkvOp(AKV_OP_APPEND, int(op[1]), None)
+        elif op[0] == "drop":
+            r = np.ascontiguousarray(np.asarray(op[1], dtype=np.int64).reshape(-1, 2))
+            keep.append(r)
+            arr[i] = AkvOp(AKV_OP_DROP, r.shape[0], r.ctypes.data_as(_PI64))
+        elif op[0] == "repos":
+            arr[i] = AkvOp(AKV_OP_REPOS, 0, None)
+        else:
+            raise ValueError(op)
+    return arr, keep
+
+
+def akv_restore_attention(cache, program, layer, q, k_raw, v, n_tokens, out):
+    arr, keep = make_program(program)
+    _check(lib().akv_restore_attention(cache, arr, len(program), layer, q, k_raw, v, n_tokens,
+                                       out), cache)
+    del keep
 
 
 def akv_set_layer_window(cache, layer, window):

@@ -65,6 +65,18 @@ class Cache:
     def reposition(self, seqs):
         abi.akv_reposition(self.handle, seqs)
 
+    def restore_attention(self, program, layer, q, k_raw, v, out=None):
+        """Segment-batch restore attention of one layer: q [T, hq, D],
+        k_raw/v [T, hkv, D] device tensors; returns out [T, hq, D] fp32."""
+        torch = self.torch
+        n = q.shape[0]
+        if out is None:
+            out = torch.empty((n, self.hq, self.d), dtype=torch.float32, device="cuda")
+        assert q.is_contiguous() and k_raw.is_contiguous() and v.is_contiguous()
+        abi.akv_restore_attention(self.handle, program, layer, q.data_ptr(), k_raw.data_ptr(),
+                                  v.data_ptr(), n, out.data_ptr())
+        return out
+
     def set_layer_window(self, layer, window):
         abi.akv_set_layer_window(self.handle, layer, window)
 

@@ -188,6 +188,8 @@ struct akv_cache {
   int mma_blocks_per_sm = 0;
   int32_t decode_waves = 1;
   int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
+  void* d_restore = nullptr;       // temporary key/value versions of restore attention
+  size_t restore_cap = 0;
 };
 
 namespace {
@@ -283,6 +285,7 @@ void destroy(akv_cache* c) {
   cudaFree(c->d_err);
   for (auto& pl : c->plans) cudaFree(pl.d);
   cudaFree(c->d_counters);
+  cudaFree(c->d_restore);
   for (Stage& s : c->stages) {
     if (s.h) cudaFreeHost(s.h);
     if (s.d) cudaFree(s.d);
@@ -946,6 +949,112 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   CK(launch_decode(a, plan->combine, n_seqs, reinterpret_cast<const int32_t*>(plan->d + o_item0),
                    reinterpret_cast<const int32_t*>(plan->d + o_splits), c->stream));
   c->launches += plan->combine ? 2 : 1;
+  return AKV_OK;
+}
+
+// ---- segment-batch restore attention -------------------------------------------
+
+int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_t layer,
+                          const void* q, const void* k_raw, const void* v, int32_t n_tokens,
+                          float* out) {
+  if (!c || n_ops < 0 || (n_ops > 0 && !ops) || n_tokens < 0) return AKV_EINVAL;
+  if (layer < 0 || layer >= c->cfg.layers) return fail(c, AKV_EINVAL, "layer %d out of range", layer);
+  if (n_tokens > 0 && (!q || !k_raw || !v || !out)) return AKV_EINVAL;
+  // plan: times, eras, era slots (page 1 A.1.1: split at every drop/repos)
+  constexpr int32_t kNever = INT32_MAX;
+  std::vector<int32_t> held, pending;
+  std::vector<char> alive(n_tokens, 0);
+  std::vector<int32_t> birth(n_tokens, 0), death(n_tokens, kNever);
+  std::vector<RestoreKey> keys;
+  std::vector<RestoreQuery> queries(n_tokens);
+  int32_t next = 0, clock = 0;
+  auto close_era = [&]() {
+    const int32_t off = (int32_t)keys.size();
+    for (size_t slot = 0; slot < held.size(); ++slot) {
+      const int32_t t = held[slot];
+      keys.push_back({t, (int32_t)slot, birth[t], death[t]});
+    }
+    for (int32_t t : pending) queries[t].era_off = off;
+    pending.clear();
+    std::vector<int32_t> keep;
+    for (int32_t t : held)
+      if (alive[t]) keep.push_back(t);
+    held.swap(keep);
+  };
+  for (int32_t i = 0; i < n_ops; ++i) {
+    const akv_op& op = ops[i];
+    if (op.kind == AKV_OP_APPEND) {
+      if (op.count < 0 || next + (int64_t)op.count > n_tokens)
+        return fail(c, AKV_EINVAL, "program appends more than %d tokens", n_tokens);
+      for (int32_t k = 0; k < op.count; ++k) {
+        const int32_t t = next++;
+        birth[t] = clock++;
+        alive[t] = 1;
+        held.push_back(t);
+        if ((int64_t)held.size() > c->cfg.max_slots)
+          return fail(c, AKV_ECAPACITY, "restore position reaches max_slots %d", c->cfg.max_slots);
+        const int32_t pos = (int32_t)held.size() - 1;
+        queries[t] = {t, pos, birth[t], 0, pos + 1};
+        pending.push_back(t);
+      }
+    } else if (op.kind == AKV_OP_DROP) {
+      if (op.count < 0 || (op.count > 0 && !op.ranges)) return fail(c, AKV_EINVAL, "bad drop op");
+      for (int32_t r = 0; r < op.count; ++r) {
+        const int64_t b = op.ranges[2 * r], e = op.ranges[2 * r + 1];
+        if (b < 0 || e < b || e > next)
+          return fail(c, AKV_ERANGE, "drop range [%lld, %lld) outside [0, %d)", (long long)b,
+                      (long long)e, next);
+        for (int64_t t = b; t < e; ++t)
+          if (alive[t]) { alive[t] = 0; death[t] = clock; }
+      }
+      ++clock;
+    } else if (op.kind == AKV_OP_REPOS) {
+      close_era();
+      ++clock;
+    } else {
+      return fail(c, AKV_EINVAL, "unknown op kind %d", op.kind);
+    }
+  }
+  if (next != n_tokens) return fail(c, AKV_EINVAL, "program appends %d tokens, not %d", next, n_tokens);
+  close_era();
+  if (n_tokens == 0) return AKV_OK;
+
+  const size_t elem = c->cfg.dtype == AKV_DTYPE_BF16 ? 2 : 4;
+  const size_t need = 2 * keys.size() * (size_t)c->cfg.hkv * c->cfg.head_dim * elem;
+  if (need > c->restore_cap) {
+    CK(cudaStreamSynchronize(c->stream));
+    cudaFree(c->d_restore);
+    c->d_restore = nullptr;
+    c->restore_cap = 0;
+    CK(cudaMalloc(&c->d_restore, need));
+    c->restore_cap = need;
+  }
+  Blob blob;
+  const size_t o_keys = blob.put(keys.data(), keys.size());
+  const size_t o_q = blob.put(queries.data(), queries.size());
+  char* d = nullptr;
+  int rc = upload(c, blob, nullptr, &d);
+  if (rc) return rc;
+  RestoreArgs a{};
+  a.g = c->g;
+  a.keys = reinterpret_cast<const RestoreKey*>(d + o_keys);
+  a.n_keys = (int32_t)keys.size();
+  a.queries = reinterpret_cast<const RestoreQuery*>(d + o_q);
+  a.n_queries = n_tokens;
+  a.q = q;
+  a.k_raw = k_raw;
+  a.v = v;
+  a.n_tokens = n_tokens;
+  a.k_era = c->d_restore;
+  a.v_era = static_cast<char*>(c->d_restore) + need / 2;
+  a.out = out;
+  a.cs = c->d_cs;
+  a.max_pos = c->cfg.max_slots;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+  a.window = c->windows[layer];
+  a.err = c->d_err;
+  CK(launch_restore(a, c->stream));
+  c->launches += 2;
   return AKV_OK;
 }
 

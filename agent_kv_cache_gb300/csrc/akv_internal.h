@@ -114,6 +114,30 @@ struct DecodeArgs {
 };
 constexpr int kDecodeMaxTiles = 512;   // 16-token tiles in one split of the tensor-core path
 
+// ---- segment-batch restore attention -------------------------------------------
+struct RestoreKey { int32_t tok, pos, birth, death; };      // one era key row
+struct RestoreQuery { int32_t tok, pos, time, era_off, key_end; };
+struct RestoreArgs {
+  Geom g;
+  const RestoreKey* keys;
+  int32_t n_keys;
+  const RestoreQuery* queries;
+  int32_t n_queries;
+  const void* q;        // [T][hq][D] pool dtype, pre-RoPE
+  const void* k_raw;    // [T][hkv][D] pool dtype, pre-RoPE
+  const void* v;        // [T][hkv][D]
+  int32_t n_tokens;
+  void* k_era;          // [n_keys][hkv][D] temporary key versions
+  void* v_era;
+  float* out;           // [T][hq][D]
+  const float2* cs;
+  int32_t max_pos;
+  float scale_log2;
+  int32_t window;
+  uint32_t* err;
+};
+cudaError_t launch_restore(const RestoreArgs& a, cudaStream_t st);
+
 // Launchers (akv_kernels.cu / akv_decode.cu).  All enqueue on `st`.
 struct AppendLimits { int32_t n_items, n_ids, n_act, max_seqs; };
 cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* items,

@@ -185,6 +185,41 @@ int akv_decode_attention(akv_cache* cache, int32_t layer, const void* q,
  * W = 0 (the default) is full attention.  Errors: AKV_EINVAL. */
 int akv_set_layer_window(akv_cache* cache, int32_t layer, int32_t window);
 
+/* ---- segment-batch restore attention ------------------------------------
+ * Paper review 4.2.2 / 4.2.3 / Appendix A.1.1: after eviction, a sequence is
+ * rebuilt by one forward over its whole operation program, in which each
+ * token's query must see exactly the keys it saw originally -- keys dropped
+ * later included -- at the positions of that time (temporary rotated
+ * versions).  The program is an array of operations applied to an empty
+ * sequence: */
+#define AKV_OP_APPEND 0   /* append `count` tokens (the next rows of q/k/v) */
+#define AKV_OP_DROP 1     /* drop `count` logical ranges ranges[2i]..ranges[2i+1] */
+#define AKV_OP_REPOS 2    /* reposition */
+typedef struct akv_op {
+  int32_t kind;
+  int32_t count;
+  const int64_t* ranges;  /* host; AKV_OP_DROP only */
+} akv_op;
+
+/* Attention outputs of one layer for every appended token of the program,
+ * in one batched pass: out[t] = softmax(q_t' K^T / sqrt(D)) V over the keys
+ * active when token t was appended (t included), keys and query rotated to
+ * the positions of that moment.  Sliding window: the layer's
+ * akv_set_layer_window setting.
+ *   q    : device [n_tokens][hq][D] pool dtype, before RoPE
+ *   k_raw, v : device [n_tokens][hkv][D] pool dtype, K before RoPE
+ *   out  : device [n_tokens][hq][D] fp32
+ * No sequence is read or changed: rebuild the cache state by replaying the
+ * program with akv_append / akv_drop / akv_reposition.  The library keeps a
+ * scratch buffer for the temporary key versions and grows it (cudaMalloc,
+ * which waits for the device) when a program needs more.
+ * Errors: AKV_EINVAL (program appends a different number of tokens than
+ * n_tokens, bad op), AKV_ERANGE (drop range), AKV_ECAPACITY (a position
+ * reaches max_slots). */
+int akv_restore_attention(akv_cache* cache, const akv_op* ops, int32_t n_ops, int32_t layer,
+                          const void* q, const void* k_raw, const void* v,
+                          int32_t n_tokens, float* out);
+
 /* ---- decode attention that allocates nothing (no counterpart in the paper) ----
  *
  * For callers that cannot allocate device memory: applications that reserve

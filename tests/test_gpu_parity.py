@@ -242,6 +242,93 @@ def test_sliding_window_over_positions(dtype, page, G, D):
         t.check(s)
 
 
+def _random_program(rng, n_tokens, n_ops):
+    prog, appended = [], 0
+    per = max(1, n_tokens // max(1, n_ops // 2))
+    while appended < n_tokens:
+        kind = rng.choice(["append", "append", "drop", "repos"]) if appended else "append"
+        if kind == "append":
+            k = int(min(n_tokens - appended, rng.integers(1, per + 1)))
+            prog.append(("append", k))
+            appended += k
+        elif kind == "drop":
+            b = int(rng.integers(0, appended))
+            prog.append(("drop", [(b, int(min(appended, b + rng.integers(1, 40))))]))
+        else:
+            prog.append(("repos",))
+    return prog
+
+
+RESTORE = [
+    # dtype, page, G, D, rope_dim, window
+    ("bf16", 16, 4, 128, 0, 0),
+    ("bf16", 16, 8, 64, 0, 0),
+    ("fp32", 16, 2, 64, 0, 0),
+    ("bf16", 16, 4, 128, 64, 0),
+    ("bf16", 16, 4, 128, 0, 24),
+    ("fp32", 4, 16, 128, 32, 7),
+]
+
+
+@pytest.mark.parametrize("dtype,page,G,D,R,W", RESTORE)
+@pytest.mark.parametrize("seed", [1, 2])
+def test_restore_attention_random_programs(dtype, page, G, D, R, W, seed):
+    """Every appended token's restore attention equals its attention at the
+    time it was appended (oracle replay), keys dropped later included."""
+    rng = np.random.default_rng(seed * 100 + D + G + R + W)
+    t = Twin(layers=2, hq=2 * G, hkv=2, head_dim=D, page_size=page, dtype=dtype,
+             rope_theta=1e4, max_pages=512, max_seqs=4, max_slots=2048, seed=seed, rope_dim=R)
+    if W:
+        t.set_window(1, W)
+    prog = _random_program(rng, int(rng.integers(150, 400)), 16)
+    t.restore(prog, layer=0)
+    t.restore(prog, layer=1)
+    # the cache state is rebuilt by replaying the program through the API
+    s = t.create()
+    for op in prog:
+        if op[0] == "append":
+            t.append([s], [op[1]])
+        elif op[0] == "drop":
+            t.drop(s, op[1])
+        else:
+            t.reposition([s])
+    t.check(s)
+
+
+def test_restore_attention_figure10_program():
+    g = json.load(open(os.path.join(GOLD, "fig10_positions.json")))
+    names = [op[1] for op in g["ops"] if op[0] == "append"]
+    idx = {nm: i for i, nm in enumerate(names)}
+    prog = []
+    for op in g["ops"]:
+        if op[0] == "append":
+            prog.append(("append", 1))
+        elif op[0] == "drop":
+            prog.append(("drop", [(idx[x], idx[x] + 1) for x in op[1]]))
+        elif op[0] == "repos":
+            prog.append(("repos",))
+    t = Twin(layers=1, hq=8, hkv=2, head_dim=64, page_size=16, dtype="bf16", seed=10)
+    t.restore(prog)
+    t2 = Twin(layers=1, hq=8, hkv=2, head_dim=64, page_size=16, dtype="fp32", seed=10)
+    t2.restore(prog)
+
+
+def test_restore_rejects_bad_programs():
+    t = Twin(layers=1, hq=8, hkv=2, head_dim=64, page_size=16, dtype="bf16", max_slots=64)
+    z = torch.zeros((10, 8, 64), dtype=torch.bfloat16, device="cuda")
+    zk = torch.zeros((10, 2, 64), dtype=torch.bfloat16, device="cuda")
+    for prog, code in [([("append", 9)], abi.AKV_EINVAL),
+                       ([("append", 11)], abi.AKV_EINVAL),
+                       ([("append", 5), ("drop", [(3, 7)]), ("append", 5)], abi.AKV_ERANGE)]:
+        with pytest.raises(abi.AkvError) as e:
+            t.gpu.restore_attention(prog, 0, z, zk, zk)
+        assert e.value.code == code
+    t3 = Twin(layers=1, hq=8, hkv=2, head_dim=64, page_size=16, dtype="bf16", max_slots=8)
+    with pytest.raises(abi.AkvError) as e:          # positions reach max_slots
+        t3.gpu.restore_attention([("append", 10)], 0, z, zk, zk)
+    assert e.value.code == abi.AKV_ECAPACITY
+
+
 def _history(t, ops, toks):
     s = t.create()
     names = {}

@@ -73,6 +73,7 @@ class Twin:
                          max_slots, rope_theta, phys_layers=phys_layers, rope_dim=rope_dim)
         self.orc = OracleCache(hq, hkv, head_dim, rope_theta, dtype, layers=range(layers),
                                page_size=page_size, rope_dim=rope_dim)
+        self.orc.freq_theta = rope_theta
         self.windows = {}
         self.L, self.hq, self.hkv, self.d, self.S = layers, hq, hkv, head_dim, page_size
         self.dtype = dtype
@@ -162,6 +163,32 @@ class Twin:
             tmax, tmean = ATTN_TOL[self.dtype]
             assert err.max() <= tmax and err.mean() <= tmean, (l, err.max(), err.mean())
         return worst
+
+    def restore(self, program, layer=0):
+        """Restore attention of one layer over `program` on the GPU vs the
+        oracle's replay; returns (max, mean) abs error."""
+        n = sum(op[1] for op in program if op[0] == "append")
+        tag = self.next_tag
+        self.next_tag += 1
+        w = self.width
+        q = synth.block(self.seed, tag, synth.KIND_Q, layer, 0, n * self.hq * self.d, w)
+        k = synth.block(self.seed, tag, synth.KIND_K, layer, 0, n * self.hkv * self.d, w)
+        v = synth.block(self.seed, tag, synth.KIND_V, layer, 0, n * self.hkv * self.d, w)
+        q = q.reshape(n, self.hq, self.d)
+        k = k.reshape(n, self.hkv, self.d)
+        v = v.reshape(n, self.hkv, self.d)
+        dev = lambda x: torch.from_numpy(x).to(self.tdtype).cuda().contiguous()
+        got = self.gpu.restore_attention(program, layer, dev(q), dev(k), dev(v))
+        got = got.double().cpu().numpy()
+        o = OracleCache(self.hq, self.hkv, self.d, self.orc.freq_theta, self.dtype, layers=(0,),
+                        page_size=self.S, rope_dim=self.orc.rope_dim)
+        want, _ = o.replay_attention(program, q[None], k[None], v[None],
+                                     window=self.windows.get(layer, 0))
+        err = np.abs(got - want[0])
+        tmax, tmean = ATTN_TOL[self.dtype]
+        assert err.max() <= tmax and err.mean() <= tmean, (err.max(), err.mean())
+        assert self.gpu.sync_errors() == 0
+        return float(err.max()), float(err.mean())
 
     # -- comparison --------------------------------------------------------
     def check(self, g, kv=True):
