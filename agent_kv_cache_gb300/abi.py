@@ -101,6 +101,7 @@ SIGNATURES = {
     "akv_sync_errors": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "akv_kernel_launches": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "akv_set_decode_waves": (ctypes.c_int, [_P, _I32]),
+    "akv_set_restore_tensor_cores": (ctypes.c_int, [_P, _I32]),
     "akv_set_layer_window": (ctypes.c_int, [_P, _I32, _I32]),
     "akv_restore_attention": (ctypes.c_int, [_P, ctypes.POINTER(AkvOp), _I32, _I32, _P, _P, _P,
                                              _I32, _P]),
@@ -318,6 +319,10 @@ def akv_set_layer_window(cache, layer, window):
 
 def akv_set_decode_waves(cache, waves):
     _check(lib().akv_set_decode_waves(cache, waves), cache)
+
+
+def akv_set_restore_tensor_cores(cache, enable):
+    _check(lib().akv_set_restore_tensor_cores(cache, 1 if enable else 0), cache)
 
 
 def akv_kernel_launches(cache):

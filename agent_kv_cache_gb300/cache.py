@@ -77,6 +77,9 @@ class Cache:
                                   v.data_ptr(), n, out.data_ptr())
         return out
 
+    def set_restore_tensor_cores(self, enable):
+        abi.akv_set_restore_tensor_cores(self.handle, enable)
+
     def set_layer_window(self, layer, window):
         abi.akv_set_layer_window(self.handle, layer, window)
 

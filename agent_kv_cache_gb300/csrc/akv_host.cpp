@@ -190,6 +190,7 @@ struct akv_cache {
   int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
   void* d_restore = nullptr;       // temporary key/value versions of restore attention
   size_t restore_cap = 0;
+  bool restore_generic = false;    // CUDA-core restore kernel for every shape
 };
 
 namespace {
@@ -268,6 +269,22 @@ int upload(akv_cache* c, const Blob& blob, char* dst, char** dptr) {
   CK(cudaEventRecord(s.ev, c->stream));
   s.used = true;
   *dptr = dst ? dst : s.d;
+  return AKV_OK;
+}
+
+// A descriptor of any size copied to device memory at dst through the
+// staging ring, one staging block per copy.
+int upload_large(akv_cache* c, const Blob& blob, char* dst) {
+  for (size_t off = 0; off < blob.b.size(); off += c->stage_bytes) {
+    const size_t m = std::min(c->stage_bytes, blob.b.size() - off);
+    Stage& s = c->stages[c->stage_next];
+    c->stage_next = (c->stage_next + 1) % kStages;
+    if (s.used) CK(cudaEventSynchronize(s.ev));
+    std::memcpy(s.h, blob.b.data() + off, m);
+    CK(cudaMemcpyAsync(dst + off, s.h, m, cudaMemcpyHostToDevice, c->stream));
+    CK(cudaEventRecord(s.ev, c->stream));
+    s.used = true;
+  }
   return AKV_OK;
 }
 
@@ -1019,8 +1036,28 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
   close_era();
   if (n_tokens == 0) return AKV_OK;
 
+  // tensor-core path: tiles of consecutive query tokens of one era
+  std::vector<RestoreTile> tiles;
+  const bool mma = restore_mma_supported(c->g) && !c->restore_generic;
+  if (mma) {
+    const int tt = restore_tile_tokens(c->g);
+    const int32_t W = c->windows[layer];
+    for (int32_t t = 0; t < n_tokens;) {
+      int32_t e = t + 1;
+      while (e < n_tokens && e - t < tt && queries[e].era_off == queries[t].era_off) ++e;
+      const int32_t lo = W > 0 ? std::max(0, queries[t].pos - W + 1) : 0;
+      tiles.push_back({queries[t].era_off, t, e - t, lo, queries[e - 1].key_end});
+      t = e;
+    }
+  }
+  Blob blob;
+  const size_t o_keys = blob.put(keys.data(), keys.size());
+  const size_t o_q = blob.put(queries.data(), queries.size());
+  const size_t o_t = blob.put(tiles.data(), tiles.size());
+  // scratch: [K versions | V versions | descriptor]
   const size_t elem = c->cfg.dtype == AKV_DTYPE_BF16 ? 2 : 4;
-  const size_t need = 2 * keys.size() * (size_t)c->cfg.hkv * c->cfg.head_dim * elem;
+  const size_t half = (keys.size() * (size_t)c->cfg.hkv * c->cfg.head_dim * elem + 255) & ~size_t(255);
+  const size_t need = 2 * half + blob.b.size();
   if (need > c->restore_cap) {
     CK(cudaStreamSynchronize(c->stream));
     cudaFree(c->d_restore);
@@ -1029,13 +1066,13 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
     CK(cudaMalloc(&c->d_restore, need));
     c->restore_cap = need;
   }
-  Blob blob;
-  const size_t o_keys = blob.put(keys.data(), keys.size());
-  const size_t o_q = blob.put(queries.data(), queries.size());
-  char* d = nullptr;
-  int rc = upload(c, blob, nullptr, &d);
+  char* d = static_cast<char*>(c->d_restore) + 2 * half;
+  int rc = upload_large(c, blob, d);
   if (rc) return rc;
   RestoreArgs a{};
+  a.tiles = reinterpret_cast<const RestoreTile*>(d + o_t);
+  a.n_tiles = (int32_t)tiles.size();
+  a.use_mma = mma;
   a.g = c->g;
   a.keys = reinterpret_cast<const RestoreKey*>(d + o_keys);
   a.n_keys = (int32_t)keys.size();
@@ -1046,7 +1083,7 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
   a.v = v;
   a.n_tokens = n_tokens;
   a.k_era = c->d_restore;
-  a.v_era = static_cast<char*>(c->d_restore) + need / 2;
+  a.v_era = static_cast<char*>(c->d_restore) + half;
   a.out = out;
   a.cs = c->d_cs;
   a.max_pos = c->cfg.max_slots;
@@ -1194,6 +1231,12 @@ int akv_set_decode_waves(akv_cache* c, int32_t waves) {
   if (!c || waves < 1 || waves > 64) return AKV_EINVAL;
   c->decode_waves = waves;
   for (auto& pl : c->plans) pl.epoch = ~0ULL;   // re-plan on the next call
+  return AKV_OK;
+}
+
+int akv_set_restore_tensor_cores(akv_cache* c, int32_t enable) {
+  if (!c || (enable != 0 && enable != 1)) return AKV_EINVAL;
+  c->restore_generic = enable == 0;
   return AKV_OK;
 }
 

@@ -117,6 +117,8 @@ constexpr int kDecodeMaxTiles = 512;   // 16-token tiles in one split of the ten
 // ---- segment-batch restore attention -------------------------------------------
 struct RestoreKey { int32_t tok, pos, birth, death; };      // one era key row
 struct RestoreQuery { int32_t tok, pos, time, era_off, key_end; };
+// tensor-core path: consecutive query tokens of one era, their key range
+struct RestoreTile { int32_t era_off, tok0, n_tok, key_lo, key_hi; };
 struct RestoreArgs {
   Geom g;
   const RestoreKey* keys;
@@ -135,8 +137,13 @@ struct RestoreArgs {
   float scale_log2;
   int32_t window;
   uint32_t* err;
+  const RestoreTile* tiles;   // tensor-core path only
+  int32_t n_tiles;
+  int32_t use_mma;
 };
 cudaError_t launch_restore(const RestoreArgs& a, cudaStream_t st);
+bool restore_mma_supported(const Geom& g);
+int restore_tile_tokens(const Geom& g);       // query tokens per tensor-core block
 
 // Launchers (akv_kernels.cu / akv_decode.cu).  All enqueue on `st`.
 struct AppendLimits { int32_t n_items, n_ids, n_act, max_seqs; };

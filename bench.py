@@ -456,6 +456,103 @@ def gpu_arm(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# segment-batch restore attention (its own line: --restore)
+# ---------------------------------------------------------------------------
+
+RESTORE_SEED = traces.seed_for(5)
+
+
+def restore_visible(prog):
+    """Sum over appended tokens of the keys each one attends (itself included)."""
+    alive = vis = 0
+    for op in prog:
+        if op[0] == "append":
+            n = op[1]
+            vis += n * alive + n * (n + 1) // 2
+            alive += n
+        elif op[0] == "drop":
+            alive -= sum(e - b for b, e in op[1])
+    return vis
+
+
+def restore_arm(args):
+    """Restore attention of one long agent sequence on every layer: per layer
+    one akv_restore_attention call over the whole program (~34k tokens,
+    10 repositions).  FLOPs are algorithmic: 4 * D * hq per visible
+    (query, key) pair (Q K^T and P V)."""
+    import torch
+    from agent_kv_cache_gb300 import Cache, build
+    from workloads import device as dev
+    build()
+    dev.build()
+    sh = SHAPE
+    prog = traces.restore_program(RESTORE_SEED)
+    n = sum(op[1] for op in prog if op[0] == "append")
+    cache = Cache(sh.layers, sh.hq, sh.hkv, sh.head_dim, sh.page_size, sh.dtype, 16, 2, n + 64,
+                  sh.rope_theta)
+    if args.restore_cuda_cores:
+        cache.set_restore_tensor_cores(False)
+    w = synth.width_for(sh.dtype)
+    st = cache.stream
+    q = torch.empty((n, sh.hq, sh.head_dim), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((n, sh.hkv, sh.head_dim), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    keep = [dev.fill(x, [(synth.stream_key(RESTORE_SEED, 1, kind, 0), 0, 0)], x.numel(), w)
+            for x, kind in ((q, synth.KIND_Q), (k, synth.KIND_K), (v, synth.KIND_V))]
+    out = torch.empty((n, sh.hq, sh.head_dim), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    del keep
+    flops = 4.0 * sh.head_dim * sh.hq * restore_visible(prog)
+    for _ in range(args.warmup):
+        for l in range(sh.layers):
+            cache.restore_attention(prog, l, q, k, v, out=out)
+    torch.cuda.synchronize()
+    assert cache.sync_errors() == 0
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps * sh.layers)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = cache.kernel_launches()
+    with torch.cuda.stream(st):
+        start.record(st)
+        for i in range(args.steps):
+            for l in range(sh.layers):
+                e = evs[i * sh.layers + l]
+                e[0].record(st)
+                cache.restore_attention(prog, l, q, k, v, out=out)
+                e[1].record(st)
+        stop.record(st)
+    torch.cuda.synchronize()
+    assert cache.sync_errors() == 0
+    launches = (cache.kernel_launches() - n0) // args.steps
+    ms = start.elapsed_time(stop) / args.steps
+    call_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    achieved = flops / (call_ms * 1e-3) / 1e12
+    line = {
+        "metric": "segment-batch restore attention TFLOP/s (algorithmic, visible pairs)",
+        "value": round(sh.layers * flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded SplitMix64 q/K/V)",
+        "config": {"workload": f"{sh.name}-shaped long-running agent sequence: {n} tokens, "
+                               f"{sum(op[0] == 'repos' for op in prog)} repositions, "
+                               f"{sum(op[0] == 'drop' for op in prog)} drop operations; one step "
+                               f"= restore attention on all {sh.layers} layers",
+                   "kernel": "CUDA cores" if args.restore_cuda_cores else "tensor cores (mma.sync)",
+                   "flops_per_layer": flops, "tokens": n},
+        "roofline": {"kernel": "restore attention (temporary key versions + attention)",
+                     "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": "measured sustained" if "bf16_tflops_sustained" in peaks
+                     else "fallback", "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "avg_call_ms": round(call_ms, 3)},
+        "gpu_launches": int(launches),
+    }
+    print(json.dumps(line), flush=True)
+    cache.close()
+
+
 def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -490,6 +587,9 @@ def main():
     ap.add_argument("--impl", choices=["akv", "reference"], default="akv")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--restore", action="store_true",
+                    help="time segment-batch restore attention instead (its own line)")
+    ap.add_argument("--restore-cuda-cores", action="store_true")
     # smaller cases for profiler captures only; a line printed with any of
     # these is marked "profiling case" and is not the benchmark's number
     ap.add_argument("--batch", type=int, default=None)
@@ -504,7 +604,9 @@ def main():
         args.profiling_case = True
     else:
         args.profiling_case = False
-    if args.impl == "reference":
+    if args.restore or args.restore_cuda_cores:
+        restore_arm(args)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         gpu_arm(args)

@@ -211,8 +211,10 @@ typedef struct akv_op {
  *   out  : device [n_tokens][hq][D] fp32
  * No sequence is read or changed: rebuild the cache state by replaying the
  * program with akv_append / akv_drop / akv_reposition.  The library keeps a
- * scratch buffer for the temporary key versions and grows it (cudaMalloc,
- * which waits for the device) when a program needs more.
+ * scratch buffer for the temporary key versions and the program's device
+ * descriptor and grows it (cudaMalloc, which waits for the device) when a
+ * program needs more.  bf16 pools with D 64 or 128 run a tensor-core kernel
+ * (see akv_set_restore_tensor_cores).
  * Errors: AKV_EINVAL (program appends a different number of tokens than
  * n_tokens, bad op), AKV_ERANGE (drop range), AKV_ECAPACITY (a position
  * reaches max_slots). */
@@ -303,6 +305,11 @@ int akv_sync_errors(akv_cache* cache, uint32_t* word);
 /* Tuning: the tensor-core decode plans its split-KV blocks as `waves`
  * whole waves of the blocks that fit the GPU at once (default 1; 1..64). */
 int akv_set_decode_waves(akv_cache* cache, int32_t waves);
+
+/* Kernel choice for akv_restore_attention: 1 (default) = tensor-core
+ * kernel where it applies (bf16 pool, D 64 or 128), 0 = the CUDA-core
+ * kernel for every shape.  Both compute the same attention. */
+int akv_set_restore_tensor_cores(akv_cache* cache, int32_t enable);
 
 /* Number of kernels this cache has launched since creation. */
 int akv_kernel_launches(akv_cache* cache, uint64_t* count);

@@ -66,6 +66,7 @@ over it.
 Parity pins live in ``tests/test_oracle_pins.py``; every function here is
 pinned there (no function is "parity unpinned").
 """
+import bisect
 import copy
 
 import numpy as np
@@ -305,7 +306,7 @@ class OracleCache:
         return out
 
     # -- restore (segment-batch attention), by replay ------------------------------
-    def replay_attention(self, program, q, k_raw, v, window=0):
+    def replay_attention(self, program, q, k_raw, v, window=0, only=None):
         """Attention output of every appended token of ``program``, as it was
         when the token was appended.
 
@@ -313,18 +314,31 @@ class OracleCache:
         applied to a fresh sequence; ``q``, ``k_raw``, ``v`` are
         [layers][T][heads][D] for the T appended tokens in order.  Returns
         [layers][T][Hq][D].  The sequence is left in its final state.
+        With ``only`` (increasing token indices), just those tokens' outputs
+        are computed: ``q`` then holds only their rows, [layers][len(only)],
+        and so does the result.
         """
         q = np.asarray(q, dtype=np.float64)
         sid = self.create()
         out = np.zeros(q.shape[:2] + (self.hq, self.d))
+        row = {t: i for i, t in enumerate(only)} if only is not None else None
+        stops = sorted(row) if row is not None else None
         t = 0
         for op in program:
             if op[0] == "append":
-                for _ in range(op[1]):
-                    self.append(sid, k_raw[:, t:t + 1], v[:, t:t + 1])
-                    for li in range(len(self.layers)):
-                        out[li, t] = self.attention(li, q[li, t:t + 1], [sid], window)[0]
-                    t += 1
+                end = t + op[1]
+                while t < end:
+                    # append up to the next token whose output is wanted
+                    stop = t + 1
+                    if stops is not None:
+                        j = bisect.bisect_left(stops, t)
+                        stop = stops[j] + 1 if j < len(stops) and stops[j] < end else end
+                    self.append(sid, k_raw[:, t:stop], v[:, t:stop])
+                    t = stop
+                    i = t - 1 if row is None else row.get(t - 1)
+                    if i is not None:
+                        for li in range(len(self.layers)):
+                            out[li, i] = self.attention(li, q[li, i:i + 1], [sid], window)[0]
             elif op[0] == "drop":
                 self.drop(sid, op[1])
             else:

@@ -1,5 +1,6 @@
 """Full-size workloads: every sequence's metadata bit-exact against the
-oracle, sampled keys/values/attention element by element.
+oracle, sampled keys/values/attention element by element; restore attention
+of a full-length agent sequence on sampled tokens.
 
 The four large workloads run at their full shapes and batch sizes, through
 the same batched calls as the benchmark (so the same decode launch plan).
@@ -13,9 +14,11 @@ import numpy as np
 import pytest
 import torch
 
-from agent_kv_cache_gb300 import abi, build
+from agent_kv_cache_gb300 import Cache, abi, build
 from fullsize import FullSize
-from workloads import traces
+from oracle.akv_oracle import OracleCache
+from twin import ATTN_TOL
+from workloads import device, synth, traces
 
 pytestmark = pytest.mark.gpu
 
@@ -153,3 +156,40 @@ def test_llama70b_steady_state_fullsize():
     fs.check_metadata()
     fs.check_kv()
     fs.close()
+
+
+def test_restore_llama8b_fullsize():
+    """Restore attention of the long-running agent sequence (~34k tokens,
+    10 repositions, 8B shape) on the tensor-core kernel, exactly as the
+    restore benchmark calls it; 26 sampled tokens (first, last, random)
+    checked against the oracle replay, and a windowed layer."""
+    sh = traces.LLAMA8B
+    seed = traces.seed_for(5)
+    prog = traces.restore_program(seed)
+    n = sum(op[1] for op in prog if op[0] == "append")
+    H, D, Hq = sh.hkv, sh.head_dim, sh.hq
+    w = synth.width_for(sh.dtype)
+    gpu = Cache(2, Hq, H, D, sh.page_size, sh.dtype, 16, 2, n + 64, sh.rope_theta)
+    gpu.set_layer_window(1, 4096)
+    q = torch.empty((n, Hq, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((n, H, D), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    keep = [device.fill(x, [(synth.stream_key(seed, 1, kind, 0), 0, 0)], x.numel(), w)
+            for x, kind in ((q, synth.KIND_Q), (k, synth.KIND_K), (v, synth.KIND_V))]
+    torch.cuda.synchronize()
+    del keep
+    outs = [gpu.restore_attention(prog, l, q, k, v).double().cpu().numpy() for l in (0, 1)]
+    assert gpu.sync_errors() == 0
+    rng = np.random.default_rng(11)
+    only = sorted(set([0, n - 1] + rng.integers(0, n, 24).tolist()))
+    kk = synth.block(seed, 1, synth.KIND_K, 0, 0, n * H * D, w).reshape(1, n, H, D)
+    vv = synth.block(seed, 1, synth.KIND_V, 0, 0, n * H * D, w).reshape(1, n, H, D)
+    qq = np.stack([synth.block(seed, 1, synth.KIND_Q, 0, t * Hq * D, Hq * D, w).reshape(Hq, D)
+                   for t in only])[None]
+    for l, win in ((0, 0), (1, 4096)):
+        o = OracleCache(Hq, H, D, sh.rope_theta, sh.dtype, layers=(0,), page_size=sh.page_size)
+        want, _ = o.replay_attention(prog, qq, kk, vv, window=win, only=only)
+        err = np.abs(outs[l][only] - want[0])
+        tmax, tmean = ATTN_TOL[sh.dtype]
+        assert err.max() <= tmax and err.mean() <= tmean, (l, err.max(), err.mean())
+    gpu.close()

@@ -260,24 +260,33 @@ def _random_program(rng, n_tokens, n_ops):
 
 
 RESTORE = [
-    # dtype, page, G, D, rope_dim, window
-    ("bf16", 16, 4, 128, 0, 0),
-    ("bf16", 16, 8, 64, 0, 0),
-    ("fp32", 16, 2, 64, 0, 0),
-    ("bf16", 16, 4, 128, 64, 0),
-    ("bf16", 16, 4, 128, 0, 24),
-    ("fp32", 4, 16, 128, 32, 7),
+    # dtype, page, G, D, rope_dim, window, tensor cores
+    ("bf16", 16, 4, 128, 0, 0, True),
+    ("bf16", 16, 4, 128, 0, 0, False),
+    ("bf16", 16, 8, 64, 0, 0, True),
+    ("bf16", 16, 8, 64, 0, 0, False),
+    ("bf16", 16, 1, 128, 0, 0, True),
+    ("bf16", 16, 2, 64, 0, 0, True),
+    ("bf16", 8, 16, 64, 32, 0, True),
+    ("fp32", 16, 2, 64, 0, 0, True),
+    ("bf16", 16, 4, 128, 64, 0, True),
+    ("bf16", 16, 4, 128, 64, 0, False),
+    ("bf16", 16, 4, 128, 0, 24, True),
+    ("bf16", 16, 2, 128, 0, 100, True),
+    ("fp32", 4, 16, 128, 32, 7, True),
 ]
 
 
-@pytest.mark.parametrize("dtype,page,G,D,R,W", RESTORE)
+@pytest.mark.parametrize("dtype,page,G,D,R,W,tc", RESTORE)
 @pytest.mark.parametrize("seed", [1, 2])
-def test_restore_attention_random_programs(dtype, page, G, D, R, W, seed):
+def test_restore_attention_random_programs(dtype, page, G, D, R, W, tc, seed):
     """Every appended token's restore attention equals its attention at the
-    time it was appended (oracle replay), keys dropped later included."""
+    time it was appended (oracle replay), keys dropped later included.
+    bf16 runs both the tensor-core and the CUDA-core kernel."""
     rng = np.random.default_rng(seed * 100 + D + G + R + W)
     t = Twin(layers=2, hq=2 * G, hkv=2, head_dim=D, page_size=page, dtype=dtype,
              rope_theta=1e4, max_pages=512, max_seqs=4, max_slots=2048, seed=seed, rope_dim=R)
+    t.gpu.set_restore_tensor_cores(tc)
     if W:
         t.set_window(1, W)
     prog = _random_program(rng, int(rng.integers(150, 400)), 16)
@@ -293,6 +302,31 @@ def test_restore_attention_random_programs(dtype, page, G, D, R, W, seed):
         else:
             t.reposition([s])
     t.check(s)
+
+
+@pytest.mark.parametrize("tc", [True, False])
+def test_restore_attention_long_program(tc):
+    """A 2000-token program with few repositions: eras of thousands of keys
+    (many 64-key tiles per query tile), drops that empty whole tiles, and a
+    query tile that straddles an era boundary."""
+    rng = np.random.default_rng(77)
+    prog, appended = [], 0
+    while appended < 2000:
+        n = int(rng.integers(1, 300))
+        prog.append(("append", n))
+        appended += n
+        u = rng.random()
+        if u < 0.5:
+            b = int(rng.integers(0, appended))
+            prog.append(("drop", [(b, int(min(appended, b + rng.integers(1, 200))))]))
+        elif u < 0.7:
+            prog.append(("repos",))
+    t = Twin(layers=2, hq=8, hkv=2, head_dim=128, page_size=16, dtype="bf16", rope_theta=5e5,
+             max_pages=1024, max_seqs=4, max_slots=8192, seed=5)
+    t.gpu.set_restore_tensor_cores(tc)
+    t.set_window(1, 700)
+    t.restore(prog, layer=0)
+    t.restore(prog, layer=1)
 
 
 def test_restore_attention_figure10_program():

@@ -243,3 +243,20 @@ def steady_state(seed, n_seqs=64, n_turns=100, sys_len=1024, decode_per_turn=64,
             turns.append(Turn(tl, drops, repos))
         out.append(turns)
     return out
+
+
+def restore_program(seed, n_turns=30, sys_len=1024, decode_per_turn=64, active_cap=16384):
+    """Operation program of one long-running agent sequence (the steady-state
+    schedule above, one sequence) for restore attention: the system prompt,
+    then per turn the tool response and its decoded tokens as one append, the
+    turn's drops of the oldest tool responses and its reposition."""
+    turns = steady_state(seed, n_seqs=1, n_turns=n_turns, sys_len=sys_len,
+                         decode_per_turn=decode_per_turn, active_cap=active_cap)[0]
+    prog = [("append", sys_len)]
+    for t in turns:
+        prog.append(("append", t.tool_len + decode_per_turn))
+        if t.drop_ranges:
+            prog.append(("drop", list(t.drop_ranges)))
+        if t.repos:
+            prog.append(("repos",))
+    return prog
