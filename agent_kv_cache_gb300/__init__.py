@@ -8,6 +8,6 @@ and streams).
 """
 from ._build import build, LIB as LIB_PATH
 from . import abi
-from .cache import Cache
+from .cache import Cache, PrefixIndex
 
-__all__ = ["build", "LIB_PATH", "abi", "Cache"]
+__all__ = ["build", "LIB_PATH", "abi", "Cache", "PrefixIndex"]

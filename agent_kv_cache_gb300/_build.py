@@ -17,7 +17,7 @@ OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libakv.so")
 
 SOURCES = ["akv_host.cpp", "akv_kernels.cu", "akv_decode.cu", "akv_decode_mma.cu", "akv_noalloc.cu",
-           "akv_restore.cu"]
+           "akv_restore.cu", "akv_prefix.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]

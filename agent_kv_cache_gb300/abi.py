@@ -55,6 +55,21 @@ class AkvOp(ctypes.Structure):
 
 
 AKV_OP_APPEND, AKV_OP_DROP, AKV_OP_REPOS = 0, 1, 2
+AKV_MATCH_NONE, AKV_MATCH_EXACT, AKV_MATCH_RETRIGGER = 0, 1, 2
+MATCH_KINDS = {AKV_MATCH_NONE: "none", AKV_MATCH_EXACT: "exact", AKV_MATCH_RETRIGGER: "retrigger"}
+
+
+class AkvPrefixMatch(ctypes.Structure):
+    """struct akv_prefix_match_t"""
+    _fields_ = [("kind", ctypes.c_int32), ("n_records", ctypes.c_int32),
+                ("entry", ctypes.c_int64), ("n_tokens", ctypes.c_int32),
+                ("n_rotated", ctypes.c_int32), ("op_index", ctypes.c_int32),
+                ("op_tokens", ctypes.c_int32)]
+
+    def as_dict(self):
+        return dict(kind=MATCH_KINDS[self.kind], entry=self.entry, n_records=self.n_records,
+                    n_tokens=self.n_tokens, n_rotated=self.n_rotated, op_index=self.op_index,
+                    op_tokens=self.op_tokens)
 
 
 class AkvSeqInfo(ctypes.Structure):
@@ -109,6 +124,21 @@ SIGNATURES = {
                                                     ctypes.c_double, _P, _P, _P, _I32, _I32,
                                                     _PI32, _PI32, _P, _P, _I32, _P]),
     "akv_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint32]),
+    "akv_prefix_index_create": (ctypes.c_int, [_I32, ctypes.POINTER(_P)]),
+    "akv_prefix_index_destroy": (ctypes.c_int, [_P]),
+    "akv_prefix_last_error": (ctypes.c_char_p, [_P]),
+    "akv_prefix_insert": (ctypes.c_int, [_P, _I64, ctypes.POINTER(AkvOp), _I32, _PI32, _I32,
+                                         _I64]),
+    "akv_prefix_remove": (ctypes.c_int, [_P, _I64]),
+    "akv_prefix_touch": (ctypes.c_int, [_P, _I64, _I64]),
+    "akv_prefix_match": (ctypes.c_int, [_P, ctypes.POINTER(AkvOp), _I32, _PI32, _I32,
+                                        ctypes.POINTER(AkvPrefixMatch)]),
+    "akv_prefix_evict_order": (ctypes.c_int, [_P, _PI64, _I32, _PI32]),
+    "akv_prefix_publish": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(AkvOp), _I32, _PI32, _I32,
+                                          _PI64]),
+    "akv_prefix_fork": (ctypes.c_int, [_P, _P, ctypes.POINTER(AkvOp), _I32, _PI32, _I32,
+                                       ctypes.POINTER(AkvPrefixMatch), _PI64]),
+    "akv_prefix_evict": (ctypes.c_int, [_P, _P, _I32, _PI32, _PI32]),
 }
 
 _lib = None
@@ -347,3 +377,83 @@ def akv_decode_attention_noalloc(k_slab, v_slab, max_pages, hq, hkv, head_dim, p
 
 def akv_set_wait_limit(cache, polls):
     _check(lib().akv_set_wait_limit(cache, polls), cache)
+
+
+# ---- history-keyed prefix sharing ------------------------------------------
+
+def _icheck(rc, index):
+    if rc != AKV_OK:
+        raise AkvError(rc, lib().akv_prefix_last_error(index).decode() if index else "")
+
+
+def _ids(token_ids):
+    a = np.ascontiguousarray(np.asarray(token_ids, dtype=np.int32).reshape(-1))
+    return a, a.ctypes.data_as(_PI32)
+
+
+def akv_prefix_index_create(page_size):
+    h = _P()
+    _check(lib().akv_prefix_index_create(page_size, ctypes.byref(h)))
+    return h
+
+
+def akv_prefix_index_destroy(index):
+    _check(lib().akv_prefix_index_destroy(index))
+
+
+def akv_prefix_insert(index, entry, program, token_ids, use_time=-1):
+    arr, keep = make_program(program)
+    ids, pid = _ids(token_ids)
+    _icheck(lib().akv_prefix_insert(index, entry, arr, len(program), pid, ids.size, use_time), index)
+    del keep
+
+
+def akv_prefix_remove(index, entry):
+    _icheck(lib().akv_prefix_remove(index, entry), index)
+
+
+def akv_prefix_touch(index, entry, use_time=-1):
+    _icheck(lib().akv_prefix_touch(index, entry, use_time), index)
+
+
+def akv_prefix_match(index, program, token_ids):
+    arr, keep = make_program(program)
+    ids, pid = _ids(token_ids)
+    m = AkvPrefixMatch()
+    _icheck(lib().akv_prefix_match(index, arr, len(program), pid, ids.size, ctypes.byref(m)), index)
+    del keep
+    return m.as_dict()
+
+
+def akv_prefix_evict_order(index, capacity=4096):
+    out = (ctypes.c_int64 * max(1, capacity))()
+    n = ctypes.c_int32()
+    _icheck(lib().akv_prefix_evict_order(index, out, capacity, ctypes.byref(n)), index)
+    return [int(out[i]) for i in range(n.value)]
+
+
+def akv_prefix_publish(cache, index, seq, program, token_ids):
+    arr, keep = make_program(program)
+    ids, pid = _ids(token_ids)
+    e = ctypes.c_int64()
+    _check(lib().akv_prefix_publish(cache, index, seq, arr, len(program), pid, ids.size,
+                                    ctypes.byref(e)), cache)
+    del keep
+    return e.value
+
+
+def akv_prefix_fork(cache, index, program, token_ids):
+    arr, keep = make_program(program)
+    ids, pid = _ids(token_ids)
+    m = AkvPrefixMatch()
+    child = ctypes.c_int64()
+    _check(lib().akv_prefix_fork(cache, index, arr, len(program), pid, ids.size, ctypes.byref(m),
+                                 ctypes.byref(child)), cache)
+    del keep
+    return child.value, m.as_dict()
+
+
+def akv_prefix_evict(cache, index, want_pages):
+    f, n = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().akv_prefix_evict(cache, index, want_pages, ctypes.byref(f), ctypes.byref(n)), cache)
+    return f.value, n.value

@@ -77,6 +77,21 @@ class Cache:
                                   v.data_ptr(), n, out.data_ptr())
         return out
 
+    # -- history-keyed prefix sharing ----------------------------------------
+    def prefix_publish(self, index, seq, program, token_ids):
+        """Publish `seq` (whose history is `program` with `token_ids`) into a
+        PrefixIndex; returns the entry id (a frozen snapshot sequence)."""
+        return abi.akv_prefix_publish(self.handle, index.handle, seq, program, token_ids)
+
+    def prefix_fork(self, index, program, token_ids):
+        """Match a request program and materialise the matched prefix as a new
+        sequence; returns (child or -1, match dict)."""
+        return abi.akv_prefix_fork(self.handle, index.handle, program, token_ids)
+
+    def prefix_evict(self, index, want_pages):
+        """Drop-aware eviction; returns (pages freed, entries evicted)."""
+        return abi.akv_prefix_evict(self.handle, index.handle, want_pages)
+
     def set_restore_tensor_cores(self, enable):
         abi.akv_set_restore_tensor_cores(self.handle, enable)
 
@@ -141,3 +156,36 @@ class Cache:
         k = self.k_pool[slab][pid, :, off]          # [n, hkv, D]
         v = self.v_pool[slab][pid, :, off]
         return (k.double().cpu().numpy(), v.double().cpu().numpy())
+
+
+class PrefixIndex:
+    """Host-only history-keyed prefix index (no GPU needed)."""
+
+    def __init__(self, page_size):
+        self.handle = abi.akv_prefix_index_create(page_size)
+
+    def insert(self, entry, program, token_ids, use_time=-1):
+        abi.akv_prefix_insert(self.handle, entry, program, token_ids, use_time)
+
+    def remove(self, entry):
+        abi.akv_prefix_remove(self.handle, entry)
+
+    def touch(self, entry, use_time=-1):
+        abi.akv_prefix_touch(self.handle, entry, use_time)
+
+    def match(self, program, token_ids):
+        return abi.akv_prefix_match(self.handle, program, token_ids)
+
+    def evict_order(self):
+        return abi.akv_prefix_evict_order(self.handle)
+
+    def close(self):
+        if self.handle:
+            abi.akv_prefix_index_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -26,6 +26,7 @@
 
 #include "akv.h"
 #include "akv_internal.h"
+#include "akv_prefix.h"
 
 using namespace akv;
 
@@ -65,6 +66,7 @@ struct HostSeq {
   int64_t gather_n = 0;
   bool gather_identity = true;     // last reposition moved nothing
   HKey key;
+  bool frozen = false;             // snapshot of a published prefix entry
 };
 
 struct Stage { char* h = nullptr; char* d = nullptr; cudaEvent_t ev = nullptr; bool used = false; };
@@ -190,6 +192,8 @@ struct akv_cache {
   int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
   void* d_restore = nullptr;       // temporary key/value versions of restore attention
   size_t restore_cap = 0;
+  void* d_fork = nullptr;          // descriptor of a prefix fork
+  size_t fork_cap = 0;
   bool restore_generic = false;    // CUDA-core restore kernel for every shape
 };
 
@@ -303,6 +307,7 @@ void destroy(akv_cache* c) {
   for (auto& pl : c->plans) cudaFree(pl.d);
   cudaFree(c->d_counters);
   cudaFree(c->d_restore);
+  cudaFree(c->d_fork);
   for (Stage& s : c->stages) {
     if (s.h) cudaFreeHost(s.h);
     if (s.d) cudaFree(s.d);
@@ -459,6 +464,7 @@ int akv_seq_fork(akv_cache* c, int64_t parent, int64_t* child) {
   if (!p) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)parent);
   if (c->free_dslots.empty()) return fail(c, AKV_ECAPACITY, "max_seqs (%d) sequences alive", c->cfg.max_seqs);
   HostSeq s = *p;
+  s.frozen = false;
   s.dslot = c->free_dslots.back();
   const SeqArrays& sa = c->sa;
   const int64_t ps = p->dslot, cs = s.dslot;
@@ -509,6 +515,7 @@ int akv_append(akv_cache* c, const int64_t* seqs, const int32_t* n_tokens, int32
   for (int i = 0; i < n_seqs; ++i) {
     hs[i] = find(c, seqs[i]);
     if (!hs[i]) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seqs[i]);
+    if (hs[i]->frozen) return fail(c, AKV_EINVAL, "sequence %lld is a published snapshot", (long long)seqs[i]);
     for (int j = 0; j < i; ++j)
       if (hs[j] == hs[i]) return fail(c, AKV_EINVAL, "sequence %lld repeated", (long long)seqs[i]);
     const int64_t n = n_tokens[i];
@@ -646,6 +653,7 @@ int akv_drop(akv_cache* c, int64_t seq, const int64_t* ranges, int32_t n_ranges)
   if (!c || n_ranges < 0 || (n_ranges > 0 && !ranges)) return AKV_EINVAL;
   HostSeq* s = find(c, seq);
   if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  if (s->frozen) return fail(c, AKV_EINVAL, "sequence %lld is a published snapshot", (long long)seq);
   std::vector<Interval> logical;
   for (int i = 0; i < n_ranges; ++i) {
     const int64_t b = ranges[2 * i], e = ranges[2 * i + 1];
@@ -719,6 +727,7 @@ int akv_reposition(akv_cache* c, const int64_t* seqs, int32_t n_seqs) {
   for (int i = 0; i < n_seqs; ++i) {
     hs[i] = find(c, seqs[i]);
     if (!hs[i]) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seqs[i]);
+    if (hs[i]->frozen) return fail(c, AKV_EINVAL, "sequence %lld is a published snapshot", (long long)seqs[i]);
     for (int j = 0; j < i; ++j)
       if (hs[j] == hs[i]) return fail(c, AKV_EINVAL, "sequence %lld repeated", (long long)seqs[i]);
     const HostSeq* s = hs[i];
@@ -1100,6 +1109,238 @@ int akv_set_layer_window(akv_cache* c, int32_t layer, int32_t window) {
   if (layer < 0 || layer >= c->cfg.layers || window < 0)
     return fail(c, AKV_EINVAL, "bad layer %d or window %d", layer, window);
   c->windows[layer] = window;
+  return AKV_OK;
+}
+
+
+// ---- history-keyed prefix sharing / drop-aware eviction ----------------------
+//
+// Paper review A.1.2 and 4.2.2-4.2.3; repo review 5.4 (materialisation plan:
+// reuse a stored version, or take a new slot and copy, with copy-on-write of
+// pages handed to another branch) and 5.6 (eviction candidates).
+
+
+namespace {
+
+HKey history_key(const PrefixIndex& idx, const std::vector<PRec>& recs, size_t n) {
+  HKey k;
+  for (size_t i = 0; i < n; ++i) {
+    const PRec& r = recs[i];
+    if (r.kind == kRecT) {
+      k.absorb(kRecAppend);
+      k.absorb((uint64_t)(uint32_t)r.v);
+    } else if (r.kind == kRecD) {
+      const auto& d = idx.delta(r.v);
+      k.absorb(kRecDrop);
+      k.absorb(d.size());
+      for (const auto& iv : d) { k.absorb((uint64_t)iv.first); k.absorb((uint64_t)iv.second); }
+    } else {
+      k.absorb(kRecRepos);
+    }
+  }
+  return k;
+}
+
+int grow_fork_scratch(akv_cache* c, size_t need) {
+  if (need <= c->fork_cap) return AKV_OK;
+  CK(cudaStreamSynchronize(c->stream));
+  cudaFree(c->d_fork);
+  c->d_fork = nullptr;
+  c->fork_cap = 0;
+  CK(cudaMalloc(&c->d_fork, need));
+  c->fork_cap = need;
+  return AKV_OK;
+}
+
+}  // namespace
+
+int akv_prefix_publish(akv_cache* c, akv_prefix_index* x, int64_t seq, const akv_op* ops,
+                       int32_t n_ops, const int32_t* token_ids, int32_t n_tokens, int64_t* entry) {
+  if (!c || !x || !entry) return AKV_EINVAL;
+  if (x->idx.page_size() != c->cfg.page_size)
+    return fail(c, AKV_EINVAL, "index page size %d != cache page size %d", x->idx.page_size(),
+                c->cfg.page_size);
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  PProgram p;
+  const char* why = "";
+  int rc = x->idx.expand(ops, n_ops, token_ids, n_tokens, &p, &why);
+  if (rc) return fail(c, rc, "%s", why);
+  const HKey k = history_key(x->idx, p.recs, p.recs.size());
+  if (k.a != s->key.a || k.b != s->key.b)
+    return fail(c, AKV_EINVAL, "the program is not the history of sequence %lld", (long long)seq);
+  const int64_t same = x->idx.find_equal(p);
+  if (same >= 0 && find(c, same)) {
+    x->idx.touch(same, -1);
+    *entry = same;
+    return AKV_OK;
+  }
+  int64_t snap = -1;
+  rc = akv_seq_fork(c, seq, &snap);
+  if (rc) return rc;
+  find(c, snap)->frozen = true;
+  if (x->idx.insert(snap, p, -1) != AKV_OK) {
+    akv_seq_free(c, snap);
+    return fail(c, AKV_EINVAL, "entry %lld already in the index", (long long)snap);
+  }
+  *entry = snap;
+  return AKV_OK;
+}
+
+int akv_prefix_fork(akv_cache* c, akv_prefix_index* x, const akv_op* ops, int32_t n_ops,
+                    const int32_t* token_ids, int32_t n_tokens, akv_prefix_match_t* mo,
+                    int64_t* child) {
+  if (!c || !x || !child) return AKV_EINVAL;
+  *child = -1;
+  if (x->idx.page_size() != c->cfg.page_size)
+    return fail(c, AKV_EINVAL, "index page size %d != cache page size %d", x->idx.page_size(),
+                c->cfg.page_size);
+  PProgram req;
+  const char* why = "";
+  int rc = x->idx.expand(ops, n_ops, token_ids, n_tokens, &req, &why);
+  if (rc) return fail(c, rc, "%s", why);
+  const PMatch m = x->idx.match(req);
+  if (mo) {
+    mo->kind = m.kind;
+    mo->n_records = m.n_records;
+    mo->entry = m.entry;
+    mo->n_tokens = m.n_tokens;
+    mo->n_rotated = m.n_rotated;
+    mo->op_index = m.op_index;
+    mo->op_tokens = m.op_tokens;
+  }
+  if (m.kind == AKV_MATCH_NONE) return AKV_OK;
+  HostSeq* E = find(c, m.entry);
+  const PEntry* pe = x->idx.entry(m.entry);
+  if (!E || !pe) return fail(c, AKV_ENOSEQ, "entry %lld has no snapshot in this cache", (long long)m.entry);
+  const PrefixIndex::State st = x->idx.replay(req.recs, (size_t)m.n_records);
+  const int S = c->cfg.page_size;
+  const int64_t n_slots = st.next_pos;
+  const int64_t n_pages = (n_slots + S - 1) / S;
+  if (n_slots > c->cfg.max_slots) return fail(c, AKV_ECAPACITY, "prefix holds more than max_slots");
+  if (c->free_dslots.empty()) return fail(c, AKV_ECAPACITY, "max_seqs (%d) sequences alive", c->cfg.max_seqs);
+  // per destination page: 0 no needed token, 1 every needed token keeps its slot, 2 fresh
+  std::vector<int8_t> kind((size_t)n_pages, 0);
+  const size_t n_tok = st.active.size();
+  for (size_t t = 0; t < n_tok; ++t) {
+    if (!st.active[t]) continue;
+    const int32_t src = pe->stored[t];
+    if (src < 0 || src / S >= (int64_t)E->pages.size() || E->pages[src / S] < 0)
+      return fail(c, AKV_EINVAL, "entry %lld lost the key of token %zu", (long long)m.entry, t);
+    const int64_t k = st.pos[t] / S;
+    if (kind[k] == 0) kind[k] = 1;
+    if (src != st.pos[t]) kind[k] = 2;
+  }
+  // a partly filled tail page is always held (the next append writes into
+  // it), even when none of its slots is needed: a fresh empty page
+  if (n_slots % S && kind[n_pages - 1] == 0) kind[n_pages - 1] = 3;
+  size_t n_fresh = 0;
+  for (int8_t k : kind) n_fresh += k >= 2;
+  if (n_fresh > c->free_pages.size())
+    return fail(c, AKV_ENOPAGES, "prefix fork needs %zu pages, %zu free", n_fresh, c->free_pages.size());
+
+  // plan the new sequence
+  HostSeq s;
+  s.pages.assign((size_t)n_pages, -1);
+  std::vector<int32_t> fresh = peek_pages(c, n_fresh);
+  size_t fi = 0;
+  for (int64_t k = 0; k < n_pages; ++k) {
+    if (kind[k] == 1) s.pages[k] = E->pages[k];
+    else if (kind[k] >= 2) s.pages[k] = fresh[fi++];
+  }
+  std::vector<MoveItem> moves;
+  std::vector<int32_t> act;
+  for (int64_t k = 0; k < n_pages; ++k)
+    if (kind[k] == 1 || kind[k] == 2) act.push_back((int32_t)k);
+  std::vector<uint32_t> keep((size_t)((n_slots + 31) / 32), 0u);
+  int64_t n_alive = 0;
+  for (size_t t = 0; t < n_tok; ++t) {
+    if (st.held[t]) {
+      const int64_t slot = st.pos[t];
+      if (!s.runs.empty() && s.runs.back().slot0 + s.runs.back().len == slot &&
+          s.runs.back().log0 + s.runs.back().len == (int64_t)t)
+        ++s.runs.back().len;
+      else
+        s.runs.push_back({slot, (int64_t)t, 1});
+    }
+    if (!st.active[t]) continue;
+    const int64_t slot = st.pos[t];
+    keep[slot / 32] |= 1u << (slot % 32);
+    ++n_alive;
+    if (!s.alive.empty() && s.alive.back().b == slot) s.alive.back().b = slot + 1;
+    else s.alive.push_back({slot, slot + 1});
+    const int32_t src = pe->stored[t];
+    if (kind[slot / S] == 2)
+      moves.push_back({E->pages[src / S], src % S, s.pages[slot / S], (int32_t)(slot % S),
+                       (int32_t)(slot - src)});
+  }
+  s.n_logical = (int64_t)n_tok;
+  s.n_slots = n_slots;
+  s.n_alive = n_alive;
+  s.n_active_pages = (int32_t)act.size();
+  s.gather_identity = true;
+  s.gather_n = 0;
+  s.key = history_key(x->idx, req.recs, (size_t)m.n_records);
+
+  Blob blob;
+  const size_t o_keep = blob.put(keep.data(), keep.size());
+  const size_t o_pages = blob.put(s.pages.data(), s.pages.size());
+  const size_t o_act = blob.put(act.data(), act.size());
+  const size_t o_mv = blob.put(moves.data(), moves.size());
+  rc = grow_fork_scratch(c, blob.b.size() + 16);
+  if (rc) return rc;
+  rc = upload_large(c, blob, static_cast<char*>(c->d_fork));
+  if (rc) return rc;
+
+  // commit
+  take_pages(c, n_fresh);
+  for (int64_t k = 0; k < n_pages; ++k)
+    if (kind[k] == 1) ++c->refcnt[s.pages[k]];
+  s.dslot = c->free_dslots.back();
+  c->free_dslots.pop_back();
+  const SeqArrays& sa = c->sa;
+  char* d = static_cast<char*>(c->d_fork);
+  if (!keep.empty())
+    CK(cudaMemcpyAsync(sa.keep + (int64_t)s.dslot * sa.keep_words, d + o_keep,
+                       keep.size() * sizeof(uint32_t), cudaMemcpyDeviceToDevice, c->stream));
+  if (!s.pages.empty())
+    CK(cudaMemcpyAsync(sa.pages + (int64_t)s.dslot * sa.seq_pages, d + o_pages,
+                       s.pages.size() * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
+  if (!act.empty())
+    CK(cudaMemcpyAsync(sa.active + (int64_t)s.dslot * sa.seq_pages, d + o_act,
+                       act.size() * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
+  const int64_t id = c->next_id++;
+  c->seqs.emplace(id, std::move(s));
+  ++c->epoch;
+  x->idx.touch(m.entry, -1);
+  *child = id;
+  if (!moves.empty()) {
+    CK(launch_transplant(c->g, reinterpret_cast<const MoveItem*>(d + o_mv), (int)moves.size(),
+                         c->d_cs, c->cfg.max_slots, c->d_err, c->stream));
+    ++c->launches;
+  }
+  return AKV_OK;
+}
+
+int akv_prefix_evict(akv_cache* c, akv_prefix_index* x, int32_t want_pages, int32_t* freed_pages,
+                     int32_t* n_evicted) {
+  if (!c || !x || want_pages < 0) return AKV_EINVAL;
+  const std::vector<int64_t> order = x->idx.evict_order();
+  const size_t before = c->free_pages.size();
+  int32_t ev = 0;
+  for (int64_t id : order) {
+    if ((int64_t)(c->free_pages.size() - before) >= want_pages) break;
+    HostSeq* s = find(c, id);
+    if (s) {
+      s->frozen = false;
+      const int rc = akv_seq_free(c, id);
+      if (rc) return rc;
+    }
+    x->idx.remove(id);
+    ++ev;
+  }
+  if (freed_pages) *freed_pages = (int32_t)(c->free_pages.size() - before);
+  if (n_evicted) *n_evicted = ev;
   return AKV_OK;
 }
 

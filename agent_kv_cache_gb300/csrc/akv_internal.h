@@ -142,6 +142,12 @@ struct RestoreArgs {
   int32_t use_mma;
 };
 cudaError_t launch_restore(const RestoreArgs& a, cudaStream_t st);
+
+// ---- prefix fork: stored keys of a snapshot moved into fresh pages ----------
+struct MoveItem { int32_t src_page, src_off, dst_page, dst_off, delta; };
+constexpr int kMoveTokens = 16;   // moves per block
+cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves, const float2* cs,
+                              int max_pos, uint32_t* err, cudaStream_t st);
 bool restore_mma_supported(const Geom& g);
 int restore_tile_tokens(const Geom& g);       // query tokens per tensor-core block
 

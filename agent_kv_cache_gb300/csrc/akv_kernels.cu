@@ -517,11 +517,99 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
   }
 }
 
+// ---------------------------------------------------------------------------
+// prefix fork: needed keys of a published snapshot moved into fresh pages of
+// a new sequence, each rotated by its own delta = p_request - p_stored (bit
+// copy when delta == 0), V copied.  One block per kMoveTokens moves, all
+// layers and KV heads.
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(256, 4)
+k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
+             const float2* __restrict__ cs, int max_pos, uint32_t* err) {
+  extern __shared__ float2 s_cs[];   // [kMoveTokens][R/2] (unit-minor), angle delta f
+  __shared__ MoveItem s_mv[kMoveTokens];
+  const int m0 = blockIdx.x * kMoveTokens;
+  const int nm = min(kMoveTokens, n_moves - m0);
+  const int S = g.s, D = g.d, R = g.rope, RH = R / 2;
+  const int tid = threadIdx.x, bs = blockDim.x;
+  for (int t = tid; t < nm; t += bs) {
+    MoveItem mv = moves[m0 + t];
+    const bool ok = mv.src_page >= 0 && mv.src_page < g.max_pages && mv.dst_page >= 0 &&
+                    mv.dst_page < g.max_pages && mv.src_off >= 0 && mv.src_off < S &&
+                    mv.dst_off >= 0 && mv.dst_off < S && mv.delta > -max_pos && mv.delta < max_pos;
+    if (!ok) { flag(err, AKV_DERR_PAGE); mv.src_page = -1; }
+    s_mv[t] = mv;
+  }
+  {
+    constexpr int E = Vec<T>::E;
+    const int kr = RH / E;
+    for (int i = tid; i < nm * RH; i += bs) {
+      const int t = i / RH, j = i % RH;
+      const int delta = moves[m0 + t].delta;
+      const int a = delta < 0 ? -delta : delta;
+      float2 c = make_float2(1.f, 0.f);
+      if (a < max_pos) c = cs[(int64_t)a * RH + j];
+      s_cs[t * RH + (j % E) * kr + j / E] = make_float2(c.x, delta < 0 ? -c.y : c.y);
+    }
+  }
+  __syncthreads();
+  constexpr int E = Vec<T>::E;
+  const int kr = RH / E, kc = (D - R) / E, vu = D / E, per_row = kr + kc + vu;
+  const int units = g.hkv * nm * per_row;
+  T* kp = static_cast<T*>(g.k);
+  T* vp = static_cast<T*>(g.v);
+  for (int u = tid; u < units; u += bs) {
+    const int r = u % per_row;
+    const int t = (u / per_row) % nm;
+    const int h = u / (per_row * nm);
+    const MoveItem mv = s_mv[t];
+    if (mv.src_page < 0) continue;
+    const int64_t src_off = (int64_t)mv.src_page * g.page_stride + (int64_t)h * g.head_stride +
+                            (int64_t)mv.src_off * D;
+    const int64_t dst_off = (int64_t)mv.dst_page * g.page_stride + (int64_t)h * g.head_stride +
+                            (int64_t)mv.dst_off * D;
+    if (r < kr) {
+      for (int l = 0; l < g.phys_layers; ++l) {
+        const T* src = kp + (int64_t)l * g.layer_stride + src_off;
+        T* dst = kp + (int64_t)l * g.layer_stride + dst_off;
+        const uint4 lo = ld16(src + r * E), hi = ld16(src + RH + r * E);
+        if (mv.delta == 0) {
+          st16(dst + r * E, lo);
+          st16(dst + RH + r * E, hi);
+        } else {
+          rotate_regs<T>(lo, hi, dst, r, RH, s_cs + t * RH, kr);
+        }
+      }
+    } else {
+      T* base = r < kr + kc ? kp : vp;
+      const int o = r < kr + kc ? R + (r - kr) * E : (r - kr - kc) * E;
+      for (int l = 0; l < g.phys_layers; ++l) {
+        const int64_t slab = (int64_t)l * g.layer_stride;
+        st16(base + slab + dst_off + o, ld16(base + slab + src_off + o));
+      }
+    }
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
+
+cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves, const float2* cs,
+                              int max_pos, uint32_t* err, cudaStream_t st) {
+  if (n_moves <= 0) return cudaSuccess;
+  const int blocks = (n_moves + kMoveTokens - 1) / kMoveTokens;
+  const size_t smem = (size_t)kMoveTokens * (g.rope / 2) * sizeof(float2);
+  if (g.dtype == AKV_DTYPE_BF16)
+    k_transplant<__nv_bfloat16><<<blocks, 256, smem, st>>>(g, moves, n_moves, cs, max_pos, err);
+  else
+    k_transplant<float><<<blocks, 256, smem, st>>>(g, moves, n_moves, cs, max_pos, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* items,
                           const AppendBlock* blocks, int n_blocks, const int32_t* ids,

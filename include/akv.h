@@ -317,6 +317,99 @@ int akv_kernel_launches(akv_cache* cache, uint64_t* count);
 /* Iteration limit of every bounded device wait (default 1<<22 polls). */
 int akv_set_wait_limit(akv_cache* cache, uint32_t polls);
 
+/* ==== History-keyed prefix sharing and drop-aware eviction ====
+ *
+ * Paper review, Appendix A.1.2 (Reposition Scheme) and 4.2.2 / 4.2.3;
+ * repo review 5.4 (context records TOKEN / DELTA / REPOSITION, plan of
+ * occurrence materialisation) and 5.6 (drop-aware eviction candidates).
+ *
+ * A program (akv_op list plus one token id per appended token) is expanded
+ * into context records: TOKEN(id) per appended token, DELTA(ranges) per
+ * non-empty drop (sorted, merged), REPOSITION per reposition.  An index
+ * holds published entries: snapshots of sequences, each with its records.
+ * A request matches an entry on a prefix of n records when the records are
+ * equal up to n and every token active after those n records still has its
+ * key stored in the entry (its slot held and its page holding an active
+ * token).  The match is EXACT when each such key is stored at the position
+ * the request gives it, RETRIGGER when some keys have to be rotated.  The
+ * longest exact prefix is taken unless a retrigger prefix is strictly
+ * longer; ties between entries go to the lowest entry id (for retrigger: the
+ * fewest rotated keys first).  The search stops at the first differing
+ * record: an operation cannot be skipped to line up final positions
+ * (paper review, Figure 11). */
+#define AKV_MATCH_NONE 0
+#define AKV_MATCH_EXACT 1
+#define AKV_MATCH_RETRIGGER 2
+
+typedef struct akv_prefix_index akv_prefix_index;
+
+typedef struct akv_prefix_match_t {
+  int32_t kind;        /* AKV_MATCH_* */
+  int32_t n_records;   /* records of the request covered */
+  int64_t entry;       /* entry id, -1 for none */
+  int32_t n_tokens;    /* appended tokens covered */
+  int32_t n_rotated;   /* keys whose stored position differs (retrigger) */
+  int32_t op_index;    /* the covered prefix is ops[0..op_index) plus ... */
+  int32_t op_tokens;   /* ... the first op_tokens tokens of ops[op_index]
+                        * (0 when the prefix ends at an op boundary) */
+} akv_prefix_match_t;
+
+/* Host-only index (no GPU work); page_size must equal the cache's.  The
+ * index and its entries belong to the caller; one index serves one cache. */
+int akv_prefix_index_create(int32_t page_size, akv_prefix_index** index);
+int akv_prefix_index_destroy(akv_prefix_index* index);
+const char* akv_prefix_last_error(akv_prefix_index* index);
+
+/* Inserts a program as entry `entry` (>= 0, unused).  use_time orders
+ * eviction (older first); < 0 takes the index's own clock.
+ * Errors: AKV_EINVAL (bad program, id taken), AKV_ERANGE (drop range). */
+int akv_prefix_insert(akv_prefix_index* index, int64_t entry, const akv_op* ops,
+                      int32_t n_ops, const int32_t* token_ids, int32_t n_tokens,
+                      int64_t use_time);
+int akv_prefix_remove(akv_prefix_index* index, int64_t entry);
+int akv_prefix_touch(akv_prefix_index* index, int64_t entry, int64_t use_time);
+
+/* Best match of a request program (host only). */
+int akv_prefix_match(akv_prefix_index* index, const akv_op* ops, int32_t n_ops,
+                     const int32_t* token_ids, int32_t n_tokens, akv_prefix_match_t* out);
+
+/* Drop-aware eviction order of all entries: first the entries that another
+ * entry extends with a DELTA record dropping a token active at the entry's
+ * end (their KV is proven unneeded on that path), then leaves, then the
+ * remaining ancestors; oldest use first within each class, then lower id.
+ * Writes *n ids (AKV_ECAPACITY when capacity < *n). */
+int akv_prefix_evict_order(akv_prefix_index* index, int64_t* entries, int32_t capacity,
+                           int32_t* n);
+
+/* Publishes sequence `seq` as an entry: the program must be the sequence's
+ * own history (checked against its history key, which must have been built
+ * with token ids).  The entry is a snapshot (a fork sharing all pages; it
+ * counts against max_seqs); its id is returned in *entry.  A program equal
+ * to an existing entry's returns that entry (its use time refreshed).
+ * Errors: AKV_EINVAL (program is not the history), AKV_ECAPACITY. */
+int akv_prefix_publish(akv_cache* cache, akv_prefix_index* index, int64_t seq,
+                       const akv_op* ops, int32_t n_ops, const int32_t* token_ids,
+                       int32_t n_tokens, int64_t* entry);
+
+/* Matches the request and materialises the covered prefix as a new
+ * sequence (*child; -1 with kind NONE): the request's slots, positions,
+ * keep mask and history; each needed key comes from the entry's stored key,
+ * rotated by R(p_request - p_stored) in fp32 and rounded once (copied when
+ * the positions agree), V copied.  A page whose needed slots all keep their
+ * slot is shared with the entry (reference count), the others are fresh.
+ * The caller continues the program from (op_index, op_tokens).
+ * Errors: AKV_ENOSEQ (entry's snapshot gone), AKV_ENOPAGES, AKV_ECAPACITY. */
+int akv_prefix_fork(akv_cache* cache, akv_prefix_index* index, const akv_op* ops,
+                    int32_t n_ops, const int32_t* token_ids, int32_t n_tokens,
+                    akv_prefix_match_t* match, int64_t* child);
+
+/* Frees entries in drop-aware eviction order until at least want_pages
+ * pool pages returned to the free list (or no entry is left): each evicted
+ * entry's snapshot is freed (pages still used by other sequences or
+ * entries stay) and the entry leaves the index. */
+int akv_prefix_evict(akv_cache* cache, akv_prefix_index* index, int32_t want_pages,
+                     int32_t* freed_pages, int32_t* n_evicted);
+
 #ifdef __cplusplus
 }
 #endif
