@@ -1082,6 +1082,10 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
   a.tiles = reinterpret_cast<const RestoreTile*>(d + o_t);
   a.n_tiles = (int32_t)tiles.size();
   a.use_mma = mma;
+  a.wait_limit = c->wait_limit;
+  if (mma && !make_restore_tensor_maps(c->g, c->d_restore, static_cast<char*>(c->d_restore) + half,
+                                       (int64_t)keys.size(), &a.tm_k, &a.tm_v))
+    a.use_mma = 0;   // no tensor maps: the CUDA-core kernel
   a.g = c->g;
   a.keys = reinterpret_cast<const RestoreKey*>(d + o_keys);
   a.n_keys = (int32_t)keys.size();

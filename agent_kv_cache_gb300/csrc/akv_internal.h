@@ -120,6 +120,7 @@ struct RestoreQuery { int32_t tok, pos, time, era_off, key_end; };
 // tensor-core path: consecutive query tokens of one era, their key range
 struct RestoreTile { int32_t era_off, tok0, n_tok, key_lo, key_hi; };
 struct RestoreArgs {
+  CUtensorMap tm_k, tm_v;     // tensor-core path: era K / V, (D, hkv, n_keys), 64 x 1 x 64 boxes
   Geom g;
   const RestoreKey* keys;
   int32_t n_keys;
@@ -140,16 +141,21 @@ struct RestoreArgs {
   const RestoreTile* tiles;   // tensor-core path only
   int32_t n_tiles;
   int32_t use_mma;
+  uint32_t wait_limit;        // bounded waits of the tensor-core path
 };
 cudaError_t launch_restore(const RestoreArgs& a, cudaStream_t st);
+bool restore_mma_supported(const Geom& g);
+int restore_tile_tokens(const Geom& g);       // query tokens per tensor-core block
+// tensor maps over the era buffers of the tensor-core path (false: unavailable)
+bool make_restore_tensor_maps(const Geom& g, const void* k_era, const void* v_era, int64_t n_keys,
+                              CUtensorMap* tk, CUtensorMap* tv);
 
 // ---- prefix fork: stored keys of a snapshot moved into fresh pages ----------
 struct MoveItem { int32_t src_page, src_off, dst_page, dst_off, delta; };
-constexpr int kMoveTokens = 16;   // moves per block
+constexpr int kMoveTokens = 32;   // moves per block
+constexpr int kMoveLayers = 4;    // physical layers per block
 cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves, const float2* cs,
                               int max_pos, uint32_t* err, cudaStream_t st);
-bool restore_mma_supported(const Geom& g);
-int restore_tile_tokens(const Geom& g);       // query tokens per tensor-core block
 
 // Launchers (akv_kernels.cu / akv_decode.cu).  All enqueue on `st`.
 struct AppendLimits { int32_t n_items, n_ids, n_act, max_seqs; };

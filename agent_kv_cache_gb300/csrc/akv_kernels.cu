@@ -520,18 +520,21 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
 // ---------------------------------------------------------------------------
 // prefix fork: needed keys of a published snapshot moved into fresh pages of
 // a new sequence, each rotated by its own delta = p_request - p_stored (bit
-// copy when delta == 0), V copied.  One block per kMoveTokens moves, all
-// layers and KV heads.
+// copy when delta == 0), V copied.  One block per kMoveTokens moves and
+// kMoveLayers physical layers, all KV heads; each thread keeps 4 chunks in
+// flight.
 // ---------------------------------------------------------------------------
 
 template <typename T>
-__global__ void __launch_bounds__(256, 4)
+__global__ void __launch_bounds__(256)
 k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
              const float2* __restrict__ cs, int max_pos, uint32_t* err) {
   extern __shared__ float2 s_cs[];   // [kMoveTokens][R/2] (unit-minor), angle delta f
   __shared__ MoveItem s_mv[kMoveTokens];
   const int m0 = blockIdx.x * kMoveTokens;
   const int nm = min(kMoveTokens, n_moves - m0);
+  const int layer0 = blockIdx.y * kMoveLayers;   // physical slabs of this block
+  const int nl = min(kMoveLayers, g.phys_layers - layer0);
   const int S = g.s, D = g.d, R = g.rope, RH = R / 2;
   const int tid = threadIdx.x, bs = blockDim.x;
   for (int t = tid; t < nm; t += bs) {
@@ -539,7 +542,10 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
     const bool ok = mv.src_page >= 0 && mv.src_page < g.max_pages && mv.dst_page >= 0 &&
                     mv.dst_page < g.max_pages && mv.src_off >= 0 && mv.src_off < S &&
                     mv.dst_off >= 0 && mv.dst_off < S && mv.delta > -max_pos && mv.delta < max_pos;
-    if (!ok) { flag(err, AKV_DERR_PAGE); mv.src_page = -1; }
+    if (!ok) {
+      if (layer0 == 0) flag(err, AKV_DERR_PAGE);
+      mv.src_page = -1;
+    }
     s_mv[t] = mv;
   }
   {
@@ -556,38 +562,59 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
   }
   __syncthreads();
   constexpr int E = Vec<T>::E;
+  constexpr int B = 4;               // units in flight per thread
   const int kr = RH / E, kc = (D - R) / E, vu = D / E, per_row = kr + kc + vu;
   const int units = g.hkv * nm * per_row;
-  T* kp = static_cast<T*>(g.k);
-  T* vp = static_cast<T*>(g.v);
-  for (int u = tid; u < units; u += bs) {
-    const int r = u % per_row;
-    const int t = (u / per_row) % nm;
-    const int h = u / (per_row * nm);
-    const MoveItem mv = s_mv[t];
-    if (mv.src_page < 0) continue;
-    const int64_t src_off = (int64_t)mv.src_page * g.page_stride + (int64_t)h * g.head_stride +
-                            (int64_t)mv.src_off * D;
-    const int64_t dst_off = (int64_t)mv.dst_page * g.page_stride + (int64_t)h * g.head_stride +
-                            (int64_t)mv.dst_off * D;
-    if (r < kr) {
-      for (int l = 0; l < g.phys_layers; ++l) {
-        const T* src = kp + (int64_t)l * g.layer_stride + src_off;
-        T* dst = kp + (int64_t)l * g.layer_stride + dst_off;
-        const uint4 lo = ld16(src + r * E), hi = ld16(src + RH + r * E);
-        if (mv.delta == 0) {
-          st16(dst + r * E, lo);
-          st16(dst + RH + r * E, hi);
-        } else {
-          rotate_regs<T>(lo, hi, dst, r, RH, s_cs + t * RH, kr);
-        }
+  const T* __restrict__ ks = static_cast<const T*>(g.k);
+  const T* __restrict__ vs = static_cast<const T*>(g.v);
+  T* __restrict__ kd = static_cast<T*>(g.k);
+  T* __restrict__ vd = static_cast<T*>(g.v);
+  for (int w0 = tid; w0 < nl * units; w0 += B * bs) {
+    uint4 lo[B], hi[B];
+    int64_t so[B], dof[B];
+    int rr[B], tt[B];
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      const int w = w0 + j * bs;
+      rr[j] = -1;
+      if (w >= nl * units) continue;
+      const int u = w % units;
+      const int64_t slab = (int64_t)(layer0 + w / units) * g.layer_stride;
+      const int r = u % per_row;
+      const int t = (u / per_row) % nm;
+      const int h = u / (per_row * nm);
+      const MoveItem mv = s_mv[t];
+      if (mv.src_page < 0) continue;
+      rr[j] = r;
+      tt[j] = t;
+      so[j] = slab + (int64_t)mv.src_page * g.page_stride + (int64_t)h * g.head_stride +
+              (int64_t)mv.src_off * D;
+      dof[j] = slab + (int64_t)mv.dst_page * g.page_stride + (int64_t)h * g.head_stride +
+               (int64_t)mv.dst_off * D;
+      if (r < kr) {
+        lo[j] = ld16(ks + so[j] + r * E);
+        hi[j] = ld16(ks + so[j] + RH + r * E);
+      } else if (r < kr + kc) {
+        lo[j] = ld16(ks + so[j] + R + (r - kr) * E);
+      } else {
+        lo[j] = ld16(vs + so[j] + (r - kr - kc) * E);
       }
-    } else {
-      T* base = r < kr + kc ? kp : vp;
-      const int o = r < kr + kc ? R + (r - kr) * E : (r - kr - kc) * E;
-      for (int l = 0; l < g.phys_layers; ++l) {
-        const int64_t slab = (int64_t)l * g.layer_stride;
-        st16(base + slab + dst_off + o, ld16(base + slab + src_off + o));
+    }
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      const int r = rr[j];
+      if (r < 0) continue;
+      if (r < kr) {
+        if (s_mv[tt[j]].delta == 0) {
+          st16(kd + dof[j] + r * E, lo[j]);
+          st16(kd + dof[j] + RH + r * E, hi[j]);
+        } else {
+          rotate_regs<T>(lo[j], hi[j], kd + dof[j], r, RH, s_cs + tt[j] * RH, kr);
+        }
+      } else if (r < kr + kc) {
+        st16(kd + dof[j] + R + (r - kr) * E, lo[j]);
+      } else {
+        st16(vd + dof[j] + (r - kr - kc) * E, lo[j]);
       }
     }
   }
@@ -602,12 +629,13 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
 cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves, const float2* cs,
                               int max_pos, uint32_t* err, cudaStream_t st) {
   if (n_moves <= 0) return cudaSuccess;
-  const int blocks = (n_moves + kMoveTokens - 1) / kMoveTokens;
+  const dim3 grid((n_moves + kMoveTokens - 1) / kMoveTokens,
+                  (g.phys_layers + kMoveLayers - 1) / kMoveLayers);
   const size_t smem = (size_t)kMoveTokens * (g.rope / 2) * sizeof(float2);
   if (g.dtype == AKV_DTYPE_BF16)
-    k_transplant<__nv_bfloat16><<<blocks, 256, smem, st>>>(g, moves, n_moves, cs, max_pos, err);
+    k_transplant<__nv_bfloat16><<<grid, 256, smem, st>>>(g, moves, n_moves, cs, max_pos, err);
   else
-    k_transplant<float><<<blocks, 256, smem, st>>>(g, moves, n_moves, cs, max_pos, err);
+    k_transplant<float><<<grid, 256, smem, st>>>(g, moves, n_moves, cs, max_pos, err);
   return cudaGetLastError();
 }
 

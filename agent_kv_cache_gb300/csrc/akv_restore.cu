@@ -12,7 +12,9 @@
 // birth(k) <= t(x) < death(k), which also makes the attention causal.
 #include <algorithm>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include "akv.h"
 #include "akv_internal.h"
@@ -178,16 +180,25 @@ cudaError_t launch_simple_g(const RestoreArgs& a, int G, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core path (bf16, D in {64, 128}): FA2-style tiles on mma.sync.
-// Block = 64 query rows: warp w takes head (w % NH) of the block's head
-// subgroup and 16 consecutive tokens (group w / NH), NH = min(G, 4), so a
-// K/V tile in shared memory serves NH heads.  64-key tiles, double-buffered
-// with cp.async into rows whose 16-byte chunks are XOR-swizzled by row % 8
-// (conflict-free ldmatrix).  S = Q K^T and O += P V (P reused from the
-// accumulator registers as the A operand); interval mask per (row, key).
+// Tensor-core path (bf16, D in {64, 128}): tcgen05 UMMA with accumulators in
+// tensor memory.  One CTA = 128 query rows (TT tokens x NH heads of one KV
+// group, NH = min(G, 8)) and 128 threads, thread r owning row r (TMEM lane
+// r).  Per 64-key tile:
+//   S = Q K^T      M=128, N=64, K=D    -> TMEM columns [0, 64)
+//   softmax        tcgen05.ld of the S row, interval mask, online max/sum,
+//                  P (bf16) to shared memory, O rescaled in TMEM if needed
+//   O += P V       M=128, N=D,  K=64   -> TMEM columns [64, 64+D)
+// Operands live in shared memory in the 128-byte swizzled layout (rows of
+// 128 bytes, 16-byte chunk c of row r at c ^ (r % 8), 64-element atoms of
+// rows*128 bytes); Q, K and P are K-major, V (the same bytes as K's layout)
+// is read MN-major.  One thread issues the MMAs and commits them to an
+// mbarrier that the CTA waits on (bounded).  Two CTAs share an SM (about
+// 82 KB of shared memory and 256 TMEM columns each for D = 128), so one
+// CTA's softmax overlaps the other's MMAs.
 // ---------------------------------------------------------------------------
 
-constexpr int kKT = 64;   // keys per tile
+constexpr int kBM = 128;   // query rows per CTA
+constexpr int kBN = 64;    // keys per tile
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -200,283 +211,420 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
+// byte offset of (row, 16-byte chunk) in an operand of `rows` rows
+__device__ __forceinline__ uint32_t sw128(int row, int chunk, int rows) {
+  return (uint32_t)((chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
+// shared memory matrix descriptor: start, leading / stride byte offsets,
+// fixed version bits 46-47 = 1, 128-byte swizzle (layout type 2, bits 61-63)
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
-__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+// instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), B major-ness (bit 16), N >> 3 (bits 17-22),
+// M >> 4 (bits 24-28)
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int acc) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+               ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 "selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok) : "r"(mbar), "r"(parity) : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-// byte offset of (row, 16-byte chunk) in a tile of rows of D bf16
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void proxy_fence() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+               "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                 "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                 "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                 "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                 "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+               "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+               "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                 "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),
+                 "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+                 "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+                 "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
+                 "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 template <int D>
-__device__ __forceinline__ uint32_t rsw(int row, int chunk) {
-  return (uint32_t)(row * (D * 2) + (((chunk & ~7) | ((chunk & 7) ^ (row & 7))) << 4));
+__host__ __device__ constexpr int restore_tc_cols() { return D == 64 ? 128 : 256; }   // TMEM columns (power of 2)
+template <int D>
+constexpr size_t restore_tc_smem() {
+  return 1024 /* alignment slack */ + (size_t)kBM * D * 2 + 2 * (size_t)kBN * D * 2 +
+         (size_t)kBM * kBN * 2 + 2 * kBN * sizeof(int) + 4 * sizeof(int) + 32;
 }
 
 template <int D, int NH>
 __global__ void __launch_bounds__(128)
-k_restore_attn_mma(const __grid_constant__ RestoreArgs a) {
-  constexpr int KS = D / 16, NTD = D / 8, CH = D / 8, TILE = kKT * D * 2;
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* s_k = smem;                       // [2][kKT][D]  (stage 0 also stages Q)
-  unsigned char* s_v = smem + 2 * TILE;            // [2][kKT][D]
-  int* s_birth = reinterpret_cast<int*>(smem + 4 * TILE);   // [2][kKT]
-  int* s_death = s_birth + 2 * kKT;
+k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
+  constexpr int NCOL = restore_tc_cols<D>();
+  constexpr uint32_t KV_BYTES = kBN * D * 2;     // one tile of K (or V)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm;                           // kBM x D (K-major)
+  uint8_t* sK = sQ + kBM * D * 2;             // kBN x D, TMA 64-element atoms
+  uint8_t* sV = sK + kBN * D * 2;             // same layout, read MN-major
+  uint8_t* sP = sV + kBN * D * 2;             // kBM x kBN (K-major)
+  int* s_death = reinterpret_cast<int*>(sP + kBM * kBN * 2);   // [2][kBN]
+  int* s_dmin = s_death + 2 * kBN;                              // [2][2] per-warp minima
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(s_dmin + 4);     // MMA, K, V
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 3);
 
   const RestoreTile tl = a.tiles[blockIdx.x];
   const int kvh = blockIdx.y;
-  const int G = a.g.hq / a.g.hkv, H = a.g.hkv;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int head = blockIdx.z * NH + warp % NH;
-  const int tbase = tl.tok0 + (warp / NH) * 16;   // first token of this warp's rows
+  const int G = a.g.hq / a.g.hkv;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int tend = tl.tok0 + tl.n_tok;
   const int R = a.g.rope, RH = R / 2;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k_era);
-  const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.v_era);
 
-  // stage rotated, scaled Q rows (bf16, swizzled) in s_k[0]; row = warp*16 + r
-  for (int i = tid; i < 64 * (D / 2); i += 128) {
+  // rotated, scaled Q rows: row = token * NH + head
+  for (int i = tid; i < kBM * (D / 2); i += 128) {
     const int row = i / (D / 2), d = i % (D / 2);
-    const int w = row / 16, r = row % 16;
-    const int t = tl.tok0 + (w / NH) * 16 + r;
-    const int hq = kvh * G + blockIdx.z * NH + w % NH;
+    const int t = tl.tok0 + row / NH;
+    const int hq = kvh * G + blockIdx.z * NH + row % NH;
     float x = 0.f, y = 0.f;
-    int dx = d, dy = d + D / 2;
-    const bool ok = t < tend && a.queries[t].pos >= 0 && a.queries[t].pos < a.max_pos;
-    if (t < tend && !ok && d == 0) atomicOr(a.err, AKV_DERR_INDEX);
-    if (ok) {
+    int dx, dy;
+    if (d < RH) { dx = d; dy = d + RH; }
+    else { dx = R + 2 * (d - RH); dy = dx + 1; }
+    if (t < tend) {
       const RestoreQuery qq = a.queries[t];
-      const __nv_bfloat16* qr = qg + ((int64_t)t * a.g.hq + hq) * D;
-      if (d < RH) {                    // rotary pair (d, d + RH)
-        dy = d + RH;
-        const float2 c = a.cs[(int64_t)qq.pos * RH + d];
-        const float qx = __bfloat162float(qr[d]), qy = __bfloat162float(qr[dy]);
-        x = fmaf(qx, c.x, -qy * c.y) * a.scale_log2;
-        y = fmaf(qx, c.y, qy * c.x) * a.scale_log2;
-      } else {                         // two dims past the rotary part
-        dx = R + 2 * (d - RH);
-        dy = dx + 1;
-        x = __bfloat162float(qr[dx]) * a.scale_log2;
-        y = __bfloat162float(qr[dy]) * a.scale_log2;
+      if (qq.pos >= 0 && qq.pos < a.max_pos) {
+        const __nv_bfloat16* qr = qg + ((int64_t)t * a.g.hq + hq) * D;
+        if (d < RH) {
+          const float2 c = a.cs[(int64_t)qq.pos * RH + d];
+          const float qx = __bfloat162float(qr[dx]), qy = __bfloat162float(qr[dy]);
+          x = fmaf(qx, c.x, -qy * c.y) * a.scale_log2;
+          y = fmaf(qx, c.y, qy * c.x) * a.scale_log2;
+        } else {
+          x = __bfloat162float(qr[dx]) * a.scale_log2;
+          y = __bfloat162float(qr[dy]) * a.scale_log2;
+        }
+      } else if (d == 0 && row % NH == 0) {
+        atomicOr(a.err, AKV_DERR_INDEX);
       }
-    } else if (d >= RH) {
-      dx = R + 2 * (d - RH);
-      dy = dx + 1;
-    } else {
-      dy = d + RH;
     }
-    __nv_bfloat16* q0 = reinterpret_cast<__nv_bfloat16*>(s_k + rsw<D>(row, dx / 8)) + dx % 8;
-    __nv_bfloat16* q1 = reinterpret_cast<__nv_bfloat16*>(s_k + rsw<D>(row, dy / 8)) + dy % 8;
-    *q0 = __float2bfloat16_rn(x);
-    *q1 = __float2bfloat16_rn(y);
+    *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dx / 8, kBM)) + dx % 8) = __float2bfloat16_rn(x);
+    *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dy / 8, kBM)) + dy % 8) = __float2bfloat16_rn(y);
   }
+  // this thread's row: key j is visible iff lo_r <= j < kend_r and the key
+  // is still alive at time_r (keys are born in slot order, so "born by
+  // time_r" is j < kend_r); padding rows see nothing
+  int time_r = -1, lo_r = 0, kend_r = 0;
+  const int t_r = tl.tok0 + tid / NH;
+  if (t_r < tend) {
+    const RestoreQuery qq = a.queries[t_r];
+    if (qq.pos >= 0 && qq.pos < a.max_pos) {
+      time_r = qq.time;
+      kend_r = qq.key_end;
+      lo_r = a.window > 0 ? max(0, qq.pos - a.window + 1) : 0;
+    }
+  }
+  // warp bounds for the unmasked fast path (padding rows do not constrain)
+  const bool real = t_r < tend;
+  const int w_kend = __reduce_min_sync(0xffffffffu, real ? kend_r : INT32_MAX);
+  const int w_lo = __reduce_max_sync(0xffffffffu, real ? lo_r : INT32_MIN);
+  const int w_time = __reduce_max_sync(0xffffffffu, real ? time_r : INT32_MIN);
+
+  const uint32_t mb = smem_u32(mbar), mbk = smem_u32(mbar + 1), mbv = smem_u32(mbar + 2);
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mb) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbk) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbv) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(tslot)), "r"(NCOL) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  proxy_fence();
+  tc_before();
   __syncthreads();
-  uint32_t qa[KS][4];
-  {
-    const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) ldsm_x4(smem_u32(s_k + rsw<D>(row, ks * 2 + (lane >> 4))), qa[ks]);
-  }
-  // per-row time and window bound (rows r0 = lane/4 and r1 = r0 + 8)
-  int time0 = -1, time1 = -1, lo0 = 0, lo1 = 0;
-  {
-    const int t0 = tbase + (lane >> 2), t1 = t0 + 8;
-    // a row past the tile or with a bad position sees no key (output 0)
-    if (t0 < tend) {
-      const RestoreQuery q0 = a.queries[t0];
-      time0 = q0.pos >= 0 && q0.pos < a.max_pos ? q0.time : -1;
-      lo0 = a.window > 0 ? q0.pos - a.window + 1 : 0;
-    }
-    if (t1 < tend) {
-      const RestoreQuery q1 = a.queries[t1];
-      time1 = q1.pos >= 0 && q1.pos < a.max_pos ? q1.time : -1;
-      lo1 = a.window > 0 ? q1.pos - a.window + 1 : 0;
-    }
-  }
-  __syncthreads();   // Q staging area is reused for key tiles
+  tc_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS = tbase, tO = tbase + kBN;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  const uint32_t id_s = idesc_bf16(kBM, kBN, 0), id_o = idesc_bf16(kBM, D, 1);
+  uint32_t ph = 0, ph_k = 0, ph_v = 0;
+  int k_out = 0, v_out = 0;     // TMA loads issued and not yet waited for
+  bool ok = true;
 
-  auto load_tile = [&](int kt, int buf) {
-    const int k0 = tl.key_lo + kt * kKT;
-    for (int i = tid; i < kKT * CH; i += 128) {
-      const int row = i / CH, ch = i % CH;
-      const int j = k0 + row;
-      const bool ok = j < tl.key_hi;
-      const int64_t off = ((int64_t)(tl.era_off + (ok ? j : 0)) * H + kvh) * D + ch * 8;
-      cp_async16(smem_u32(s_k + buf * TILE + rsw<D>(row, ch)), kg + off, ok);
-      cp_async16(smem_u32(s_v + buf * TILE + rsw<D>(row, ch)), vg + off, ok);
+  float m_r = -INFINITY, l_r = 0.f;
+  const int n_kt = (tl.key_hi - tl.key_lo + kBN - 1) / kBN;
+  // one tile's K (TMA) and its keys' deaths with per-warp minima
+  auto load_k = [&](int kt) {
+    if (kt >= n_kt) return;
+    ++k_out;
+    const int k0 = tl.key_lo + kt * kBN;
+    if (tid == 0) {
+      mbar_expect_tx(mbk, KV_BYTES);
+#pragma unroll
+      for (int at = 0; at < D / 64; ++at)
+        tma_load_3d(smem_u32(sK + at * kBN * 128), &a.tm_k, at * 64, kvh, tl.era_off + k0, mbk);
     }
-    for (int i = tid; i < kKT; i += 128) {
-      const int j = k0 + i;
-      int b = INT32_MAX, dth = 0;
-      if (j < tl.key_hi) {
-        const RestoreKey kk = a.keys[tl.era_off + j];
-        b = kk.birth;
-        dth = kk.death;
-      }
-      s_birth[buf * kKT + i] = b;
-      s_death[buf * kKT + i] = dth;
+    if (tid < kBN) {
+      const int j = k0 + tid;
+      const int dd = j < tl.key_hi ? a.keys[tl.era_off + j].death : 0;
+      s_death[(kt & 1) * kBN + tid] = dd;
+      const int wm = __reduce_min_sync(0xffffffffu, dd);
+      if ((tid & 31) == 0) s_dmin[(kt & 1) * 2 + (tid >> 5)] = wm;
     }
-    cp_commit();
   };
-
-  float o[NTD][4];
+  auto load_v = [&](int kt) {
+    if (kt >= n_kt) return;
+    ++v_out;
+    if (tid != 0) return;
+    const int k0 = tl.key_lo + kt * kBN;
+    mbar_expect_tx(mbv, KV_BYTES);
 #pragma unroll
-  for (int n = 0; n < NTD; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int n_kt = (tl.key_hi - tl.key_lo + kKT - 1) / kKT;
-  if (n_kt > 0) load_tile(0, 0);
-  for (int kt = 0; kt < n_kt; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < n_kt) {
-      load_tile(kt + 1, buf ^ 1);
-      cp_wait<1>();
+    for (int at = 0; at < D / 64; ++at)
+      tma_load_3d(smem_u32(sV + at * kBN * 128), &a.tm_v, at * 64, kvh, tl.era_off + k0, mbv);
+  };
+  load_k(0);
+  load_v(0);
+  for (int kt = 0; kt < n_kt && ok; ++kt) {
+    const int k0 = tl.key_lo + kt * kBN;
+    ok = __syncthreads_and(mbar_wait(mbk, ph_k, a.wait_limit));    // K(kt), deaths(kt)
+    if (!ok) break;
+    ph_k ^= 1;
+    --k_out;
+    tc_after();
+    // S = Q K^T
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qa = smem_u32(sQ) + (kk >> 2) * kBM * 128 + (kk & 3) * 32;
+        const uint32_t ka = smem_u32(sK) + (kk >> 2) * kBN * 128 + (kk & 3) * 32;
+        umma(tS, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), id_s, kk > 0);
+      }
+      umma_commit(mb);
+    }
+    ok = __syncthreads_and(mbar_wait(mb, ph, a.wait_limit));
+    ph ^= 1;
+    tc_after();
+    if (!ok) break;
+    // this tile's deaths are read before K(kt+1) fills the other buffer
+    const int* de = s_death + (kt & 1) * kBN;
+    const int dmin = min(s_dmin[(kt & 1) * 2], s_dmin[(kt & 1) * 2 + 1]);
+    const bool full = k0 >= w_lo && k0 + kBN <= w_kend && dmin > w_time;   // warp-uniform
+    load_k(kt + 1);             // K buffer is free: prefetch the next tile
+    uint32_t sr[kBN];
+    tmem_ld32(tS + lane_off, sr);
+    tmem_ld32(tS + lane_off + 32, sr + 32);
+    tmem_wait_ld();
+    float sv[kBN];
+    float mx = -INFINITY;
+    if (full) {
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) {
+        sv[c] = __uint_as_float(sr[c]);
+        mx = fmaxf(mx, sv[c]);
+      }
     } else {
-      cp_wait<0>();
-    }
-    __syncthreads();
-    const uint32_t kb = smem_u32(s_k + buf * TILE), vb = smem_u32(s_v + buf * TILE);
-    const int k0 = tl.key_lo + kt * kKT;
-    // S = Q K^T: 16 rows x 64 keys per warp
-    float sc[8][4];
 #pragma unroll
-    for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-      for (int n2 = 0; n2 < 4; ++n2) {
-        uint32_t b[4];
-        ldsm_x4(kb + rsw<D>(n2 * 16 + (lane & 7) + ((lane >> 4) & 1) * 8, ks * 2 + ((lane >> 3) & 1)), b);
-        mma16816(sc[2 * n2], qa[ks], b[0], b[1]);
-        mma16816(sc[2 * n2 + 1], qa[ks], b[2], b[3]);
+      for (int c = 0; c < kBN; ++c) {
+        const int j = k0 + c;
+        const bool vis = j >= lo_r && j < kend_r && de[c] > time_r;
+        sv[c] = vis ? __uint_as_float(sr[c]) : -INFINITY;
+        mx = fmaxf(mx, sv[c]);
       }
     }
-    // interval mask (and window)
-    const int* bi = s_birth + buf * kKT;
-    const int* de = s_death + buf * kKT;
+    // the reference max moves only when the row max grows by more than 2^8
+    const float m_new = (mx > m_r + 8.f) ? mx : m_r;
+    const float alpha = m_new == -INFINITY ? 1.f : ex2(m_r - m_new);
+    const float msub = m_new == -INFINITY ? 0.f : m_new;
+    float ps = 0.f;
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
+    for (int c = 0; c < kBN; c += 8) {
+      float p[8];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int kc = n * 8 + (lane & 3) * 2 + e;
-        const int j = k0 + kc;
-        const int b = bi[kc], dd = de[kc];
-        if (!(b <= time0 && time0 < dd && j >= lo0)) sc[n][e] = -INFINITY;
-        if (!(b <= time1 && time1 < dd && j >= lo1)) sc[n][2 + e] = -INFINITY;
+      for (int e = 0; e < 8; ++e) {
+        p[e] = ex2(sv[c + e] - msub);
+        ps += p[e];
       }
+      uint4 w;
+      w.x = pack_bf16x2(p[0], p[1]);
+      w.y = pack_bf16x2(p[2], p[3]);
+      w.z = pack_bf16x2(p[4], p[5]);
+      w.w = pack_bf16x2(p[6], p[7]);
+      *reinterpret_cast<uint4*>(sP + sw128(tid, c / 8, kBM)) = w;
     }
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    l_r = fmaf(l_r, alpha, ps);
+    m_r = m_new;
+    if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-      mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
-    }
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + lane_off + c, o);
+        tmem_wait_ld();
 #pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(tO + lane_off + c, o);
+      }
+      tmem_wait_st();
     }
-    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
-    const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
-    m0 = n0;
-    m1 = n1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      sc[n][0] = n0 == -INFINITY ? 0.f : exp2f(sc[n][0] - n0);
-      sc[n][1] = n0 == -INFINITY ? 0.f : exp2f(sc[n][1] - n0);
-      sc[n][2] = n1 == -INFINITY ? 0.f : exp2f(sc[n][2] - n1);
-      sc[n][3] = n1 == -INFINITY ? 0.f : exp2f(sc[n][3] - n1);
-      ps0 += sc[n][0] + sc[n][1];
-      ps1 += sc[n][2] + sc[n][3];
-    }
-    l0 = fmaf(l0, a0, ps0);
-    l1 = fmaf(l1, a1, ps1);
-#pragma unroll
-    for (int n = 0; n < NTD; ++n) {
-      o[n][0] *= a0; o[n][1] *= a0; o[n][2] *= a1; o[n][3] *= a1;
-    }
+    proxy_fence();
+    tc_before();
+    ok = __syncthreads_and(mbar_wait(mbv, ph_v, a.wait_limit));    // V(kt); P written
+    tc_after();
+    if (!ok) break;
+    ph_v ^= 1;
+    --v_out;
     // O += P V
+    if (tid == 0) {
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-      pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-      pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-      pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint32_t pa = smem_u32(sP) + kk * 32;
+        const uint32_t va = smem_u32(sV) + kk * 16 * 128;
+        umma(tO, sdesc(pa, 16, 1024), sdesc(va, kBN * 128, 1024), id_o, kt > 0 || kk > 0);
+      }
+      umma_commit(mb);
+    }
+    ok = __syncthreads_and(mbar_wait(mb, ph, a.wait_limit));
+    ph ^= 1;
+    tc_after();
+    load_v(kt + 1);             // V buffer is free
+  }
+  if (!ok) {
+    if (tid == 0) atomicOr(a.err, AKV_DERR_WAIT);
+    // let the (at most one each) copies still in flight land before the
+    // CTA's shared memory goes; bounded
+    if (k_out > 0) mbar_wait(mbk, ph_k, a.wait_limit);
+    if (v_out > 0) mbar_wait(mbv, ph_v, a.wait_limit);
+  }
+  // epilogue: O / l of this thread's row
+  if (ok && n_kt > 0) {
+    const int hq = kvh * G + blockIdx.z * NH + tid % NH;
+    float* po = a.out + ((int64_t)t_r * a.g.hq + hq) * D;
+    const float inv = l_r > 0.f ? 1.f / l_r : 0.f;
 #pragma unroll
-      for (int nd2 = 0; nd2 < NTD / 2; ++nd2) {
-        uint32_t b[4];
-        ldsm_x4_t(vb + rsw<D>(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, nd2 * 2 + (lane >> 4)), b);
-        mma16816(o[2 * nd2], pa, b[0], b[1]);
-        mma16816(o[2 * nd2 + 1], pa, b[2], b[3]);
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      tmem_ld32(tO + lane_off + c, o);
+      tmem_wait_ld();
+      if (t_r < tend) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(po + c + e) =
+              make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                          __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
       }
     }
-    __syncthreads();   // this buffer is refilled next-but-one iteration
   }
-#pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  const int t0 = tbase + (lane >> 2), t1 = t0 + 8;
-  const int hq = kvh * G + head;
-#pragma unroll
-  for (int n = 0; n < NTD; ++n) {
-    const int d = n * 8 + (lane & 3) * 2;
-    if (t0 < tend) {
-      float* po = a.out + ((int64_t)t0 * a.g.hq + hq) * D + d;
-      po[0] = l0 > 0.f ? o[n][0] / l0 : 0.f;
-      po[1] = l0 > 0.f ? o[n][1] / l0 : 0.f;
-    }
-    if (t1 < tend) {
-      float* po = a.out + ((int64_t)t1 * a.g.hq + hq) * D + d;
-      po[0] = l1 > 0.f ? o[n][2] / l1 : 0.f;
-      po[1] = l1 > 0.f ? o[n][3] / l1 : 0.f;
-    }
-  }
+  tc_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(NCOL) : "memory");
 }
 
 template <int D, int NH>
-cudaError_t launch_mma_nh(const RestoreArgs& a, int G, cudaStream_t st) {
-  const size_t smem = 4 * (size_t)kKT * D * 2 + 4 * kKT * sizeof(int);
+cudaError_t launch_tc_nh(const RestoreArgs& a, int G, cudaStream_t st) {
+  constexpr size_t smem = restore_tc_smem<D>();
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(k_restore_attn_mma<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(k_restore_attn_tc<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
     attr = true;
   }
   const dim3 grid(a.n_tiles, a.g.hkv, G / NH);
-  k_restore_attn_mma<D, NH><<<grid, 128, smem, st>>>(a);
+  k_restore_attn_tc<D, NH><<<grid, 128, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_mma(const RestoreArgs& a, cudaStream_t st) {
+cudaError_t launch_tc(const RestoreArgs& a, cudaStream_t st) {
   const int G = a.g.hq / a.g.hkv;
   switch (G) {
-    case 1: return launch_mma_nh<D, 1>(a, G, st);
-    case 2: return launch_mma_nh<D, 2>(a, G, st);
-    default: return launch_mma_nh<D, 4>(a, G, st);
+    case 1: return launch_tc_nh<D, 1>(a, G, st);
+    case 2: return launch_tc_nh<D, 2>(a, G, st);
+    case 4: return launch_tc_nh<D, 4>(a, G, st);
+    default: return launch_tc_nh<D, 8>(a, G, st);
   }
 }
 
 }  // namespace
+
+bool make_restore_tensor_maps(const Geom& g, const void* k_era, const void* v_era, int64_t n_keys,
+                              CUtensorMap* tk, CUtensorMap* tv) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&encode),
+                                         12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !encode) {
+      encode = nullptr;
+      return false;
+    }
+  }
+  if (n_keys < 1) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)g.hkv, (cuuint64_t)n_keys};
+  const cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)g.hkv * g.d * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBN};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = encode(i == 0 ? tk : tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(i == 0 ? k_era : v_era), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+  }
+  return true;
+}
 
 bool restore_mma_supported(const Geom& g) {
   const int G = g.hq / g.hkv;
@@ -486,7 +634,7 @@ bool restore_mma_supported(const Geom& g) {
 
 int restore_tile_tokens(const Geom& g) {
   const int G = g.hq / g.hkv;
-  return 16 * (4 / (G < 4 ? G : 4));
+  return kBM / (G < 8 ? G : 8);
 }
 
 cudaError_t launch_restore(const RestoreArgs& a, cudaStream_t st) {
@@ -507,7 +655,7 @@ cudaError_t launch_restore(const RestoreArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   if (a.n_queries <= 0) return cudaSuccess;
-  if (a.use_mma) return a.g.d == 64 ? launch_mma<64>(a, st) : launch_mma<128>(a, st);
+  if (a.use_mma) return a.g.d == 64 ? launch_tc<64>(a, st) : launch_tc<128>(a, st);
   const int G = a.g.hq / a.g.hkv;
   if (a.g.dtype == AKV_DTYPE_BF16)
     return a.g.d == 64 ? launch_simple_g<__nv_bfloat16, 64>(a, G, st)

@@ -553,6 +553,165 @@ def restore_arm(args):
     cache.close()
 
 
+# ---------------------------------------------------------------------------
+# history-keyed prefix sharing and drop-aware eviction (its own line: --prefix)
+# ---------------------------------------------------------------------------
+
+def prefix_arm(args):
+    """One long-running agent sequence (8B shape, ~34k tokens, 30 turns,
+    drops of old tool spans and a reposition every 3 turns) published at the
+    end of every turn (30 entries).  Timed: host matching of two requests,
+    an exact fork that continues the conversation (every page shared), a
+    retrigger fork of a request that skipped the last reposition (every
+    survivor after the first dropped span rotated into fresh pages: the
+    k_transplant kernel, HBM-bound), and drop-aware eviction of all
+    entries."""
+    import torch
+    from agent_kv_cache_gb300 import Cache, PrefixIndex, build
+    from workloads import device as dev
+    build()
+    dev.build()
+    sh = SHAPE
+    seed = RESTORE_SEED
+    turns = traces.turn_programs(seed)
+    n_total = sum(op[1] for t in turns for op in t if op[0] == "append")
+    ids = traces.token_ids(seed, n_total + 64)
+    S = sh.page_size
+    max_pages = 16384
+    cache = Cache(sh.layers, sh.hq, sh.hkv, sh.head_dim, S, sh.dtype, max_pages, 64,
+                  n_total + 64, sh.rope_theta)
+    idx = PrefixIndex(S)
+    st = cache.stream
+    w = synth.width_for(sh.dtype)
+    live = cache.seq_create()
+    hist, t = [], 0
+    entries = []
+    for ops in turns:
+        for op in ops:
+            if op[0] == "append":
+                n = op[1]
+                for c0 in range(0, n, CHUNK):
+                    m = min(CHUNK, n - c0)
+                    k = torch.empty((sh.layers, m, sh.hkv, sh.head_dim), dtype=torch.bfloat16,
+                                    device="cuda")
+                    v = torch.empty_like(k)
+                    keep = [dev.kv_tokens(k, seed, 1, synth.KIND_K, range(sh.layers), t, m,
+                                          sh.hkv, sh.head_dim, w),
+                            dev.kv_tokens(v, seed, 1, synth.KIND_V, range(sh.layers), t, m,
+                                          sh.hkv, sh.head_dim, w)]
+                    torch.cuda.synchronize()
+                    cache.append([live], [m], k, v, ids[t:t + m].tolist())
+                    torch.cuda.synchronize()
+                    del keep
+                    t += m
+            elif op[0] == "drop":
+                cache.drop(live, op[1])
+            else:
+                cache.reposition([live])
+        hist += ops
+        entries.append(cache.prefix_publish(idx, live, hist, ids[:t].tolist()))
+    torch.cuda.synchronize()
+    assert cache.sync_errors() == 0
+    n_tok = t
+    # requests: continue the conversation (exact), and the history without its
+    # last reposition followed by one new turn (retrigger)
+    cont = hist + [("append", 64)]
+    cont_ids = ids[:n_tok + 64].tolist()
+    assert hist[-1][0] == "repos"
+    skip = hist[:-1] + [("append", 64)]
+
+    def timed_host(fn, reps):
+        fn()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        return (time.perf_counter() - t0) / reps
+
+    match_cont = timed_host(lambda: idx.match(cont, cont_ids), 20)
+    match_skip = timed_host(lambda: idx.match(skip, cont_ids), 20)
+    m_skip = idx.match(skip, cont_ids)
+    m_cont = idx.match(cont, cont_ids)
+    # forks: GPU time by events on the cache stream (a spin on the stream
+    # first, so that the call's host planning is over before the start event
+    # fires and only the GPU work is timed), host time by the clock
+    def fork_times(prog, reps):
+        gpu_ms, host_s = [], []
+        for i in range(args.warmup + reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(st):
+                torch.cuda._sleep(20_000_000)
+            t0 = time.perf_counter()
+            a.record(st)
+            child, m = cache.prefix_fork(idx, prog, cont_ids)
+            b.record(st)
+            t1 = time.perf_counter()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                gpu_ms.append(a.elapsed_time(b))
+                host_s.append(t1 - t0)
+            info = cache.info(child)
+            cache.seq_free(child)
+        return float(np.mean(gpu_ms)), float(np.mean(host_s)), m, info
+
+    n0 = cache.kernel_launches()
+    ex_gpu, ex_host, m1, info1 = fork_times(cont, args.steps)
+    re_gpu, re_host, m2, info2 = fork_times(skip, args.steps)
+    launches = cache.kernel_launches() - n0
+    assert cache.sync_errors() == 0
+    moved = m2["n_rotated"]
+    # algorithmic bytes of the retrigger fork: every rotated key and its value
+    # read and written once on every layer, plus the keys copied unrotated
+    # into fresh pages (tokens of a moved page that keep their position)
+    per_tok = sh.layers * 2 * sh.hkv * sh.head_dim * BYTES_EL
+    plan_tokens = info2["n_active"]
+    # tokens in fresh pages = rotated keys + unrotated ones sharing their pages;
+    # count from the page table: pages not shared with the entry
+    child, _ = cache.prefix_fork(idx, skip, cont_ids)
+    pc, _ = cache.page_table(child)
+    pe, _ = cache.page_table(m2["entry"])
+    keep = cache.keep_mask(child)
+    fresh_pages = [k for k in range(len(pc)) if pc[k] >= 0 and (k >= len(pe) or pc[k] != pe[k])]
+    fresh_tok = int(sum(keep[k * S:(k + 1) * S].sum() for k in fresh_pages))
+    cache.seq_free(child)
+    algo = 2 * fresh_tok * per_tok
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = peaks.get("hbm_gbs", 6800.0)
+    gbs = algo / (re_gpu * 1e-3) / 1e9
+    used_before = cache.pool_stats()[1]
+    t0 = time.perf_counter()
+    freed, n_ev = cache.prefix_evict(idx, 1 << 30)
+    ev_s = time.perf_counter() - t0
+    cache.seq_free(live)
+    line = {
+        "metric": "prefix fork (retrigger) GB/s & history-keyed matching / eviction latency",
+        "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (seeded K/V and token ids, seeded agent turn schedule)",
+        "config": {"workload": f"{sh.name}-shaped long-running agent sequence: {n_tok} tokens, "
+                               f"{len(turns)} turns published as {len(set(entries))} entries; "
+                               "requests: continue (exact), skip the last reposition (retrigger)",
+                   "page_size": S},
+        "match_us": {"continue": round(match_cont * 1e6, 1), "skip_repos": round(match_skip * 1e6, 1)},
+        "exact_fork": {"match": m1, "gpu_ms": round(ex_gpu, 4), "host_ms": round(ex_host * 1e3, 3),
+                       "tokens": info1["n_active"]},
+        "retrigger_fork": {"match": m2, "gpu_ms": round(re_gpu, 4),
+                           "host_ms": round(re_host * 1e3, 3), "fresh_pages": len(fresh_pages),
+                           "tokens_in_fresh_pages": fresh_tok, "tokens": plan_tokens,
+                           "algorithmic_bytes": algo},
+        "roofline": {"kernel": "k_transplant (retrigger fork)", "bound": "hbm",
+                     "achieved": round(gbs, 1), "peak": peak,
+                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+                     "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None},
+        "eviction": {"entries": n_ev, "pages_freed": freed, "pages_used_before": used_before,
+                     "host_ms": round(ev_s * 1e3, 3)},
+        "gpu_launches": int(launches),
+    }
+    print(json.dumps(line), flush=True)
+    cache.close()
+
+
 def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -590,6 +749,8 @@ def main():
     ap.add_argument("--restore", action="store_true",
                     help="time segment-batch restore attention instead (its own line)")
     ap.add_argument("--restore-cuda-cores", action="store_true")
+    ap.add_argument("--prefix", action="store_true",
+                    help="time prefix matching / forks / eviction instead (its own line)")
     # smaller cases for profiler captures only; a line printed with any of
     # these is marked "profiling case" and is not the benchmark's number
     ap.add_argument("--batch", type=int, default=None)
@@ -604,7 +765,9 @@ def main():
         args.profiling_case = True
     else:
         args.profiling_case = False
-    if args.restore or args.restore_cuda_cores:
+    if args.prefix:
+        prefix_arm(args)
+    elif args.restore or args.restore_cuda_cores:
         restore_arm(args)
     elif args.impl == "reference":
         reference_arm(args)

@@ -193,3 +193,107 @@ def test_restore_llama8b_fullsize():
         tmax, tmean = ATTN_TOL[sh.dtype]
         assert err.max() <= tmax and err.mean() <= tmean, (l, err.max(), err.mean())
     gpu.close()
+
+
+def test_prefix_fork_llama8b_fullsize():
+    """The prefix-sharing workload at full size (8B shape, ~34k-token agent
+    sequence published at every turn end), as the prefix benchmark runs it:
+    the retrigger fork of the request that skipped the last reposition and
+    the exact fork of the continuing request.  Checked: the match against
+    properties the oracle's records fix at any size (equal records up to n,
+    the next record differs, every needed key stored, rotated count), the
+    child's keep mask / logical map bit-exact, and layer-0 keys and values
+    against a cache built directly from the request prefix on sampled
+    tokens."""
+    import oracle.akv_prefix as P
+    from agent_kv_cache_gb300 import PrefixIndex
+    from twin import key_tolerance
+    sh = traces.LLAMA8B
+    seed = traces.seed_for(5)
+    turns = traces.turn_programs(seed)
+    n_total = sum(op[1] for t in turns for op in t if op[0] == "append")
+    ids = traces.token_ids(seed, n_total + 64)
+    S, L, H, D = sh.page_size, sh.layers, sh.hkv, sh.head_dim
+    w = synth.width_for(sh.dtype)
+    gpu = Cache(L, sh.hq, H, D, S, sh.dtype, 16384, 64, n_total + 64, sh.rope_theta)
+    idx = PrefixIndex(S)
+    live = gpu.seq_create()
+    hist, t, entries = [], 0, {}
+    for ops in turns:
+        for op in ops:
+            if op[0] == "append":
+                for c0 in range(0, op[1], 4096):
+                    m = min(4096, op[1] - c0)
+                    k = torch.empty((L, m, H, D), dtype=torch.bfloat16, device="cuda")
+                    v = torch.empty_like(k)
+                    keep = [device.kv_tokens(k, seed, 1, synth.KIND_K, range(L), t, m, H, D, w),
+                            device.kv_tokens(v, seed, 1, synth.KIND_V, range(L), t, m, H, D, w)]
+                    torch.cuda.synchronize()
+                    gpu.append([live], [m], k, v, ids[t:t + m].tolist())
+                    torch.cuda.synchronize()
+                    del keep
+                    t += m
+            elif op[0] == "drop":
+                gpu.drop(live, op[1])
+            else:
+                gpu.reposition([live])
+        hist += ops
+        e = gpu.prefix_publish(idx, live, hist, ids[:t].tolist())
+        entries[e] = P.records(hist, ids[:t])
+    assert gpu.sync_errors() == 0
+    cont_ids = ids[:t + 64].tolist()
+    skip = hist[:-1] + [("append", 64)]
+    cont = hist + [("append", 64)]
+    last = max(entries)
+    for prog, kind in ((skip, "retrigger"), (cont, "exact")):
+        req = P.records(prog, cont_ids)
+        child, m = gpu.prefix_fork(idx, prog, cont_ids)
+        assert m["kind"] == kind and m["entry"] == last
+        n = m["n_records"]
+        er = entries[last]
+        assert req[:n] == er[:n] and (n == len(er) or n == len(req) or req[n] != er[n])
+        st = P.State(req[:n])
+        stored = P.State(er).stored(S)
+        need = [x for x in range(len(st.alive)) if st.alive[x]]
+        assert all(x in stored for x in need)
+        assert m["n_rotated"] == sum(stored[x] != st.pos[x] for x in need)
+        if kind == "retrigger":
+            assert m["n_rotated"] > 1000
+        held = [x for x in range(len(st.alive)) if st.held[x]]
+        np.testing.assert_array_equal(gpu.logical(child), held)
+        np.testing.assert_array_equal(gpu.keep_mask(child), [st.alive[x] for x in held])
+        # layer-0 keys of sampled needed tokens against the direct oracle replay
+        oc = OracleCache(sh.hq, H, D, sh.rope_theta, sh.dtype, layers=(0,), page_size=S)
+        osid = oc.create()
+        tt = 0
+        covered = list(prog[:m["op_index"]])
+        if m["op_tokens"]:
+            covered.append(("append", m["op_tokens"]))
+        for op in covered:
+            if op[0] == "append":
+                cnt = op[1]
+                kk = synth.kv_tokens(seed, 1, synth.KIND_K, [0], tt, cnt, H, D, w)
+                vv = synth.kv_tokens(seed, 1, synth.KIND_V, [0], tt, cnt, H, D, w)
+                oc.append(osid, kk, vv)
+                tt += cnt
+            elif op[0] == "drop":
+                oc.drop(osid, op[1])
+            else:
+                oc.reposition(osid)
+        os_ = oc.seqs[osid]
+        assert np.array_equal(os_.logical, held)
+        kg, vg = gpu.read_kv(child, 0)
+        rng = np.random.default_rng(3)
+        live_slots = np.flatnonzero(os_.alive)
+        pick = rng.choice(live_slots, size=min(512, live_slots.size), replace=False)
+        ref = os_.K[0][pick]
+        n_rot = 1 + sum(1 for r in er if r[0] == "R") + 1
+        assert not (np.abs(kg[pick] - ref) > key_tolerance(ref, sh.dtype, n_rot)).any()
+        np.testing.assert_array_equal(vg[pick], os_.V[0][pick])
+        gpu.seq_free(child)
+    assert gpu.sync_errors() == 0
+    freed, n_ev = gpu.prefix_evict(idx, 1 << 30)
+    assert n_ev == len(entries) and freed > 0
+    gpu.seq_free(live)
+    assert gpu.pool_stats()[1] == 0
+    gpu.close()

@@ -260,3 +260,27 @@ def restore_program(seed, n_turns=30, sys_len=1024, decode_per_turn=64, active_c
         if t.repos:
             prog.append(("repos",))
     return prog
+
+
+def turn_programs(seed, n_turns=30, sys_len=1024, decode_per_turn=64, active_cap=16384):
+    """The same long-running sequence as ``restore_program``, cut at the end
+    of every turn: element k is the list of operations of turn k (turn 0
+    starts with the system prompt).  Concatenating elements 0..k gives the
+    sequence's history after turn k."""
+    turns = steady_state(seed, n_seqs=1, n_turns=n_turns, sys_len=sys_len,
+                         decode_per_turn=decode_per_turn, active_cap=active_cap)[0]
+    out = []
+    for k, t in enumerate(turns):
+        ops = [("append", sys_len)] if k == 0 else []
+        ops.append(("append", t.tool_len + decode_per_turn))
+        if t.drop_ranges:
+            ops.append(("drop", list(t.drop_ranges)))
+        if t.repos:
+            ops.append(("repos",))
+        out.append(ops)
+    return out
+
+
+def token_ids(seed, n, vocab=128256):
+    """Seeded synthetic token ids (uniform over a Llama-3-sized vocabulary)."""
+    return np.random.default_rng([seed, 77]).integers(0, vocab, size=n).astype(np.int32)
