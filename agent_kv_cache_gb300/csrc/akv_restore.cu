@@ -233,6 +233,12 @@ __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_
                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
                ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(acc));
 }
+// A operand from tensor memory (row per lane, bf16 pairs per 32-bit column)
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, int acc) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
 __device__ __forceinline__ void umma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                ::"r"(mbar) : "memory");
@@ -300,12 +306,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// TMEM columns: two S buffers (kBN each) and O (D), rounded to a power of 2
 template <int D>
-__host__ __device__ constexpr int restore_tc_cols() { return D == 64 ? 128 : 256; }   // TMEM columns (power of 2)
+__host__ __device__ constexpr int restore_tc_cols() { return 256; }
+static_assert(2 * kBN + 128 <= 256, "S buffers and O must fit the TMEM allocation");
 template <int D>
 constexpr size_t restore_tc_smem() {
-  return 1024 /* alignment slack */ + (size_t)kBM * D * 2 + 2 * (size_t)kBN * D * 2 +
-         (size_t)kBM * kBN * 2 + 2 * kBN * sizeof(int) + 4 * sizeof(int) + 32;
+  return 1024 /* alignment slack */ + (size_t)kBM * D * 2 + 4 * (size_t)kBN * D * 2 +
+         2 * kBN * sizeof(int) + 4 * sizeof(int) + 7 * sizeof(uint64_t) + 16;
 }
 
 template <int D, int NH>
@@ -316,13 +324,12 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm;                           // kBM x D (K-major)
-  uint8_t* sK = sQ + kBM * D * 2;             // kBN x D, TMA 64-element atoms
-  uint8_t* sV = sK + kBN * D * 2;             // same layout, read MN-major
-  uint8_t* sP = sV + kBN * D * 2;             // kBM x kBN (K-major)
-  int* s_death = reinterpret_cast<int*>(sP + kBM * kBN * 2);   // [2][kBN]
-  int* s_dmin = s_death + 2 * kBN;                              // [2][2] per-warp minima
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(s_dmin + 4);     // MMA, K, V
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 3);
+  uint8_t* sK = sQ + kBM * D * 2;             // [2] kBN x D, TMA 64-element atoms
+  uint8_t* sV = sK + 2 * kBN * D * 2;         // [2] same layout, read MN-major
+  int* s_death = reinterpret_cast<int*>(sV + 2 * kBN * D * 2);   // [2][kBN]
+  int* s_dmin = s_death + 2 * kBN;                                // [2][2] per-warp minima
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(s_dmin + 4);       // S[2], O, K[2], V[2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 7);
 
   const RestoreTile tl = a.tiles[blockIdx.x];
   const int kvh = blockIdx.y;
@@ -380,11 +387,11 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
   const int w_lo = __reduce_max_sync(0xffffffffu, real ? lo_r : INT32_MIN);
   const int w_time = __reduce_max_sync(0xffffffffu, real ? time_r : INT32_MIN);
 
-  const uint32_t mb = smem_u32(mbar), mbk = smem_u32(mbar + 1), mbv = smem_u32(mbar + 2);
+  const uint32_t mbS0 = smem_u32(mbar), mbO = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 3),
+                 mbV0 = smem_u32(mbar + 5);
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mb) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbk) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbv) : "memory");
+    for (int i = 0; i < 7; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar + i)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -392,81 +399,101 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
                  ::"r"(smem_u32(tslot)), "r"(NCOL) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  const int n_kt = (tl.key_hi - tl.key_lo + kBN - 1) / kBN;
+  // deaths of tile kt (and per-warp minima) into buffer kt & 1
+  auto load_deaths = [&](int kt) {
+    if (kt >= n_kt || tid >= kBN) return;
+    const int j = tl.key_lo + kt * kBN + tid;
+    const int dd = j < tl.key_hi ? a.keys[tl.era_off + j].death : 0;
+    s_death[(kt & 1) * kBN + tid] = dd;
+    const int wm = __reduce_min_sync(0xffffffffu, dd);
+    if ((tid & 31) == 0) s_dmin[(kt & 1) * 2 + (tid >> 5)] = wm;
+  };
+  load_deaths(0);
+  load_deaths(1);
   proxy_fence();
   tc_before();
   __syncthreads();
   tc_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tO = tbase + kBN;
+  const uint32_t tO = tbase + 2 * kBN;                          // S buffers at 0 and kBN
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
   const uint32_t id_s = idesc_bf16(kBM, kBN, 0), id_o = idesc_bf16(kBM, D, 1);
-  uint32_t ph = 0, ph_k = 0, ph_v = 0;
-  int k_out = 0, v_out = 0;     // TMA loads issued and not yet waited for
-  bool ok = true;
 
-  float m_r = -INFINITY, l_r = 0.f;
-  const int n_kt = (tl.key_hi - tl.key_lo + kBN - 1) / kBN;
-  // one tile's K (TMA) and its keys' deaths with per-warp minima
-  auto load_k = [&](int kt) {
-    if (kt >= n_kt) return;
-    ++k_out;
-    const int k0 = tl.key_lo + kt * kBN;
-    if (tid == 0) {
-      mbar_expect_tx(mbk, KV_BYTES);
-#pragma unroll
-      for (int at = 0; at < D / 64; ++at)
-        tma_load_3d(smem_u32(sK + at * kBN * 128), &a.tm_k, at * 64, kvh, tl.era_off + k0, mbk);
-    }
-    if (tid < kBN) {
-      const int j = k0 + tid;
-      const int dd = j < tl.key_hi ? a.keys[tl.era_off + j].death : 0;
-      s_death[(kt & 1) * kBN + tid] = dd;
-      const int wm = __reduce_min_sync(0xffffffffu, dd);
-      if ((tid & 31) == 0) s_dmin[(kt & 1) * 2 + (tid >> 5)] = wm;
-    }
-  };
-  auto load_v = [&](int kt) {
-    if (kt >= n_kt) return;
-    ++v_out;
-    if (tid != 0) return;
-    const int k0 = tl.key_lo + kt * kBN;
-    mbar_expect_tx(mbv, KV_BYTES);
+  // thread 0 owns the TMA copies and the MMAs; pending work for the drain
+  int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1}, s_pend = -1, o_pend = -1;
+  auto tma_k = [&](int kt) {
+    const int b = kt & 1;
+    mbar_expect_tx(mbK0 + 8 * b, KV_BYTES);
 #pragma unroll
     for (int at = 0; at < D / 64; ++at)
-      tma_load_3d(smem_u32(sV + at * kBN * 128), &a.tm_v, at * 64, kvh, tl.era_off + k0, mbv);
+      tma_load_3d(smem_u32(sK + b * kBN * D * 2 + at * kBN * 128), &a.tm_k, at * 64, kvh,
+                  tl.era_off + tl.key_lo + kt * kBN, mbK0 + 8 * b);
+    k_pend[b] = kt;
   };
-  load_k(0);
-  load_v(0);
-  for (int kt = 0; kt < n_kt && ok; ++kt) {
-    const int k0 = tl.key_lo + kt * kBN;
-    ok = __syncthreads_and(mbar_wait(mbk, ph_k, a.wait_limit));    // K(kt), deaths(kt)
-    if (!ok) break;
-    ph_k ^= 1;
-    --k_out;
-    tc_after();
-    // S = Q K^T
-    if (tid == 0) {
+  auto tma_v = [&](int kt) {
+    const int b = kt & 1;
+    mbar_expect_tx(mbV0 + 8 * b, KV_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t qa = smem_u32(sQ) + (kk >> 2) * kBM * 128 + (kk & 3) * 32;
-        const uint32_t ka = smem_u32(sK) + (kk >> 2) * kBN * 128 + (kk & 3) * 32;
-        umma(tS, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), id_s, kk > 0);
-      }
-      umma_commit(mb);
+    for (int at = 0; at < D / 64; ++at)
+      tma_load_3d(smem_u32(sV + b * kBN * D * 2 + at * kBN * 128), &a.tm_v, at * 64, kvh,
+                  tl.era_off + tl.key_lo + kt * kBN, mbV0 + 8 * b);
+    v_pend[b] = kt;
+  };
+  auto issue_s = [&](int kt) {        // S(kt) = Q K(kt)^T into S buffer kt & 1
+    const int b = kt & 1;
+    const uint32_t kb = smem_u32(sK + b * kBN * D * 2);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t qa = smem_u32(sQ) + (kk >> 2) * kBM * 128 + (kk & 3) * 32;
+      const uint32_t ka = kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32;
+      umma(tbase + b * kBN, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), id_s, kk > 0);
     }
-    ok = __syncthreads_and(mbar_wait(mb, ph, a.wait_limit));
-    ph ^= 1;
+    umma_commit(mbS0 + 8 * b);
+    s_pend = kt;
+  };
+  bool bad = false;
+  if (tid == 0 && n_kt > 0) {
+    tma_k(0);
+    tma_v(0);
+    if (n_kt > 1) { tma_k(1); tma_v(1); }
+    bad = !mbar_wait(mbK0, 0, a.wait_limit);
+    if (!bad) { k_pend[0] = -1; tc_after(); issue_s(0); }
+  }
+  float m_r = -INFINITY, l_r = 0.f;
+  for (int kt = 0; kt < n_kt; ++kt) {
+    const int b = kt & 1;
+    const int k0 = tl.key_lo + kt * kBN;
+    const uint32_t tSb = tbase + b * kBN;
+    // S(kt) done
+    bad |= !mbar_wait(mbS0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
     tc_after();
-    if (!ok) break;
-    // this tile's deaths are read before K(kt+1) fills the other buffer
-    const int* de = s_death + (kt & 1) * kBN;
-    const int dmin = min(s_dmin[(kt & 1) * 2], s_dmin[(kt & 1) * 2 + 1]);
-    const bool full = k0 >= w_lo && k0 + kBN <= w_kend && dmin > w_time;   // warp-uniform
-    load_k(kt + 1);             // K buffer is free: prefetch the next tile
     uint32_t sr[kBN];
-    tmem_ld32(tS + lane_off, sr);
-    tmem_ld32(tS + lane_off + 32, sr + 32);
+    tmem_ld32(tSb + lane_off, sr);
+    tmem_ld32(tSb + lane_off + 32, sr + 32);
     tmem_wait_ld();
+    if (tid == 0 && !bad) {
+      s_pend = -1;
+      // PV(kt-1) done: its P (in the other S buffer) and V buffer are free
+      if (kt > 0) {
+        bad |= !mbar_wait(mbO, (kt - 1) & 1, a.wait_limit);
+        if (!bad) o_pend = -1;
+      }
+      if (!bad && kt + 1 < n_kt) {
+        bad |= !mbar_wait(mbK0 + 8 * (b ^ 1), ((kt + 1) >> 1) & 1, a.wait_limit);
+        if (!bad) {
+          k_pend[b ^ 1] = -1;
+          tc_after();
+          issue_s(kt + 1);               // runs during this tile's softmax
+        }
+      }
+      if (!bad && kt + 2 < n_kt) tma_k(kt + 2);          // K buffer b is free
+      if (!bad && kt + 1 < n_kt && kt + 1 >= 2) tma_v(kt + 1);   // V buffer b^1 is free
+    }
+    // softmax of this thread's row
+    const int* de = s_death + b * kBN;
+    const int dmin = min(s_dmin[b * 2], s_dmin[b * 2 + 1]);
+    const bool full = k0 >= w_lo && k0 + kBN <= w_kend && dmin > w_time;   // warp-uniform
     float sv[kBN];
     float mx = -INFINITY;
     if (full) {
@@ -489,24 +516,20 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
     const float alpha = m_new == -INFINITY ? 1.f : ex2(m_r - m_new);
     const float msub = m_new == -INFINITY ? 0.f : m_new;
     float ps = 0.f;
+    uint32_t pk[kBN / 2];
 #pragma unroll
-    for (int c = 0; c < kBN; c += 8) {
-      float p[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        p[e] = ex2(sv[c + e] - msub);
-        ps += p[e];
-      }
-      uint4 w;
-      w.x = pack_bf16x2(p[0], p[1]);
-      w.y = pack_bf16x2(p[2], p[3]);
-      w.z = pack_bf16x2(p[4], p[5]);
-      w.w = pack_bf16x2(p[6], p[7]);
-      *reinterpret_cast<uint4*>(sP + sw128(tid, c / 8, kBM)) = w;
+    for (int c = 0; c < kBN; c += 2) {
+      const float p0 = ex2(sv[c] - msub), p1 = ex2(sv[c + 1] - msub);
+      ps += p0 + p1;
+      pk[c / 2] = pack_bf16x2(p0, p1);
     }
     l_r = fmaf(l_r, alpha, ps);
     m_r = m_new;
+    tmem_st32(tSb + lane_off, pk);     // P(kt) over S(kt): A operand of PV(kt)
     if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // O is stable once PV(kt-1) is done
+      bad |= !mbar_wait(mbO, (kt - 1) & 1, a.wait_limit);
+      tc_after();
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
@@ -516,39 +539,48 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
         tmem_st32(tO + lane_off + c, o);
       }
-      tmem_wait_st();
     }
-    proxy_fence();
+    tmem_wait_st();
     tc_before();
-    ok = __syncthreads_and(mbar_wait(mbv, ph_v, a.wait_limit));    // V(kt); P written
+    bad = __syncthreads_or(bad);
+    if (bad) break;
     tc_after();
-    if (!ok) break;
-    ph_v ^= 1;
-    --v_out;
-    // O += P V
+    load_deaths(kt + 2);               // buffer b: every row has read this tile's deaths
+    // O += P(kt) V(kt)
     if (tid == 0) {
+      bad = !mbar_wait(mbV0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
+      if (!bad) {
+        v_pend[b] = -1;
+        tc_after();
+        const uint32_t vb = smem_u32(sV + b * kBN * D * 2);
 #pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        const uint32_t pa = smem_u32(sP) + kk * 32;
-        const uint32_t va = smem_u32(sV) + kk * 16 * 128;
-        umma(tO, sdesc(pa, 16, 1024), sdesc(va, kBN * 128, 1024), id_o, kt > 0 || kk > 0);
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(tO, tSb + kk * 8, sdesc(vb + kk * 16 * 128, kBN * 128, 1024), id_o, kt > 0 || kk > 0);
+        umma_commit(mbO);
+        o_pend = kt;
       }
-      umma_commit(mb);
     }
-    ok = __syncthreads_and(mbar_wait(mb, ph, a.wait_limit));
-    ph ^= 1;
-    tc_after();
-    load_v(kt + 1);             // V buffer is free
   }
-  if (!ok) {
-    if (tid == 0) atomicOr(a.err, AKV_DERR_WAIT);
-    // let the (at most one each) copies still in flight land before the
-    // CTA's shared memory goes; bounded
-    if (k_out > 0) mbar_wait(mbk, ph_k, a.wait_limit);
-    if (v_out > 0) mbar_wait(mbv, ph_v, a.wait_limit);
+  // the last PV
+  if (!bad && n_kt > 0) {
+    bad |= !mbar_wait(mbO, (n_kt - 1) & 1, a.wait_limit);
+    if (tid == 0 && !bad) o_pend = -1;
   }
-  // epilogue: O / l of this thread's row
-  if (ok && n_kt > 0) {
+  tc_after();
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (tid == 0) {
+      atomicOr(a.err, AKV_DERR_WAIT);
+      // let work still in flight finish before the CTA's memory goes (bounded)
+      for (int b = 0; b < 2; ++b) {
+        if (k_pend[b] >= 0) mbar_wait(mbK0 + 8 * b, (k_pend[b] >> 1) & 1, a.wait_limit);
+        if (v_pend[b] >= 0) mbar_wait(mbV0 + 8 * b, (v_pend[b] >> 1) & 1, a.wait_limit);
+      }
+      if (s_pend >= 0) mbar_wait(mbS0 + 8 * (s_pend & 1), (s_pend >> 1) & 1, a.wait_limit);
+      if (o_pend >= 0) mbar_wait(mbO, o_pend & 1, a.wait_limit);
+    }
+  } else if (n_kt > 0) {
+    // epilogue: O / l of this thread's row
     const int hq = kvh * G + blockIdx.z * NH + tid % NH;
     float* po = a.out + ((int64_t)t_r * a.g.hq + hq) * D;
     const float inv = l_r > 0.f ? 1.f / l_r : 0.f;
