@@ -257,6 +257,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             int z, uint32_t bar) {
   asm volatile(
@@ -303,6 +306,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
                  "r"(r[30]), "r"(r[31])
                : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+               "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                 "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),
+                 "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -313,11 +324,19 @@ static_assert(2 * kBN + 128 <= 256, "S buffers and O must fit the TMEM allocatio
 template <int D>
 constexpr size_t restore_tc_smem() {
   return 1024 /* alignment slack */ + (size_t)kBM * D * 2 + 4 * (size_t)kBN * D * 2 +
-         2 * kBN * sizeof(int) + 4 * sizeof(int) + 7 * sizeof(uint64_t) + 16;
+         2 * kBN * sizeof(int) + 6 * kBM * sizeof(float) + 4 * sizeof(int) +
+         19 * sizeof(uint64_t) + 16;
 }
 
+// softmax warps: warp w reads TMEM lanes 32 (w % 4) .. (its rows) and the
+// key half w / 4 of every S tile (and of O's columns); rows are shared by
+// warps w and w + 4, which combine their row maxima through shared memory
+constexpr int kSoftmaxWarps = 8;
+constexpr int kRestoreThreads = 32 * (kSoftmaxWarps + 1);   // + one control warp
+constexpr int kHalf = kBN / 2;                              // keys per softmax warp and tile
+
 template <int D, int NH>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kRestoreThreads, 2)
 k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
   constexpr int NCOL = restore_tc_cols<D>();
   constexpr uint32_t KV_BYTES = kBN * D * 2;     // one tile of K (or V)
@@ -327,20 +346,25 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
   uint8_t* sK = sQ + kBM * D * 2;             // [2] kBN x D, TMA 64-element atoms
   uint8_t* sV = sK + 2 * kBN * D * 2;         // [2] same layout, read MN-major
   int* s_death = reinterpret_cast<int*>(sV + 2 * kBN * D * 2);   // [2][kBN]
-  int* s_dmin = s_death + 2 * kBN;                                // [2][2] per-warp minima
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(s_dmin + 4);       // S[2], O, K[2], V[2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 7);
+  // row maxima of the two halves per tile parity, then the two row sums
+  float* s_mx = reinterpret_cast<float*>(s_death + 2 * kBN);     // [3][2 halves][kBM]
+  int* s_dmin = reinterpret_cast<int*>(s_mx + 6 * kBM);           // [2]
+  volatile int* s_abort = s_dmin + 2;
+  // S[2] O K[2] V[2] P[2] D[2], then X[4 quarters][2]: row-max exchange of a pair
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(s_dmin + 4);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 19);
 
   const RestoreTile tl = a.tiles[blockIdx.x];
   const int kvh = blockIdx.y;
   const int G = a.g.hq / a.g.hkv;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool control = warp == kSoftmaxWarps;
   const int tend = tl.tok0 + tl.n_tok;
   const int R = a.g.rope, RH = R / 2;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
 
   // rotated, scaled Q rows: row = token * NH + head
-  for (int i = tid; i < kBM * (D / 2); i += 128) {
+  for (int i = tid; i < kBM * (D / 2); i += kRestoreThreads) {
     const int row = i / (D / 2), d = i % (D / 2);
     const int t = tl.tok0 + row / NH;
     const int hq = kvh * G + blockIdx.z * NH + row % NH;
@@ -368,209 +392,165 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
     *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dx / 8, kBM)) + dx % 8) = __float2bfloat16_rn(x);
     *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dy / 8, kBM)) + dy % 8) = __float2bfloat16_rn(y);
   }
-  // this thread's row: key j is visible iff lo_r <= j < kend_r and the key
-  // is still alive at time_r (keys are born in slot order, so "born by
-  // time_r" is j < kend_r); padding rows see nothing
-  int time_r = -1, lo_r = 0, kend_r = 0;
-  const int t_r = tl.tok0 + tid / NH;
-  if (t_r < tend) {
-    const RestoreQuery qq = a.queries[t_r];
-    if (qq.pos >= 0 && qq.pos < a.max_pos) {
-      time_r = qq.time;
-      kend_r = qq.key_end;
-      lo_r = a.window > 0 ? max(0, qq.pos - a.window + 1) : 0;
-    }
-  }
-  // warp bounds for the unmasked fast path (padding rows do not constrain)
-  const bool real = t_r < tend;
-  const int w_kend = __reduce_min_sync(0xffffffffu, real ? kend_r : INT32_MAX);
-  const int w_lo = __reduce_max_sync(0xffffffffu, real ? lo_r : INT32_MIN);
-  const int w_time = __reduce_max_sync(0xffffffffu, real ? time_r : INT32_MIN);
-
   const uint32_t mbS0 = smem_u32(mbar), mbO = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 3),
-                 mbV0 = smem_u32(mbar + 5);
-  if (tid == 0) {
-    for (int i = 0; i < 7; ++i)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar + i)) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0) {
+                 mbV0 = smem_u32(mbar + 5), mbP0 = smem_u32(mbar + 7), mbD0 = smem_u32(mbar + 9),
+                 mbX0 = smem_u32(mbar + 11);
+  if (control) {
+    if (lane == 0) {
+      for (int i = 0; i < 19; ++i) {
+        // P: one arrival per softmax warp; X: one per warp of the pair
+        const uint32_t cnt = (i == 7 || i == 8) ? kSoftmaxWarps : (i >= 11 ? 2 : 1);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar + i)), "r"(cnt) : "memory");
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      *s_abort = 0;
+    }
+    __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(tslot)), "r"(NCOL) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  const int n_kt = (tl.key_hi - tl.key_lo + kBN - 1) / kBN;
-  // deaths of tile kt (and per-warp minima) into buffer kt & 1
-  auto load_deaths = [&](int kt) {
-    if (kt >= n_kt || tid >= kBN) return;
-    const int j = tl.key_lo + kt * kBN + tid;
-    const int dd = j < tl.key_hi ? a.keys[tl.era_off + j].death : 0;
-    s_death[(kt & 1) * kBN + tid] = dd;
-    const int wm = __reduce_min_sync(0xffffffffu, dd);
-    if ((tid & 31) == 0) s_dmin[(kt & 1) * 2 + (tid >> 5)] = wm;
-  };
-  load_deaths(0);
-  load_deaths(1);
   proxy_fence();
   tc_before();
   __syncthreads();
   tc_after();
   const uint32_t tbase = *tslot;
   const uint32_t tO = tbase + 2 * kBN;                          // S buffers at 0 and kBN
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  const uint32_t id_s = idesc_bf16(kBM, kBN, 0), id_o = idesc_bf16(kBM, D, 1);
+  const int n_kt = (tl.key_hi - tl.key_lo + kBN - 1) / kBN;
+  auto fail = [&]() {
+    *s_abort = 1;
+    atomicOr(a.err, AKV_DERR_WAIT);
+  };
 
-  // thread 0 owns the TMA copies and the MMAs; pending work for the drain
-  int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1}, s_pend = -1, o_pend = -1;
-  auto tma_k = [&](int kt) {
-    const int b = kt & 1;
-    mbar_expect_tx(mbK0 + 8 * b, KV_BYTES);
-#pragma unroll
-    for (int at = 0; at < D / 64; ++at)
-      tma_load_3d(smem_u32(sK + b * kBN * D * 2 + at * kBN * 128), &a.tm_k, at * 64, kvh,
-                  tl.era_off + tl.key_lo + kt * kBN, mbK0 + 8 * b);
-    k_pend[b] = kt;
-  };
-  auto tma_v = [&](int kt) {
-    const int b = kt & 1;
-    mbar_expect_tx(mbV0 + 8 * b, KV_BYTES);
-#pragma unroll
-    for (int at = 0; at < D / 64; ++at)
-      tma_load_3d(smem_u32(sV + b * kBN * D * 2 + at * kBN * 128), &a.tm_v, at * 64, kvh,
-                  tl.era_off + tl.key_lo + kt * kBN, mbV0 + 8 * b);
-    v_pend[b] = kt;
-  };
-  auto issue_s = [&](int kt) {        // S(kt) = Q K(kt)^T into S buffer kt & 1
-    const int b = kt & 1;
-    const uint32_t kb = smem_u32(sK + b * kBN * D * 2);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t qa = smem_u32(sQ) + (kk >> 2) * kBM * 128 + (kk & 3) * 32;
-      const uint32_t ka = kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32;
-      umma(tbase + b * kBN, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), id_s, kk > 0);
-    }
-    umma_commit(mbS0 + 8 * b);
-    s_pend = kt;
-  };
-  bool bad = false;
-  if (tid == 0 && n_kt > 0) {
-    tma_k(0);
-    tma_v(0);
-    if (n_kt > 1) { tma_k(1); tma_v(1); }
-    bad = !mbar_wait(mbK0, 0, a.wait_limit);
-    if (!bad) { k_pend[0] = -1; tc_after(); issue_s(0); }
-  }
   float m_r = -INFINITY, l_r = 0.f;
-  for (int kt = 0; kt < n_kt; ++kt) {
-    const int b = kt & 1;
-    const int k0 = tl.key_lo + kt * kBN;
-    const uint32_t tSb = tbase + b * kBN;
-    // S(kt) done
-    bad |= !mbar_wait(mbS0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
-    tc_after();
-    uint32_t sr[kBN];
-    tmem_ld32(tSb + lane_off, sr);
-    tmem_ld32(tSb + lane_off + 32, sr + 32);
-    tmem_wait_ld();
-    if (tid == 0 && !bad) {
-      s_pend = -1;
-      // PV(kt-1) done: its P (in the other S buffer) and V buffer are free
-      if (kt > 0) {
-        bad |= !mbar_wait(mbO, (kt - 1) & 1, a.wait_limit);
-        if (!bad) o_pend = -1;
+  int t_r = 0;
+  if (control) {
+    // ---- control warp: TMA copies, key deaths, MMAs (lane 0 issues) ----
+    const uint32_t id_s = idesc_bf16(kBM, kBN, 0), id_o = idesc_bf16(kBM, D, 1);
+    int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1}, s_pend = -1, o_pend = -1;
+    auto tma_k = [&](int kt) {
+      const int b = kt & 1;
+      mbar_expect_tx(mbK0 + 8 * b, KV_BYTES);
+#pragma unroll
+      for (int at = 0; at < D / 64; ++at)
+        tma_load_3d(smem_u32(sK + b * kBN * D * 2 + at * kBN * 128), &a.tm_k, at * 64, kvh,
+                    tl.era_off + tl.key_lo + kt * kBN, mbK0 + 8 * b);
+      k_pend[b] = kt;
+    };
+    auto tma_v = [&](int kt) {
+      const int b = kt & 1;
+      mbar_expect_tx(mbV0 + 8 * b, KV_BYTES);
+#pragma unroll
+      for (int at = 0; at < D / 64; ++at)
+        tma_load_3d(smem_u32(sV + b * kBN * D * 2 + at * kBN * 128), &a.tm_v, at * 64, kvh,
+                    tl.era_off + tl.key_lo + kt * kBN, mbV0 + 8 * b);
+      v_pend[b] = kt;
+    };
+    // whole warp: deaths of tile kt (loaded early into registers, stored
+    // once the buffer is free) and their minimum
+    auto fetch_deaths = [&](int kt, int* dd) {
+#pragma unroll
+      for (int h = 0; h < kBN / 32; ++h) {
+        const int j = tl.key_lo + kt * kBN + lane + 32 * h;
+        dd[h] = (kt < n_kt && j < tl.key_hi) ? a.keys[tl.era_off + j].death : 0;
       }
-      if (!bad && kt + 1 < n_kt) {
-        bad |= !mbar_wait(mbK0 + 8 * (b ^ 1), ((kt + 1) >> 1) & 1, a.wait_limit);
-        if (!bad) {
-          k_pend[b ^ 1] = -1;
-          tc_after();
-          issue_s(kt + 1);               // runs during this tile's softmax
+    };
+    auto store_deaths = [&](int kt, const int* dd) {
+      const int b = kt & 1;
+      int mn = INT32_MAX;
+#pragma unroll
+      for (int h = 0; h < kBN / 32; ++h) {
+        s_death[b * kBN + lane + 32 * h] = dd[h];
+        mn = min(mn, dd[h]);
+      }
+      mn = __reduce_min_sync(0xffffffffu, mn);
+      if (lane == 0) s_dmin[b] = mn;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(mbD0 + 8 * b);
+    };
+    auto deaths = [&](int kt) {
+      int dd[kBN / 32];
+      fetch_deaths(kt, dd);
+      store_deaths(kt, dd);
+    };
+    auto issue_s = [&](int kt) {
+      const int b = kt & 1;
+      const uint32_t kb = smem_u32(sK + b * kBN * D * 2);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qa = smem_u32(sQ) + (kk >> 2) * kBM * 128 + (kk & 3) * 32;
+        const uint32_t ka = kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32;
+        umma(tbase + b * kBN, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), id_s, kk > 0);
+      }
+      umma_commit(mbS0 + 8 * b);
+      s_pend = kt;
+    };
+    bool ok = true;
+    if (n_kt > 0) {
+      if (lane == 0) {
+        tma_k(0);
+        tma_v(0);
+        if (n_kt > 1) { tma_k(1); tma_v(1); }
+      }
+      deaths(0);
+      if (n_kt > 1) deaths(1);
+      if (lane == 0) {
+        ok = mbar_wait(mbK0, 0, a.wait_limit);
+        if (ok) { k_pend[0] = -1; tc_after(); issue_s(0); } else fail();
+      }
+    }
+    for (int kt = 0; kt < n_kt; ++kt) {
+      const int b = kt & 1;
+      ok = __shfl_sync(0xffffffffu, ok, 0) && !*s_abort;
+      if (!ok) break;
+      int dnext[kBN / 32];
+      fetch_deaths(kt + 2, dnext);      // in flight while lane 0 waits
+      if (lane == 0) {
+        // S(kt+1) into the other S buffer once PV(kt-1) has read its P
+        if (kt + 1 < n_kt) {
+          if (kt > 0) {
+            ok = mbar_wait(mbO, (kt - 1) & 1, a.wait_limit);
+            if (ok) o_pend = -1;
+          }
+          if (ok) ok = mbar_wait(mbK0 + 8 * (b ^ 1), ((kt + 1) >> 1) & 1, a.wait_limit);
+          if (ok) {
+            k_pend[b ^ 1] = -1;
+            tc_after();
+            issue_s(kt + 1);
+            if (kt + 1 >= 2) tma_v(kt + 1);   // V buffer b^1 was read by PV(kt-1)
+          }
+        }
+        // softmax of tile kt done: S(kt) and the deaths of kt are consumed
+        if (ok) ok = mbar_wait(mbP0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
+        if (ok) {
+          s_pend = s_pend == kt ? -1 : s_pend;
+          if (kt + 2 < n_kt) tma_k(kt + 2);   // K buffer b is free
+        } else {
+          fail();
         }
       }
-      if (!bad && kt + 2 < n_kt) tma_k(kt + 2);          // K buffer b is free
-      if (!bad && kt + 1 < n_kt && kt + 1 >= 2) tma_v(kt + 1);   // V buffer b^1 is free
-    }
-    // softmax of this thread's row
-    const int* de = s_death + b * kBN;
-    const int dmin = min(s_dmin[b * 2], s_dmin[b * 2 + 1]);
-    const bool full = k0 >= w_lo && k0 + kBN <= w_kend && dmin > w_time;   // warp-uniform
-    float sv[kBN];
-    float mx = -INFINITY;
-    if (full) {
+      if (lane == 0 && ok) {
+        // O += P(kt) V(kt)
+        ok = mbar_wait(mbV0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
+        if (ok) {
+          v_pend[b] = -1;
+          tc_after();
+          const uint32_t vb = smem_u32(sV + b * kBN * D * 2);
+          const uint32_t tSb = tbase + b * kBN;
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        sv[c] = __uint_as_float(sr[c]);
-        mx = fmaxf(mx, sv[c]);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(tO, tSb + kk * 8, sdesc(vb + kk * 16 * 128, kBN * 128, 1024), id_o, kt > 0 || kk > 0);
+          umma_commit(mbO);
+          o_pend = kt;
+        } else {
+          fail();
+        }
       }
-    } else {
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        const int j = k0 + c;
-        const bool vis = j >= lo_r && j < kend_r && de[c] > time_r;
-        sv[c] = vis ? __uint_as_float(sr[c]) : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
-      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (kt + 2 < n_kt) store_deaths(kt + 2, dnext);   // buffer b: deaths(kt) consumed
     }
-    // the reference max moves only when the row max grows by more than 2^8
-    const float m_new = (mx > m_r + 8.f) ? mx : m_r;
-    const float alpha = m_new == -INFINITY ? 1.f : ex2(m_r - m_new);
-    const float msub = m_new == -INFINITY ? 0.f : m_new;
-    float ps = 0.f;
-    uint32_t pk[kBN / 2];
-#pragma unroll
-    for (int c = 0; c < kBN; c += 2) {
-      const float p0 = ex2(sv[c] - msub), p1 = ex2(sv[c + 1] - msub);
-      ps += p0 + p1;
-      pk[c / 2] = pack_bf16x2(p0, p1);
-    }
-    l_r = fmaf(l_r, alpha, ps);
-    m_r = m_new;
-    tmem_st32(tSb + lane_off, pk);     // P(kt) over S(kt): A operand of PV(kt)
-    if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-      // O is stable once PV(kt-1) is done
-      bad |= !mbar_wait(mbO, (kt - 1) & 1, a.wait_limit);
-      tc_after();
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + lane_off + c, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-        tmem_st32(tO + lane_off + c, o);
-      }
-    }
-    tmem_wait_st();
-    tc_before();
-    bad = __syncthreads_or(bad);
-    if (bad) break;
-    tc_after();
-    load_deaths(kt + 2);               // buffer b: every row has read this tile's deaths
-    // O += P(kt) V(kt)
-    if (tid == 0) {
-      bad = !mbar_wait(mbV0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
-      if (!bad) {
-        v_pend[b] = -1;
-        tc_after();
-        const uint32_t vb = smem_u32(sV + b * kBN * D * 2);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tO, tSb + kk * 8, sdesc(vb + kk * 16 * 128, kBN * 128, 1024), id_o, kt > 0 || kk > 0);
-        umma_commit(mbO);
-        o_pend = kt;
-      }
-    }
-  }
-  // the last PV
-  if (!bad && n_kt > 0) {
-    bad |= !mbar_wait(mbO, (n_kt - 1) & 1, a.wait_limit);
-    if (tid == 0 && !bad) o_pend = -1;
-  }
-  tc_after();
-  bad = __syncthreads_or(bad);
-  if (bad) {
-    if (tid == 0) {
-      atomicOr(a.err, AKV_DERR_WAIT);
+    if (lane == 0 && *s_abort) {
       // let work still in flight finish before the CTA's memory goes (bounded)
       for (int b = 0; b < 2; ++b) {
         if (k_pend[b] >= 0) mbar_wait(mbK0 + 8 * b, (k_pend[b] >> 1) & 1, a.wait_limit);
@@ -579,15 +559,134 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
       if (s_pend >= 0) mbar_wait(mbS0 + 8 * (s_pend & 1), (s_pend >> 1) & 1, a.wait_limit);
       if (o_pend >= 0) mbar_wait(mbO, o_pend & 1, a.wait_limit);
     }
-  } else if (n_kt > 0) {
-    // epilogue: O / l of this thread's row
-    const int hq = kvh * G + blockIdx.z * NH + tid % NH;
-    float* po = a.out + ((int64_t)t_r * a.g.hq + hq) * D;
-    const float inv = l_r > 0.f ? 1.f / l_r : 0.f;
+  } else {
+    // ---- softmax warps: row = TMEM lane, keys and O columns split in halves ----
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = 32 * quarter + lane;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    // key j is visible iff lo_r <= j < kend_r and the key is still alive at
+    // time_r (keys are born in slot order: "born by time_r" is j < kend_r);
+    // padding rows see nothing
+    int time_r = -1, lo_r = 0, kend_r = 0;
+    t_r = tl.tok0 + row / NH;
+    if (t_r < tend) {
+      const RestoreQuery qq = a.queries[t_r];
+      if (qq.pos >= 0 && qq.pos < a.max_pos) {
+        time_r = qq.time;
+        kend_r = qq.key_end;
+        lo_r = a.window > 0 ? max(0, qq.pos - a.window + 1) : 0;
+      }
+    }
+    const bool real = t_r < tend;
+    const int w_kend = __reduce_min_sync(0xffffffffu, real ? kend_r : INT32_MAX);
+    const int w_lo = __reduce_max_sync(0xffffffffu, real ? lo_r : INT32_MIN);
+    const int w_time = __reduce_max_sync(0xffffffffu, real ? time_r : INT32_MIN);
+    for (int kt = 0; kt < n_kt; ++kt) {
+      const int b = kt & 1;
+      const int k0 = tl.key_lo + kt * kBN + half * kHalf;
+      const uint32_t tSb = tbase + b * kBN;
+      bool ok = mbar_wait(mbD0 + 8 * b, (kt >> 1) & 1, a.wait_limit) &&
+                mbar_wait(mbS0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
+      ok = __all_sync(0xffffffffu, ok) && !*s_abort;
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_after();
+      uint32_t sr[kHalf];
+      tmem_ld32(tSb + lane_off + half * kHalf, sr);
+      tmem_wait_ld();
+      const int* de = s_death + b * kBN + half * kHalf;
+      const bool full = k0 >= w_lo && k0 + kHalf <= w_kend && s_dmin[b] > w_time;   // warp-uniform
+      float sv[kHalf];
+      float mx = -INFINITY;
+      if (full) {
 #pragma unroll
-    for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < kHalf; ++c) {
+          sv[c] = __uint_as_float(sr[c]);
+          mx = fmaxf(mx, sv[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c) {
+          const int j = k0 + c;
+          const bool vis = j >= lo_r && j < kend_r && de[c] > time_r;
+          sv[c] = vis ? __uint_as_float(sr[c]) : -INFINITY;
+          mx = fmaxf(mx, sv[c]);
+        }
+      }
+      // row max over both halves (bounded exchange with the partner warp)
+      s_mx[(b * 2 + half) * kBM + row] = mx;
+      __syncwarp();
+      const uint32_t xb = mbX0 + 8 * (quarter * 2 + b);
+      if (lane == 0) mbar_arrive(xb);
+      if (!__all_sync(0xffffffffu, mbar_wait(xb, (kt >> 1) & 1, a.wait_limit))) {
+        if (lane == 0) fail();
+        break;
+      }
+      mx = fmaxf(mx, s_mx[(b * 2 + (half ^ 1)) * kBM + row]);
+      // the reference max moves only when the row max grows by more than 2^8
+      const float m_new = (mx > m_r + 8.f) ? mx : m_r;
+      const float alpha = m_new == -INFINITY ? 1.f : ex2(m_r - m_new);
+      const float msub = m_new == -INFINITY ? 0.f : m_new;
+      float ps = 0.f;
+      uint32_t pk[kHalf / 2];
+#pragma unroll
+      for (int c = 0; c < kHalf; c += 2) {
+        const float p0 = ex2(sv[c] - msub), p1 = ex2(sv[c + 1] - msub);
+        ps += p0 + p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+      }
+      l_r = fmaf(l_r, alpha, ps);     // this half's share of the row sum
+      m_r = m_new;
+      tmem_st16(tSb + lane_off + half * (kHalf / 2), pk);   // P(kt) over S(kt)
+      if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O is stable once PV(kt-1) is done; this half rescales its columns
+        const bool okv = __all_sync(0xffffffffu, mbar_wait(mbO, (kt - 1) & 1, a.wait_limit));
+        if (!okv) {
+          if (lane == 0) fail();
+          break;
+        }
+        tc_after();
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + half * (D / 2) + c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + lane_off + half * (D / 2) + c, o);
+        }
+      }
+      tmem_wait_st();
+      tc_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(mbP0 + 8 * b);
+    }
+    // the last PV
+    if (n_kt > 0 && !*s_abort) {
+      const bool okv = __all_sync(0xffffffffu, mbar_wait(mbO, (n_kt - 1) & 1, a.wait_limit));
+      if (!okv && lane == 0) fail();
+    }
+    // this half's row sum, combined in the epilogue
+    s_mx[(4 + half) * kBM + row] = l_r;
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  if (!control && n_kt > 0 && !*s_abort) {
+    // epilogue: this half's columns of O / l
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = 32 * quarter + lane;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const int hq = kvh * G + blockIdx.z * NH + row % NH;
+    float* po = a.out + ((int64_t)t_r * a.g.hq + hq) * D + half * (D / 2);
+    const float l = s_mx[4 * kBM + row] + s_mx[5 * kBM + row];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 2; c += 32) {
       uint32_t o[32];
-      tmem_ld32(tO + lane_off + c, o);
+      tmem_ld32(tO + lane_off + half * (D / 2) + c, o);
       tmem_wait_ld();
       if (t_r < tend) {
 #pragma unroll
@@ -600,7 +699,7 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
   }
   tc_before();
   __syncthreads();
-  if (warp == 0)
+  if (control)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(NCOL) : "memory");
 }
 
@@ -614,7 +713,7 @@ cudaError_t launch_tc_nh(const RestoreArgs& a, int G, cudaStream_t st) {
     attr = true;
   }
   const dim3 grid(a.n_tiles, a.g.hkv, G / NH);
-  k_restore_attn_tc<D, NH><<<grid, 128, smem, st>>>(a);
+  k_restore_attn_tc<D, NH><<<grid, kRestoreThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
