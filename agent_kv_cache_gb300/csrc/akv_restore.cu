@@ -277,6 +277,23 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  lo = __uint_as_float((uint32_t)v);
+  hi = __uint_as_float((uint32_t)(v >> 32));
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -606,10 +623,9 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
       float mx = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) {
-          sv[c] = __uint_as_float(sr[c]);
-          mx = fmaxf(mx, sv[c]);
-        }
+        for (int c = 0; c < kHalf; ++c) sv[c] = __uint_as_float(sr[c]);
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 2) mx = fmax3(mx, sv[c], sv[c + 1]);
       } else {
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) {
@@ -633,15 +649,21 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
       const float m_new = (mx > m_r + 8.f) ? mx : m_r;
       const float alpha = m_new == -INFINITY ? 1.f : ex2(m_r - m_new);
       const float msub = m_new == -INFINITY ? 0.f : m_new;
-      float ps = 0.f;
+      // pairs of scores in packed f32x2 arithmetic: s - m, then the sums
+      uint64_t ps2 = 0;
+      const uint64_t neg_m = pack_f32x2(-msub, -msub);
       uint32_t pk[kHalf / 2];
 #pragma unroll
       for (int c = 0; c < kHalf; c += 2) {
-        const float p0 = ex2(sv[c] - msub), p1 = ex2(sv[c + 1] - msub);
-        ps += p0 + p1;
+        float d0, d1;
+        unpack_f32x2(add_f32x2(pack_f32x2(sv[c], sv[c + 1]), neg_m), d0, d1);
+        const float p0 = ex2(d0), p1 = ex2(d1);
+        ps2 = add_f32x2(ps2, pack_f32x2(p0, p1));
         pk[c / 2] = pack_bf16x2(p0, p1);
       }
-      l_r = fmaf(l_r, alpha, ps);     // this half's share of the row sum
+      float ps_lo, ps_hi;
+      unpack_f32x2(ps2, ps_lo, ps_hi);
+      l_r = fmaf(l_r, alpha, ps_lo + ps_hi);     // this half's share of the row sum
       m_r = m_new;
       tmem_st16(tSb + lane_off + half * (kHalf / 2), pk);   // P(kt) over S(kt)
       if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
