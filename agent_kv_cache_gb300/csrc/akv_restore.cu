@@ -494,15 +494,19 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
       fetch_deaths(kt, dd);
       store_deaths(kt, dd);
     };
+    // descriptors built once; a k step or a buffer adds a constant to the
+    // start-address field (addresses stay below 256 KB: no carry)
+    const uint64_t dq = sdesc(smem_u32(sQ), 16, 1024);
+    const uint64_t dk = sdesc(smem_u32(sK), 16, 1024);
+    const uint64_t dv = sdesc(smem_u32(sV), kBN * 128, 1024);
     auto issue_s = [&](int kt) {
       const int b = kt & 1;
-      const uint32_t kb = smem_u32(sK + b * kBN * D * 2);
+      const uint64_t kb = dk + (uint64_t)((b * kBN * D * 2) >> 4);
+      const uint32_t ts = tbase + b * kBN;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t qa = smem_u32(sQ) + (kk >> 2) * kBM * 128 + (kk & 3) * 32;
-        const uint32_t ka = kb + (kk >> 2) * kBN * 128 + (kk & 3) * 32;
-        umma(tbase + b * kBN, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), id_s, kk > 0);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma(ts, dq + (uint64_t)((((kk >> 2) * kBM * 128) + (kk & 3) * 32) >> 4),
+             kb + (uint64_t)((((kk >> 2) * kBN * 128) + (kk & 3) * 32) >> 4), id_s, kk > 0);
       umma_commit(mbS0 + 8 * b);
       s_pend = kt;
     };
@@ -556,11 +560,11 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
         if (ok) {
           v_pend[b] = -1;
           tc_after();
-          const uint32_t vb = smem_u32(sV + b * kBN * D * 2);
+          const uint64_t vb = dv + (uint64_t)((b * kBN * D * 2) >> 4);
           const uint32_t tSb = tbase + b * kBN;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(tO, tSb + kk * 8, sdesc(vb + kk * 16 * 128, kBN * 128, 1024), id_o, kt > 0 || kk > 0);
+            umma_ts(tO, tSb + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), id_o, kt > 0 || kk > 0);
           umma_commit(mbO);
           o_pend = kt;
         } else {
