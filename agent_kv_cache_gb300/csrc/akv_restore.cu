@@ -182,19 +182,21 @@ cudaError_t launch_simple_g(const RestoreArgs& a, int G, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // Tensor-core path (bf16, D in {64, 128}): tcgen05 UMMA with accumulators in
 // tensor memory.  One CTA = 128 query rows (TT tokens x NH heads of one KV
-// group, NH = min(G, 8)) and 128 threads, thread r owning row r (TMEM lane
-// r).  Per 64-key tile:
-//   S = Q K^T      M=128, N=64, K=D    -> TMEM columns [0, 64)
+// group, NH = min(G, 8)); TMEM lane r holds row r.  Per 64-key tile:
+//   S = Q K^T      M=128, N=64, K=D    -> one of two S buffers in TMEM
 //   softmax        tcgen05.ld of the S row, interval mask, online max/sum,
-//                  P (bf16) to shared memory, O rescaled in TMEM if needed
-//   O += P V       M=128, N=D,  K=64   -> TMEM columns [64, 64+D)
-// Operands live in shared memory in the 128-byte swizzled layout (rows of
+//                  P (bf16 pairs) written back over S with tcgen05.st, O
+//                  rescaled in TMEM when the reference max moves
+//   O += P V       M=128, N=D,  K=64, A = P from TMEM -> TMEM after the S
+//                  buffers
+// Q, K and V live in shared memory in the 128-byte swizzled layout (rows of
 // 128 bytes, 16-byte chunk c of row r at c ^ (r % 8), 64-element atoms of
-// rows*128 bytes); Q, K and P are K-major, V (the same bytes as K's layout)
-// is read MN-major.  One thread issues the MMAs and commits them to an
-// mbarrier that the CTA waits on (bounded).  Two CTAs share an SM (about
-// 82 KB of shared memory and 256 TMEM columns each for D = 128), so one
-// CTA's softmax overlaps the other's MMAs.
+// rows*128 bytes): Q and K K-major, V (the same bytes as K's layout) read
+// MN-major.  A control warp issues the TMA copies and the MMAs (one thread)
+// and loads the keys' death times; eight softmax warps, two per TMEM lane
+// quarter, split each tile's keys and O's columns in halves.  Hand-offs are
+// bounded mbarrier waits.  Two CTAs share an SM (about 103 KB of shared
+// memory and 256 TMEM columns each for D = 128).
 // ---------------------------------------------------------------------------
 
 constexpr int kBM = 128;   // query rows per CTA
@@ -203,14 +205,6 @@ constexpr int kBN = 64;    // keys per tile
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 // byte offset of (row, 16-byte chunk) in an operand of `rows` rows
 __device__ __forceinline__ uint32_t sw128(int row, int chunk, int rows) {
   return (uint32_t)((chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));

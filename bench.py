@@ -540,7 +540,8 @@ def restore_arm(args):
                                f"{sum(op[0] == 'repos' for op in prog)} repositions, "
                                f"{sum(op[0] == 'drop' for op in prog)} drop operations; one step "
                                f"= restore attention on all {sh.layers} layers",
-                   "kernel": "CUDA cores" if args.restore_cuda_cores else "tensor cores (mma.sync)",
+                   "kernel": "CUDA cores" if args.restore_cuda_cores
+                   else "tensor cores (tcgen05, accumulators in tensor memory)",
                    "flops_per_layer": flops, "tokens": n},
         "roofline": {"kernel": "restore attention (temporary key versions + attention)",
                      "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
