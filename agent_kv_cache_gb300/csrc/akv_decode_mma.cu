@@ -256,8 +256,10 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
       }
       // this block's copies must have landed before the ring is reused or
       // the block exits (immediate unless a consumer gave up early)
+      // (a fixed, generous limit: copies in flight land in microseconds, and
+      // a small user limit must not let the block exit before they do)
       for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-        if (!mbar_wait(smem_u32(&s_full[i % kStages]), (i / kStages) & 1, a.wait_limit))
+        if (!mbar_wait(smem_u32(&s_full[i % kStages]), (i / kStages) & 1, kDrainPolls))
           atomicOr(a.err, AKV_DERR_WAIT);
     }
   } else {

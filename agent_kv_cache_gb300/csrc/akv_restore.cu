@@ -570,13 +570,14 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
       if (kt + 2 < n_kt) store_deaths(kt + 2, dnext);   // buffer b: deaths(kt) consumed
     }
     if (lane == 0 && *s_abort) {
-      // let work still in flight finish before the CTA's memory goes (bounded)
+      // let work still in flight finish before the CTA's memory goes
+      // (bounded by a fixed limit, independent of the user's wait limit)
       for (int b = 0; b < 2; ++b) {
-        if (k_pend[b] >= 0) mbar_wait(mbK0 + 8 * b, (k_pend[b] >> 1) & 1, a.wait_limit);
-        if (v_pend[b] >= 0) mbar_wait(mbV0 + 8 * b, (v_pend[b] >> 1) & 1, a.wait_limit);
+        if (k_pend[b] >= 0) mbar_wait(mbK0 + 8 * b, (k_pend[b] >> 1) & 1, kDrainPolls);
+        if (v_pend[b] >= 0) mbar_wait(mbV0 + 8 * b, (v_pend[b] >> 1) & 1, kDrainPolls);
       }
-      if (s_pend >= 0) mbar_wait(mbS0 + 8 * (s_pend & 1), (s_pend >> 1) & 1, a.wait_limit);
-      if (o_pend >= 0) mbar_wait(mbO, o_pend & 1, a.wait_limit);
+      if (s_pend >= 0) mbar_wait(mbS0 + 8 * (s_pend & 1), (s_pend >> 1) & 1, kDrainPolls);
+      if (o_pend >= 0) mbar_wait(mbO, o_pend & 1, kDrainPolls);
     }
   } else {
     // ---- softmax warps: row = TMEM lane, keys and O columns split in halves ----

@@ -502,3 +502,34 @@ def test_errors_leave_state_unchanged():
     t.check(s)
     t.free(s)
     assert t.gpu.pool_stats() == (16, 0)
+
+
+def test_bounded_waits_time_out_and_recover():
+    """A one-poll wait limit makes the tcgen05 restore kernel's mbarrier
+    waits run out: it drains its own copies and MMAs, reports AKV_DERR_WAIT
+    in the error word and returns (no hang, no fault). The tensor-core
+    decode under the same limit either completes or reports the same bit
+    (one poll may already see its data land), never anything else. With the
+    limit restored both calls match the oracle again."""
+    t = Twin(layers=1, hq=8, hkv=2, head_dim=128, page_size=16, dtype="bf16", max_pages=2048,
+             max_seqs=8, max_slots=4096, seed=3)
+    seqs = [t.create() for _ in range(4)]
+    t.append(seqs, [3000] * 4)
+    prog = [("append", 120), ("drop", [(10, 40)]), ("repos",), ("append", 30)]
+    n = 150
+    q = torch.zeros((n, 8, 128), dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros((n, 2, 128), dtype=torch.bfloat16, device="cuda")
+    qd = torch.zeros((4, 8, 128), dtype=torch.bfloat16, device="cuda")
+    abi.akv_set_wait_limit(t.gpu.handle, 1)
+    t.gpu.decode_attention(0, qd, seqs)
+    w_dec = t.gpu.sync_errors()
+    t.gpu.restore_attention(prog, 0, q, kv, kv)
+    w_res = t.gpu.sync_errors()
+    abi.akv_set_wait_limit(t.gpu.handle, 1 << 22)
+    assert w_res == abi.AKV_DERR_WAIT, w_res
+    assert w_dec in (0, abi.AKV_DERR_WAIT), w_dec
+    assert t.gpu.sync_errors() == 0
+    t.decode(seqs, step=0)
+    t.restore(prog)
+    for g in seqs:
+        t.check(g)
