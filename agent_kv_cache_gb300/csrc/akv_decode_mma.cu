@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   __shared__ uint16_t s_bits[kMaxTiles];        // keep bits of each tile's 16 slots
   __shared__ int s_last;
 
+  // the next decode call may be scheduled now: its blocks start as this
+  // grid's blocks retire and wait (griddepcontrol.wait) before writing
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const DecodeItem it = a.items[blockIdx.x];
   const int kvh = blockIdx.y;
   const Geom& g = a.g;
@@ -375,6 +378,11 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   }
   __syncthreads();
 
+  // The previous decode call (launched before this one may start, see the
+  // launcher) writes the same kind of partials, counters and outputs; this
+  // block's first global write waits until that grid has finished.  Nothing
+  // above reads memory a decode call writes.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // merge the consumer warps: the output (one split) or this split's partial
   for (int i = tid; i < G * D; i += kThreads) {
     const int gq = i / D, d = i % D;
@@ -481,16 +489,33 @@ bool make_pool_tensor_maps(const Geom& g, CUtensorMap* tk, CUtensorMap* tv) {
   return true;
 }
 
+// Launched with programmatic stream serialisation: when the previous work on
+// the stream is a decode call (which signals launch_dependents at its start),
+// this grid's blocks may start while that grid's last blocks still run, so
+// its start-up (work item, tile list, query) hides behind the other's tail.
+// A decode call reads nothing a decode call writes before its
+// griddepcontrol.wait; any other predecessor (append, drop, reposition, a
+// copy, the caller's kernels) never signals early, so for it the ordering is
+// the plain stream order.
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
   const dim3 grid(a.n_items, a.g.hkv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (a.g.d == 64) {
     set_smem_attr<64>();
-    k_decode_mma<64><<<grid, kThreads, mma_smem<64>(), st>>>(a);
-  } else {
-    set_smem_attr<128>();
-    k_decode_mma<128><<<grid, kThreads, mma_smem<128>(), st>>>(a);
+    cfg.dynamicSmemBytes = mma_smem<64>();
+    return cudaLaunchKernelEx(&cfg, k_decode_mma<64>, a);
   }
-  return cudaGetLastError();
+  set_smem_attr<128>();
+  cfg.dynamicSmemBytes = mma_smem<128>();
+  return cudaLaunchKernelEx(&cfg, k_decode_mma<128>, a);
 }
 
 int decode_mma_blocks_per_sm(int d) {

@@ -313,12 +313,14 @@ class Bench:
                 self.knew[t].copy_(host["k"][t], non_blocking=True)
                 self.vnew[t].copy_(host["v"][t], non_blocking=True)
             c.append(forks, [1] * BATCH, self.knew[t], self.vnew[t])
+            # one event pair around the step's L decode calls: an event between
+            # two decode calls would end the overlap of their launches
+            if ev is not None:
+                ev["dec"][t][0].record(self.stream)
             for l in range(L):
-                if ev is not None:
-                    ev["dec"][t * L + l][0].record(self.stream)
                 c.decode_attention(l, self.q[t, l], forks, self.out[l])
-                if ev is not None:
-                    ev["dec"][t * L + l][1].record(self.stream)
+            if ev is not None:
+                ev["dec"][t][1].record(self.stream)
             if host is not None:
                 host["out"][t].copy_(self.out[L - 1], non_blocking=True)
         for f in forks:
@@ -326,9 +328,9 @@ class Bench:
 
     def events(self):
         E = self.torch.cuda.Event
-        n = DECODE_STEPS * SHAPE.layers
         return {"repos": (E(enable_timing=True), E(enable_timing=True)),
-                "dec": [(E(enable_timing=True), E(enable_timing=True)) for _ in range(n)]}
+                "dec": [(E(enable_timing=True), E(enable_timing=True))
+                        for _ in range(DECODE_STEPS)]}
 
 
 def gpu_arm(args):
@@ -375,7 +377,9 @@ def gpu_arm(args):
     assert b.cache.sync_errors() == 0
 
     by = b.bytes
-    dec_ms = [s.elapsed_time(e) for ev in evs for s, e in ev["dec"]]
+    # per decode step: the span of its L back-to-back calls; per call: span / L
+    dec_ms = [s.elapsed_time(e) / SHAPE.layers for ev in evs for s, e in ev["dec"]
+              for _ in range(SHAPE.layers)]
     repos_ms = [ev["repos"][0].elapsed_time(ev["repos"][1]) for ev in evs]
     # calls are ordered step-major, layer-minor: expand the per-step bytes per layer
     per_call = np.repeat(np.array(by["decode_per_call"]), SHAPE.layers)
@@ -431,7 +435,8 @@ def gpu_arm(args):
                        "bytes_per_step": by["total"]},
             "decode_tok_s": round(tok_s, 1),
             "roofline": {"kernel": "k_decode_mma (one launch per decode-attention call, "
-                                   "split merge fused)",
+                                   "split merge fused; per-call time = span of a step's "
+                                   f"{SHAPE.layers} back-to-back calls / {SHAPE.layers})",
                          "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic,
@@ -713,6 +718,208 @@ def prefix_arm(args):
     cache.close()
 
 
+# ---------------------------------------------------------------------------
+# decode and reposition bandwidth on the other workload shapes
+# (--config-kernels gptoss120b,branching,llama70b): one line per workload
+# ---------------------------------------------------------------------------
+
+def _decode_bytes(cache, seqs, sh):
+    """Algorithmic bytes of one decode call: per sequence (every sequence's
+    active K/V), and with pages shared by several sequences counted once."""
+    kvt = 2 * sh.hkv * sh.head_dim * BYTES_EL
+    act = sum(cache.info(s)["n_active"] for s in seqs)
+    pages = sum(cache.info(s)["n_active_pages"] for s in seqs)
+    fixed = len(seqs) * sh.hq * sh.head_dim * (BYTES_EL + 4) + pages * (8 + sh.page_size // 8)
+    uniq = set()
+    for s in seqs:
+        pt, act_pages = cache.page_table(s)
+        uniq.update(int(pt[k]) for k in act_pages)
+    return act * kvt + fixed, len(uniq) * sh.page_size * kvt + fixed
+
+
+def _moved(cache, seq, sh):
+    """Survivors a reposition relocates: those at or after the first full page
+    that holds a dropped slot."""
+    keep = cache.keep_mask(seq)
+    dead = np.flatnonzero(~keep)
+    if dead.size == 0:
+        return 0
+    kept = (int(dead[0]) // sh.page_size) * sh.page_size
+    return int(keep.sum()) - kept
+
+
+def kernels_arm(args):
+    import torch
+    from agent_kv_cache_gb300 import Cache, build
+    from workloads import device as dev
+    build()
+    dev.build()
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = peaks.get("hbm_gbs", 6800.0)
+    st_events = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+    def append(cache, seq, tag, t0, n, sh, seed):
+        L, H, D = sh.layers, sh.hkv, sh.head_dim
+        w = synth.width_for(sh.dtype)
+        for c0 in range(0, n, CHUNK):
+            m = min(CHUNK, n - c0)
+            k = torch.empty((L, m, H, D), dtype=torch.bfloat16, device="cuda")
+            v = torch.empty_like(k)
+            keep = [dev.kv_tokens(k, seed, tag, synth.KIND_K, range(L), t0 + c0, m, H, D, w),
+                    dev.kv_tokens(v, seed, tag, synth.KIND_V, range(L), t0 + c0, m, H, D, w)]
+            torch.cuda.synchronize()
+            cache.append([seq], [m], k, v)
+            torch.cuda.synchronize()
+            del keep
+
+    def measure(name, cache, sh, bases, drops, seed, note, decode_steps=2):
+        """Fork the prepared sequences, drop, time one batched reposition and
+        decode_steps x (append + decode on every layer); repeated args.steps
+        times after args.warmup."""
+        st = cache.stream
+        L, Hq, H, D = sh.layers, sh.hq, sh.hkv, sh.head_dim
+        w = synth.width_for(sh.dtype)
+        B = len(bases)
+        q = torch.empty((L, B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        kn = torch.empty((L, B, H, D), dtype=torch.bfloat16, device="cuda")
+        keep = [dev.queries(q[l], seed, list(range(B)), l, 0, Hq, D, w) for l in range(L)]
+        keep.append(dev.kv_tokens_multi(kn, seed, list(range(B)), synth.KIND_K, range(L),
+                                        [0] * B, 1, H, D, w))
+        out = torch.empty((L, B, Hq, D), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        rep_ms, dec_ms, rep_bytes, dec_bytes, dec_ubytes = [], [], 0, [], []
+        for it in range(args.warmup + args.steps):
+            forks = [cache.seq_fork(b) for b in bases]
+            for f, dr in zip(forks, drops):
+                if dr:
+                    cache.drop(f, dr)
+            moved = sum(_moved(cache, f, sh) for f in forks)
+            e = st_events()
+            e[0].record(st)
+            cache.reposition(forks)
+            e[1].record(st)
+            devs = []
+            for t in range(decode_steps):
+                cache.append(forks, [1] * B, kn, kn)
+                db, dub = _decode_bytes(cache, forks, sh)
+                ev = st_events()          # around the L back-to-back calls
+                ev[0].record(st)
+                for l in range(L):
+                    cache.decode_attention(l, q[l], forks, out[l])
+                ev[1].record(st)
+                devs.append((ev, db, dub))
+            torch.cuda.synchronize()
+            assert cache.sync_errors() == 0
+            if it >= args.warmup:
+                rep_ms.append(e[0].elapsed_time(e[1]))
+                rep_bytes = 2 * L * moved * 2 * H * D * BYTES_EL
+                for ev, db, dub in devs:
+                    dec_ms += [ev[0].elapsed_time(ev[1]) / L] * L
+                    dec_bytes += [db] * L
+                    dec_ubytes += [dub] * L
+            for f in forks:
+                cache.seq_free(f)
+        del keep
+        dgbs = float(np.sum(dec_bytes) / (np.sum(dec_ms) * 1e-3) / 1e9)
+        ugbs = float(np.sum(dec_ubytes) / (np.sum(dec_ms) * 1e-3) / 1e9)
+        rgbs = rep_bytes / (np.mean(rep_ms) * 1e-3) / 1e9 if rep_bytes else 0.0
+        line = {
+            "metric": f"decode attention and reposition HBM GB/s on the {name} workload",
+            "value": round(ugbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic (seeded SplitMix64 K/V/q, seeded trace structure)",
+            "config": {"workload": note, "batch": B, "layers": L, "heads": f"{Hq}/{H}",
+                       "head_dim": D, "decode_steps_timed": decode_steps},
+            "decode": {"avg_call_us": round(float(np.mean(dec_ms)) * 1e3, 2),
+                       "algorithmic_bytes_per_call": int(np.mean(dec_bytes)),
+                       "gbs": round(dgbs, 1), "frac": round(dgbs / peak, 4),
+                       "unique_page_bytes_per_call": int(np.mean(dec_ubytes)),
+                       "gbs_unique_pages": round(ugbs, 1), "frac_unique_pages": round(ugbs / peak, 4)},
+            "reposition": {"ms": round(float(np.mean(rep_ms)), 3), "moved_tokens": moved,
+                           "algorithmic_bytes": rep_bytes, "gbs": round(rgbs, 1),
+                           "frac": round(rgbs / peak, 4)},
+            "peak": peak, "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+        }
+        print(json.dumps(line), flush=True)
+
+    for name in args.config_kernels.split(","):
+        if name == "gptoss120b":
+            sh, seed, B, N = traces.GPTOSS120B, traces.seed_for(2), 4, 131072
+            trajs = traces.gptoss_batch(seed, batch=B, n_total=N)
+            mp = B * (N // 16) + B * (N // 16 // 4) + 512
+            cache = Cache(sh.layers, sh.hq, sh.hkv, sh.head_dim, sh.page_size, sh.dtype, mp,
+                          2 * B + 2, N + 64, sh.rope_theta)
+            bases = [cache.seq_create() for _ in range(B)]
+            for b, s in enumerate(bases):
+                append(cache, s, b + 1, 0, N, sh, seed)
+            measure(name, cache, sh, bases, [t.drop_ranges for t in trajs], seed,
+                    f"{sh.name}-shaped: {B} x {N} tokens, ~80% dropped, 1 reposition")
+        elif name == "branching":
+            # 32 of the workload's 64 branches: each fork's reposition takes
+            # fresh 2 MB pages, and 64 prepared branches plus 64 timed forks
+            # would not fit the pool next to the other state
+            sh, seed, P, NB = traces.LLAMA8B, traces.seed_for(3), 16384, 32
+            segs, branches = traces.branching(seed, n_branches=64, prefix_len=P)
+            mp = P // 16 + 2 * NB * (P // 16 + 8) + 512
+            cache = Cache(sh.layers, sh.hq, sh.hkv, sh.head_dim, sh.page_size, sh.dtype, mp,
+                          2 * NB + 4, P + 64, sh.rope_theta)
+            root = cache.seq_create()
+            append(cache, root, 1, 0, P, sh, seed)
+            # a branch's prepared state is its operations before its last
+            # reposition; the timed call is that last reposition, batched
+            kids = []
+            for br in branches[:NB]:
+                k = cache.seq_fork(root)
+                last = max(i for i, op in enumerate(br.ops) if op[0] == "repos")
+                for op in br.ops[:last]:
+                    if op[0] == "drop":
+                        cache.drop(k, op[1])
+                    else:
+                        cache.reposition([k])
+                kids.append(k)
+            measure(name, cache, sh, kids, [None] * NB, seed,
+                    f"{sh.name}-shaped: one {P}-token prefix forked into {NB} of the 64 branches "
+                    "(1-6 drop / reposition operations each); every branch's last reposition "
+                    "batched and timed, then batched decode over the branches")
+        elif name == "llama70b":
+            # turns 0..13 as scheduled, then turn 14's tool response; the timed
+            # operation is turn 14's drop of the oldest tool spans + reposition
+            # (every third turn drops once more than 16384 tokens are active)
+            sh, seed, B, TT = traces.LLAMA70B, traces.seed_for(4), 64, 14
+            turns = traces.steady_state(seed, n_seqs=B, n_turns=TT + 1, decode_per_turn=64,
+                                        active_cap=16384)
+            longest = max(1024 + sum(t.tool_len + 64 for t in ts) for ts in turns)
+            mp = B * (-(-longest // 16) + 8) * 2 + 1024
+            cache = Cache(sh.layers, sh.hq, sh.hkv, sh.head_dim, sh.page_size, sh.dtype, mp,
+                          2 * B + 2, longest + 64, sh.rope_theta, phys_layers=16)
+            bases, drops = [], []
+            for b, ts in enumerate(turns):
+                s = cache.seq_create()
+                t0 = 0
+                append(cache, s, b + 1, t0, 1024, sh, seed)
+                t0 += 1024
+                for k, tn in enumerate(ts[:TT]):
+                    append(cache, s, b + 1, t0, tn.tool_len + 64, sh, seed)
+                    t0 += tn.tool_len + 64
+                    if tn.drop_ranges:
+                        cache.drop(s, tn.drop_ranges)
+                    if tn.repos:
+                        cache.reposition([s])
+                append(cache, s, b + 1, t0, ts[TT].tool_len + 64, sh, seed)
+                bases.append(s)
+                drops.append(ts[TT].drop_ranges or None)
+            measure(name, cache, sh, bases, drops, seed,
+                    f"{sh.name}-shaped steady state: {B} sequences at turn {TT + 1} (80 logical "
+                    "layers on 16 slabs): the turn's drop of the oldest tool spans and one "
+                    "batched reposition timed, then decode on all 80 layers")
+        else:
+            raise SystemExit(f"unknown workload {name}")
+        cache.close()
+        del cache
+        torch.cuda.empty_cache()
+
+
 def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -750,6 +957,9 @@ def main():
     ap.add_argument("--restore", action="store_true",
                     help="time segment-batch restore attention instead (its own line)")
     ap.add_argument("--restore-cuda-cores", action="store_true")
+    ap.add_argument("--config-kernels", default=None,
+                    help="comma list of gptoss120b, branching, llama70b: decode and "
+                         "reposition bandwidth on those workloads (one line each)")
     ap.add_argument("--prefix", action="store_true",
                     help="time prefix matching / forks / eviction instead (its own line)")
     # smaller cases for profiler captures only; a line printed with any of
@@ -766,7 +976,9 @@ def main():
         args.profiling_case = True
     else:
         args.profiling_case = False
-    if args.prefix:
+    if args.config_kernels:
+        kernels_arm(args)
+    elif args.prefix:
         prefix_arm(args)
     elif args.restore or args.restore_cuda_cores:
         restore_arm(args)
