@@ -880,14 +880,19 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       }
     };
     if (c->use_mma) {
-      // Tensor-core path: as many blocks as fit the GPU in whole waves, the
-      // splits of each sequence proportional to its pages to read and equal
-      // within it; one split holds at most kDecodeMaxTiles tiles.
+      // Tensor-core path: blocks for a quarter of what fits the GPU at once
+      // (times decode_waves), the splits of each sequence proportional to its
+      // pages to read and equal within it; one split holds at most
+      // kDecodeMaxTiles tiles.  Leaving most block slots free lets the next
+      // decode call's blocks start while this call runs (programmatic
+      // dependent launch): back to back, a quarter wave beat a whole wave by
+      // 2-45% depending on the batch.
       const int64_t tpp = c->cfg.page_size / 16;
       const int64_t resident = (int64_t)c->sm_count * c->mma_blocks_per_sm;
+      const int64_t quarter = std::max<int64_t>(1, resident / 4);
       const int64_t pairs = (int64_t)n_seqs * c->cfg.hkv;
-      const int64_t waves = std::max<int64_t>(c->decode_waves, (pairs + resident - 1) / resident);
-      int64_t target = std::max<int64_t>(n_seqs, waves * resident / c->cfg.hkv);
+      const int64_t waves = std::max<int64_t>(c->decode_waves, (pairs + quarter - 1) / quarter);
+      int64_t target = std::max<int64_t>(n_seqs, waves * quarter / c->cfg.hkv);
       std::vector<int32_t> ns(n_seqs);
       int64_t sum = 0;
       using Entry = std::pair<int64_t, int>;        // (pages per split, seq)

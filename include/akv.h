@@ -302,8 +302,9 @@ const char* akv_last_error(akv_cache* cache);
  * (AKV_DERR_* bits).  Returns AKV_EDEVICE when it was non-zero. */
 int akv_sync_errors(akv_cache* cache, uint32_t* word);
 
-/* Tuning: the tensor-core decode plans its split-KV blocks as `waves`
- * whole waves of the blocks that fit the GPU at once (default 1; 1..64). */
+/* Tuning: the tensor-core decode plans `waves` quarters of the blocks that
+ * fit the GPU at once (default 1: a quarter, which leaves room for the next
+ * call's blocks to start early; 1..64). */
 int akv_set_decode_waves(akv_cache* cache, int32_t waves);
 
 /* Kernel choice for akv_restore_attention: 1 (default) = tensor-core
