@@ -821,7 +821,7 @@ int akv_reposition(akv_cache* c, const int64_t* seqs, int32_t n_seqs) {
                       (int)items.size(), reinterpret_cast<const int32_t*>(d + o_ids), c->d_err,
                       c->stream));
     CK(launch_gather(c->g, c->sa, reinterpret_cast<const ReposItem*>(d + o_items),
-                     (int)items.size(), blocks, c->d_cs, c->d_err, c->stream));
+                     (int)items.size(), blocks, c->d_cs, c->d_err, c->wait_limit, c->stream));
     c->launches += blocks > 0 ? 2 : 1;
   }
   return AKV_OK;

@@ -175,7 +175,7 @@ cudaError_t launch_compact(const Geom& g, const SeqArrays& sa, const ReposItem* 
                            int n_items, const int32_t* ids, uint32_t* err, cudaStream_t st);
 cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* items,
                           int n_items, int n_blocks, const float2* cs, uint32_t* err,
-                          cudaStream_t st);
+                          uint32_t wait_limit, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, bool need_combine, int n_rows,
                           const int32_t* row_item0, const int32_t* row_splits,
                           cudaStream_t st);

@@ -10,6 +10,8 @@
 // Every kernel validates the indices it takes from metadata and, instead of
 // touching memory out of bounds, sets a bit in the device error word and
 // skips the access.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 
 #include "akv.h"
@@ -395,40 +397,68 @@ k_compact(Geom g, SeqArrays sa, const ReposItem* __restrict__ items,
 }
 
 // ---------------------------------------------------------------------------
-// reposition, part 2: gather + delta rotation + store, one block per fresh
-// destination page, all layers and KV heads.  Survivor j moves from old slot
-// src_j to j: K' = R(j - src_j) K (bit copy when j == src_j), V copied.
+// reposition, part 2 (staged): one block per fresh destination page; each
+// (layer, KV head) tile of the page goes through shared memory: bulk copies
+// bring the source rows in (one copy per run of consecutive source slots in
+// one source page), the block rotates the keys in place, and one bulk copy
+// per tensor writes the page tile out.  A ring of stages keeps several
+// tiles' copies in flight per block.  Survivor j moves from old slot src_j
+// to j: K' = R(j - src_j) K (bit copy when j == src_j), V copied.
 // ---------------------------------------------------------------------------
 
+__device__ __forceinline__ uint32_t sm32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 "selp.u32 %0, 1, 0, p;\n}\n" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+constexpr int kGatherThreads = 128;
+
 template <typename T>
-__global__ void __launch_bounds__(256, 4)
+__global__ void __launch_bounds__(kGatherThreads)
 k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
-         const float2* __restrict__ cs, uint32_t* err) {
-  extern __shared__ float2 s_cs[];   // [S][R/2] (unit-minor), angle -(src - j) f
-  __shared__ int s_src_page[64];
-  __shared__ int s_src_off[64];
-  __shared__ int s_copy[64];
-  __shared__ int s_dst_page;
+         const float2* __restrict__ cs, uint32_t* err, int n_stages, uint32_t wait_limit) {
+  constexpr int E = Vec<T>::E;
+  extern __shared__ __align__(128) unsigned char gsm[];
+  const int S = g.s, D = g.d, R = g.rope, RH = R / 2;
+  const uint32_t row_bytes = D * sizeof(T);
+  const uint32_t tile_bytes = S * row_bytes;                 // one (layer, head) tile of one tensor
+  unsigned char* stage0 = gsm;                                // [n_stages][K, V][S][D]
+  float2* s_cs = reinterpret_cast<float2*>(gsm + (size_t)n_stages * 2 * tile_bytes);   // [S][R/2]
+  __shared__ int s_src_page[64], s_src_off[64], s_rot[64];
+  __shared__ int s_run_t0[64], s_run_len[64], s_n_runs, s_dst_page;
+  __shared__ uint32_t s_bytes;
+  __shared__ __align__(8) uint64_t s_full[8];
+
   int lo = 0, hi = n_items - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (items[mid].block0 <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
   }
   const ReposItem it = items[lo];
-  const int S = g.s, D = g.d, R = g.rope, RH = R / 2;
   const int k = it.n_kept + ((int)blockIdx.x - it.block0);
   const int j0 = k * S;
   const int nj = min(S, it.r - j0);
   const int32_t* gather = sa.gather + (int64_t)it.dslot * sa.max_slots;
   const int32_t* oldp = sa.old_pages + (int64_t)it.dslot * sa.seq_pages;
-  const int tid = threadIdx.x, bs = blockDim.x;
+  const int tid = threadIdx.x;
 
-  if (tid == 0) {
-    int p = (k >= 0 && k < sa.seq_pages) ? sa.pages[(int64_t)it.dslot * sa.seq_pages + k] : -1;
-    if (p < 0 || p >= g.max_pages) { flag(err, AKV_DERR_PAGE); p = -1; }
-    s_dst_page = p;
-  }
-  for (int t = tid; t < nj; t += bs) {
+  for (int t = tid; t < nj; t += kGatherThreads) {
     const int j = j0 + t;
     const int src = gather[j];
     int sp = -1;
@@ -436,85 +466,120 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
     if (sp < 0 || sp >= g.max_pages) { flag(err, AKV_DERR_PAGE); sp = -1; }
     s_src_page[t] = sp;
     s_src_off[t] = src % S;
-    s_copy[t] = (src == j);
+    s_rot[t] = src != j;
   }
   {
-    constexpr int E = Vec<T>::E;
     const int kr = RH / E;
-    for (int i = tid; i < nj * RH; i += bs) {
-      const int t = i / RH, j = i % RH;               // pair j = c*E + e of row t
+    for (int i = tid; i < nj * RH; i += kGatherThreads) {
+      const int t = i / RH, jj = i % RH;
       const int delta = gather[j0 + t] - (j0 + t);
       float2 c = make_float2(1.f, 0.f);
-      if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * RH + j];
-      s_cs[t * RH + (j % E) * kr + j / E] = make_float2(c.x, -c.y);
+      if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * RH + jj];
+      s_cs[t * RH + (jj % E) * kr + jj / E] = make_float2(c.x, -c.y);
     }
+  }
+  if (tid == 0) {
+    int p = (k >= 0 && k < sa.seq_pages) ? sa.pages[(int64_t)it.dslot * sa.seq_pages + k] : -1;
+    if (p < 0 || p >= g.max_pages) { flag(err, AKV_DERR_PAGE); p = -1; }
+    s_dst_page = p;
+    for (int s = 0; s < n_stages; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm32(&s_full[s])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // runs of rows whose source slots are consecutive in one source page
+    int nr = 0;
+    uint32_t bytes = 0;
+    for (int t = 0; t < nj; ++t) {
+      if (s_src_page[t] < 0) continue;
+      if (nr > 0 && s_run_t0[nr - 1] + s_run_len[nr - 1] == t &&
+          s_src_page[t] == s_src_page[t - 1] && s_src_off[t] == s_src_off[t - 1] + 1) {
+        ++s_run_len[nr - 1];
+      } else {
+        s_run_t0[nr] = t;
+        s_run_len[nr] = 1;
+        ++nr;
+      }
+      bytes += 2 * row_bytes;
+    }
+    s_n_runs = nr;
+    s_bytes = bytes;
   }
   __syncthreads();
   const int dpage = s_dst_page;
   if (dpage < 0) return;
-
-  constexpr int E = Vec<T>::E;
-  const int kr = RH / E, kc = (D - R) / E, vu = D / E, per_row = kr + kc + vu;
-  const int units = g.hkv * nj * per_row;
+  const int n_runs = s_n_runs;
+  const uint32_t bytes = s_bytes;
+  const int n = g.layers * g.hkv;                // tiles: (logical layer, KV head)
   T* kp = static_cast<T*>(g.k);
   T* vp = static_cast<T*>(g.v);
-  for (int u = tid; u < units; u += bs) {
-    const int r = u % per_row;
-    const int t = (u / per_row) % nj;
-    const int h = u / (per_row * nj);
-    const int sp = s_src_page[t];
-    if (sp < 0) continue;
-    const int64_t src_off = (int64_t)sp * g.page_stride + (int64_t)h * g.head_stride +
-                            (int64_t)s_src_off[t] * D;
-    const int64_t dst_off = (int64_t)dpage * g.page_stride + (int64_t)h * g.head_stride +
-                            (int64_t)t * D;
-    const bool cp = s_copy[t];
-    // Source and destination both live in the pool, so the compiler cannot
-    // move a later layer's loads above an earlier layer's stores: batch the
-    // loads of several layers explicitly to keep enough bytes in flight.
-    if (r < kr) {
-      constexpr int B = 2;
-      for (int l0 = 0; l0 < g.layers; l0 += B) {
-        uint4 lo[B], hi[B];
-#pragma unroll
-        for (int j = 0; j < B; ++j) {
-          if (l0 + j < g.layers) {
-            const T* src = kp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + src_off;
-            lo[j] = ld16(src + r * E);
-            hi[j] = ld16(src + RH + r * E);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < B; ++j) {
-          if (l0 + j >= g.layers) break;
-          T* dst = kp + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + dst_off;
-          if (cp) {
-            st16(dst + r * E, lo[j]);
-            st16(dst + RH + r * E, hi[j]);
-          } else {
-            rotate_regs<T>(lo[j], hi[j], dst, r, RH, s_cs + t * RH, kr);
-          }
-        }
-      }
-    } else {
-      // a chunk copied as it is: K past the rotary dims, or V
-      constexpr int B = 4;
-      T* base = r < kr + kc ? kp : vp;
-      const int o = r < kr + kc ? R + (r - kr) * E : (r - kr - kc) * E;
-      for (int l0 = 0; l0 < g.layers; l0 += B) {
-        uint4 x[B];
-#pragma unroll
-        for (int j = 0; j < B; ++j)
-          if (l0 + j < g.layers)
-            x[j] = ld16(base + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + src_off + o);
-#pragma unroll
-        for (int j = 0; j < B; ++j) {
-          if (l0 + j >= g.layers) break;
-          st16(base + (int64_t)((l0 + j) % g.phys_layers) * g.layer_stride + dst_off + o, x[j]);
-        }
-      }
+
+  auto issue = [&](int i) {                      // thread 0: loads of tile i into its stage
+    const int s = i % n_stages;
+    const int l = i / g.hkv, h = i % g.hkv;
+    const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
+    const uint32_t bar = sm32(&s_full[s]);
+    const uint32_t kd = sm32(stage0 + (size_t)s * 2 * tile_bytes), vd = kd + tile_bytes;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    for (int r = 0; r < n_runs; ++r) {
+      const int t0 = s_run_t0[r];
+      const int64_t off = slab + (int64_t)s_src_page[t0] * g.page_stride + (int64_t)h * g.head_stride +
+                          (int64_t)s_src_off[t0] * D;
+      const uint32_t len = s_run_len[r] * row_bytes;
+      bulk_load(kd + t0 * row_bytes, kp + off, len, bar);
+      bulk_load(vd + t0 * row_bytes, vp + off, len, bar);
+    }
+  };
+  int issued = 0;                                // thread 0: tiles whose loads are issued
+  if (tid == 0)
+    for (; issued < min(n_stages - 1, n); ++issued) issue(issued);
+  bool ok = true;
+  int waited = 0;
+  const int kr = RH / E;
+  for (int i = 0; i < n; ++i) {
+    const int s = i % n_stages;
+    if (tid == 0 && i + n_stages - 1 < n) {
+      // the stage of tile i - 1 is free once its stores have read it
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      issue(i + n_stages - 1);
+      issued = i + n_stages;
+    }
+    ok = __syncthreads_and(gwait(sm32(&s_full[s]), (i / n_stages) & 1, wait_limit));
+    if (!ok) break;
+    waited = i + 1;
+    T* kt = reinterpret_cast<T*>(stage0 + (size_t)s * 2 * tile_bytes);
+    // rotate the moved keys' rotary pairs in place
+    for (int u = tid; u < nj * kr; u += kGatherThreads) {
+      const int t = u / kr, c = u % kr;
+      if (!s_rot[t] || s_src_page[t] < 0) continue;
+      T* row = kt + (size_t)t * D;
+      const uint4 lo = *reinterpret_cast<const uint4*>(row + c * E);
+      const uint4 hi = *reinterpret_cast<const uint4*>(row + RH + c * E);
+      rotate_regs<T>(lo, hi, row, c, RH, s_cs + t * RH, kr);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+      const int l = i / g.hkv, h = i % g.hkv;
+      const int64_t dst = (int64_t)(l % g.phys_layers) * g.layer_stride +
+                          (int64_t)dpage * g.page_stride + (int64_t)h * g.head_stride;
+      const uint32_t src = sm32(stage0 + (size_t)s * 2 * tile_bytes);
+      bulk_store(kp + dst, src, nj * row_bytes);
+      bulk_store(vp + dst, src + tile_bytes, nj * row_bytes);
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
   }
+  if (tid == 0) {
+    if (!ok) flag(err, AKV_DERR_WAIT);
+    // every store has finished before the block (and its shared memory) goes;
+    // loads still in flight after a failed wait land first (bounded)
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (!ok)
+      for (int i = waited; i < issued; ++i)
+        gwait(sm32(&s_full[i % n_stages]), (i / n_stages) & 1, kDrainPolls);
+  }
+  __syncthreads();
 }
 
 // ---------------------------------------------------------------------------
@@ -685,13 +750,21 @@ cudaError_t launch_compact(const Geom& g, const SeqArrays& sa, const ReposItem* 
 
 cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* items,
                           int n_items, int n_blocks, const float2* cs, uint32_t* err,
-                          cudaStream_t st) {
+                          uint32_t wait_limit, cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
-  const size_t smem = (size_t)g.s * (g.rope / 2) * sizeof(float2);
-  if (g.dtype == AKV_DTYPE_BF16)
-    k_gather<__nv_bfloat16><<<n_blocks, 256, smem, st>>>(g, sa, items, n_items, cs, err);
-  else
-    k_gather<float><<<n_blocks, 256, smem, st>>>(g, sa, items, n_items, cs, err);
+  const size_t elem = g.dtype == AKV_DTYPE_BF16 ? 2 : 4;
+  const size_t tile = (size_t)g.s * g.d * elem;             // one (layer, head) tile, one tensor
+  const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
+  const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
+  if (g.dtype == AKV_DTYPE_BF16) {
+    cudaFuncSetAttribute(k_gather<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k_gather<__nv_bfloat16><<<n_blocks, kGatherThreads, smem, st>>>(g, sa, items, n_items, cs, err,
+                                                                   n_stages, wait_limit);
+  } else {
+    cudaFuncSetAttribute(k_gather<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k_gather<float><<<n_blocks, kGatherThreads, smem, st>>>(g, sa, items, n_items, cs, err,
+                                                           n_stages, wait_limit);
+  }
   return cudaGetLastError();
 }
 
