@@ -1291,11 +1291,19 @@ int akv_prefix_fork(akv_cache* c, akv_prefix_index* x, const akv_op* ops, int32_
   s.gather_n = 0;
   s.key = history_key(x->idx, req.recs, (size_t)m.n_records);
 
+  // moves are in slot order, so each fresh page's moves are contiguous
+  std::vector<MoveBlock> mblocks;
+  for (size_t m = 0; m < moves.size(); ++m) {
+    if (mblocks.empty() || mblocks.back().dst_page != moves[m].dst_page)
+      mblocks.push_back({(int32_t)m, 0, moves[m].dst_page});
+    ++mblocks.back().count;
+  }
   Blob blob;
   const size_t o_keep = blob.put(keep.data(), keep.size());
   const size_t o_pages = blob.put(s.pages.data(), s.pages.size());
   const size_t o_act = blob.put(act.data(), act.size());
   const size_t o_mv = blob.put(moves.data(), moves.size());
+  const size_t o_mb = blob.put(mblocks.data(), mblocks.size());
   rc = grow_fork_scratch(c, blob.b.size() + 16);
   if (rc) return rc;
   rc = upload_large(c, blob, static_cast<char*>(c->d_fork));
@@ -1325,7 +1333,8 @@ int akv_prefix_fork(akv_cache* c, akv_prefix_index* x, const akv_op* ops, int32_
   *child = id;
   if (!moves.empty()) {
     CK(launch_transplant(c->g, reinterpret_cast<const MoveItem*>(d + o_mv), (int)moves.size(),
-                         c->d_cs, c->cfg.max_slots, c->d_err, c->stream));
+                         reinterpret_cast<const MoveBlock*>(d + o_mb), (int)mblocks.size(),
+                         c->d_cs, c->cfg.max_slots, c->d_err, c->wait_limit, c->stream));
     ++c->launches;
   }
   return AKV_OK;

@@ -155,10 +155,10 @@ bool make_restore_tensor_maps(const Geom& g, const void* k_era, const void* v_er
 
 // ---- prefix fork: stored keys of a snapshot moved into fresh pages ----------
 struct MoveItem { int32_t src_page, src_off, dst_page, dst_off, delta; };
-constexpr int kMoveTokens = 32;   // moves per block
-constexpr int kMoveLayers = 4;    // physical layers per block
-cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves, const float2* cs,
-                              int max_pos, uint32_t* err, cudaStream_t st);
+struct MoveBlock { int32_t first, count, dst_page; };   // the moves into one fresh page
+cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves,
+                              const MoveBlock* blocks, int n_blocks, const float2* cs, int max_pos,
+                              uint32_t* err, uint32_t wait_limit, cudaStream_t st);
 
 // Launchers (akv_kernels.cu / akv_decode.cu).  All enqueue on `st`.
 struct AppendLimits { int32_t n_items, n_ids, n_act, max_seqs; };

@@ -427,6 +427,112 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, uint32_t li
   return false;
 }
 
+// The staged tile pipeline shared by the reposition gather and the prefix
+// fork: for every (layer, KV head) tile of destination page `dpage`, rows
+// t of the stage receive source rows (s_src_page[t], s_src_off[t]) through
+// one bulk copy per run, keys with s_rot[t] are rotated in place with the
+// row's cos/sin (s_cs, unit-minor), and rows [0, n_store) go out with one
+// bulk copy per tensor.  Layers l_begin..l_end-1 map to slab l % phys_layers.
+template <typename T>
+__device__ __forceinline__ void tile_pipeline(
+    const Geom& g, int l_begin, int l_end, unsigned char* stage0, const float2* s_cs, const int* s_src_page,
+    const int* s_src_off, const int* s_rot, const int* s_run_t0, const int* s_run_len, int n_runs,
+    uint32_t bytes, int dpage, int n_store, int n_stages, uint64_t* s_full, uint32_t* err,
+    uint32_t wait_limit) {
+  constexpr int E = Vec<T>::E;
+  const int D = g.d, RH = g.rope / 2, kr = RH / E;
+  const uint32_t row_bytes = D * sizeof(T);
+  const uint32_t tile_bytes = g.s * row_bytes;
+  const int tid = threadIdx.x;
+  const int n = (l_end - l_begin) * g.hkv;       // tiles: (layer, KV head)
+  T* kp = static_cast<T*>(g.k);
+  T* vp = static_cast<T*>(g.v);
+  auto issue = [&](int i) {                      // thread 0: loads of tile i into its stage
+    const int st = i % n_stages;
+    const int l = l_begin + i / g.hkv, h = i % g.hkv;
+    const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
+    const uint32_t bar = sm32(&s_full[st]);
+    const uint32_t kd = sm32(stage0 + (size_t)st * 2 * tile_bytes), vd = kd + tile_bytes;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    for (int r = 0; r < n_runs; ++r) {
+      const int t0 = s_run_t0[r];
+      const int64_t off = slab + (int64_t)s_src_page[t0] * g.page_stride + (int64_t)h * g.head_stride +
+                          (int64_t)s_src_off[t0] * D;
+      const uint32_t len = s_run_len[r] * row_bytes;
+      bulk_load(kd + t0 * row_bytes, kp + off, len, bar);
+      bulk_load(vd + t0 * row_bytes, vp + off, len, bar);
+    }
+  };
+  int issued = 0, waited = 0;                    // thread 0: tiles issued / complete
+  if (tid == 0)
+    for (; issued < min(n_stages - 1, n); ++issued) issue(issued);
+  bool ok = true;
+  for (int i = 0; i < n; ++i) {
+    const int st = i % n_stages;
+    if (tid == 0 && i + n_stages - 1 < n) {
+      // the stage of tile i - 1 is free once its stores have read it
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      issue(i + n_stages - 1);
+      issued = i + n_stages;
+    }
+    ok = __syncthreads_and(gwait(sm32(&s_full[st]), (i / n_stages) & 1, wait_limit));
+    if (!ok) break;
+    waited = i + 1;
+    T* kt = reinterpret_cast<T*>(stage0 + (size_t)st * 2 * tile_bytes);
+    for (int u = tid; u < n_store * kr; u += blockDim.x) {
+      const int t = u / kr, c = u % kr;
+      if (!s_rot[t] || s_src_page[t] < 0) continue;
+      T* row = kt + (size_t)t * D;
+      const uint4 lo = *reinterpret_cast<const uint4*>(row + c * E);
+      const uint4 hi = *reinterpret_cast<const uint4*>(row + RH + c * E);
+      rotate_regs<T>(lo, hi, row, c, RH, s_cs + t * RH, kr);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+      const int l = l_begin + i / g.hkv, h = i % g.hkv;
+      const int64_t dst = (int64_t)(l % g.phys_layers) * g.layer_stride +
+                          (int64_t)dpage * g.page_stride + (int64_t)h * g.head_stride;
+      const uint32_t src = sm32(stage0 + (size_t)st * 2 * tile_bytes);
+      bulk_store(kp + dst, src, n_store * row_bytes);
+      bulk_store(vp + dst, src + tile_bytes, n_store * row_bytes);
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+  }
+  if (tid == 0) {
+    if (!ok) flag(err, AKV_DERR_WAIT);
+    // every store has finished before the block (and its shared memory) goes;
+    // loads still in flight after a failed wait land first (bounded)
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (!ok)
+      for (int i = waited; i < issued; ++i)
+        gwait(sm32(&s_full[i % n_stages]), (i / n_stages) & 1, kDrainPolls);
+  }
+  __syncthreads();
+}
+
+// runs of rows whose source slots are consecutive in one source page
+__device__ __forceinline__ void find_runs(int n_rows, const int* s_src_page, const int* s_src_off,
+                                          uint32_t row_bytes, int* s_run_t0, int* s_run_len,
+                                          int* s_n_runs, uint32_t* s_bytes) {
+  int nr = 0;
+  uint32_t bytes = 0;
+  for (int t = 0; t < n_rows; ++t) {
+    if (s_src_page[t] < 0) continue;
+    if (nr > 0 && s_run_t0[nr - 1] + s_run_len[nr - 1] == t && s_src_page[t] == s_src_page[t - 1] &&
+        s_src_off[t] == s_src_off[t - 1] + 1) {
+      ++s_run_len[nr - 1];
+    } else {
+      s_run_t0[nr] = t;
+      s_run_len[nr] = 1;
+      ++nr;
+    }
+    bytes += 2 * row_bytes;
+  }
+  *s_n_runs = nr;
+  *s_bytes = bytes;
+}
+
 constexpr int kGatherThreads = 128;
 
 template <typename T>
@@ -487,202 +593,91 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (tid == 0) {
-    // runs of rows whose source slots are consecutive in one source page
-    int nr = 0;
-    uint32_t bytes = 0;
-    for (int t = 0; t < nj; ++t) {
-      if (s_src_page[t] < 0) continue;
-      if (nr > 0 && s_run_t0[nr - 1] + s_run_len[nr - 1] == t &&
-          s_src_page[t] == s_src_page[t - 1] && s_src_off[t] == s_src_off[t - 1] + 1) {
-        ++s_run_len[nr - 1];
-      } else {
-        s_run_t0[nr] = t;
-        s_run_len[nr] = 1;
-        ++nr;
-      }
-      bytes += 2 * row_bytes;
-    }
-    s_n_runs = nr;
-    s_bytes = bytes;
-  }
+  if (tid == 0) find_runs(nj, s_src_page, s_src_off, row_bytes, s_run_t0, s_run_len, &s_n_runs, &s_bytes);
   __syncthreads();
   const int dpage = s_dst_page;
   if (dpage < 0) return;
-  const int n_runs = s_n_runs;
-  const uint32_t bytes = s_bytes;
-  const int n = g.layers * g.hkv;                // tiles: (logical layer, KV head)
-  T* kp = static_cast<T*>(g.k);
-  T* vp = static_cast<T*>(g.v);
-
-  auto issue = [&](int i) {                      // thread 0: loads of tile i into its stage
-    const int s = i % n_stages;
-    const int l = i / g.hkv, h = i % g.hkv;
-    const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
-    const uint32_t bar = sm32(&s_full[s]);
-    const uint32_t kd = sm32(stage0 + (size_t)s * 2 * tile_bytes), vd = kd + tile_bytes;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-    for (int r = 0; r < n_runs; ++r) {
-      const int t0 = s_run_t0[r];
-      const int64_t off = slab + (int64_t)s_src_page[t0] * g.page_stride + (int64_t)h * g.head_stride +
-                          (int64_t)s_src_off[t0] * D;
-      const uint32_t len = s_run_len[r] * row_bytes;
-      bulk_load(kd + t0 * row_bytes, kp + off, len, bar);
-      bulk_load(vd + t0 * row_bytes, vp + off, len, bar);
-    }
-  };
-  int issued = 0;                                // thread 0: tiles whose loads are issued
-  if (tid == 0)
-    for (; issued < min(n_stages - 1, n); ++issued) issue(issued);
-  bool ok = true;
-  int waited = 0;
-  const int kr = RH / E;
-  for (int i = 0; i < n; ++i) {
-    const int s = i % n_stages;
-    if (tid == 0 && i + n_stages - 1 < n) {
-      // the stage of tile i - 1 is free once its stores have read it
-      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      issue(i + n_stages - 1);
-      issued = i + n_stages;
-    }
-    ok = __syncthreads_and(gwait(sm32(&s_full[s]), (i / n_stages) & 1, wait_limit));
-    if (!ok) break;
-    waited = i + 1;
-    T* kt = reinterpret_cast<T*>(stage0 + (size_t)s * 2 * tile_bytes);
-    // rotate the moved keys' rotary pairs in place
-    for (int u = tid; u < nj * kr; u += kGatherThreads) {
-      const int t = u / kr, c = u % kr;
-      if (!s_rot[t] || s_src_page[t] < 0) continue;
-      T* row = kt + (size_t)t * D;
-      const uint4 lo = *reinterpret_cast<const uint4*>(row + c * E);
-      const uint4 hi = *reinterpret_cast<const uint4*>(row + RH + c * E);
-      rotate_regs<T>(lo, hi, row, c, RH, s_cs + t * RH, kr);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (tid == 0) {
-      const int l = i / g.hkv, h = i % g.hkv;
-      const int64_t dst = (int64_t)(l % g.phys_layers) * g.layer_stride +
-                          (int64_t)dpage * g.page_stride + (int64_t)h * g.head_stride;
-      const uint32_t src = sm32(stage0 + (size_t)s * 2 * tile_bytes);
-      bulk_store(kp + dst, src, nj * row_bytes);
-      bulk_store(vp + dst, src + tile_bytes, nj * row_bytes);
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    }
-  }
-  if (tid == 0) {
-    if (!ok) flag(err, AKV_DERR_WAIT);
-    // every store has finished before the block (and its shared memory) goes;
-    // loads still in flight after a failed wait land first (bounded)
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    if (!ok)
-      for (int i = waited; i < issued; ++i)
-        gwait(sm32(&s_full[i % n_stages]), (i / n_stages) & 1, kDrainPolls);
-  }
-  __syncthreads();
+  const int lper = (g.layers + gridDim.y - 1) / gridDim.y;    // layers of this block
+  tile_pipeline<T>(g, blockIdx.y * lper, min(g.layers, (int)(blockIdx.y + 1) * lper), stage0, s_cs,
+                   s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes, dpage, nj,
+                   n_stages, s_full, err, wait_limit);
 }
 
 // ---------------------------------------------------------------------------
-// prefix fork: needed keys of a published snapshot moved into fresh pages of
-// a new sequence, each rotated by its own delta = p_request - p_stored (bit
-// copy when delta == 0), V copied.  One block per kMoveTokens moves and
-// kMoveLayers physical layers, all KV heads; each thread keeps 4 chunks in
-// flight.
+// prefix fork: needed keys of a published snapshot moved into a fresh page
+// of a new sequence, each rotated by its own delta = p_request - p_stored
+// (bit copy when delta == 0), V copied.  One block per fresh destination
+// page and its moves, through the staged tile pipeline (all physical
+// layers and KV heads).  Rows of the page that no move fills are dead
+// slots of the new sequence.
 // ---------------------------------------------------------------------------
 
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kGatherThreads)
 k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
-             const float2* __restrict__ cs, int max_pos, uint32_t* err) {
-  extern __shared__ float2 s_cs[];   // [kMoveTokens][R/2] (unit-minor), angle delta f
-  __shared__ MoveItem s_mv[kMoveTokens];
-  const int m0 = blockIdx.x * kMoveTokens;
-  const int nm = min(kMoveTokens, n_moves - m0);
-  const int layer0 = blockIdx.y * kMoveLayers;   // physical slabs of this block
-  const int nl = min(kMoveLayers, g.phys_layers - layer0);
-  const int S = g.s, D = g.d, R = g.rope, RH = R / 2;
-  const int tid = threadIdx.x, bs = blockDim.x;
-  for (int t = tid; t < nm; t += bs) {
-    MoveItem mv = moves[m0 + t];
-    const bool ok = mv.src_page >= 0 && mv.src_page < g.max_pages && mv.dst_page >= 0 &&
-                    mv.dst_page < g.max_pages && mv.src_off >= 0 && mv.src_off < S &&
-                    mv.dst_off >= 0 && mv.dst_off < S && mv.delta > -max_pos && mv.delta < max_pos;
-    if (!ok) {
-      if (layer0 == 0) flag(err, AKV_DERR_PAGE);
-      mv.src_page = -1;
-    }
-    s_mv[t] = mv;
+             const MoveBlock* __restrict__ blocks, const float2* __restrict__ cs, int max_pos,
+             uint32_t* err, int n_stages, uint32_t wait_limit) {
+  constexpr int E = Vec<T>::E;
+  extern __shared__ __align__(128) unsigned char gsm[];
+  const int S = g.s, D = g.d, RH = g.rope / 2, kr = RH / E;
+  const uint32_t row_bytes = D * sizeof(T);
+  const uint32_t tile_bytes = S * row_bytes;
+  unsigned char* stage0 = gsm;                                // [n_stages][K, V][S][D]
+  float2* s_cs = reinterpret_cast<float2*>(gsm + (size_t)n_stages * 2 * tile_bytes);   // [S][R/2]
+  __shared__ int s_src_page[64], s_src_off[64], s_rot[64], s_delta[64];
+  __shared__ int s_run_t0[64], s_run_len[64], s_n_runs, s_n_store;
+  __shared__ uint32_t s_bytes;
+  __shared__ __align__(8) uint64_t s_full[8];
+  const MoveBlock mb = blocks[blockIdx.x];
+  const int tid = threadIdx.x;
+  if (mb.dst_page < 0 || mb.dst_page >= g.max_pages || mb.first < 0 || mb.count < 1 ||
+      mb.count > S || mb.first + mb.count > n_moves) {
+    if (tid == 0) flag(err, AKV_DERR_PAGE);
+    return;
   }
-  {
-    constexpr int E = Vec<T>::E;
-    const int kr = RH / E;
-    for (int i = tid; i < nm * RH; i += bs) {
-      const int t = i / RH, j = i % RH;
-      const int delta = moves[m0 + t].delta;
-      const int a = delta < 0 ? -delta : delta;
-      float2 c = make_float2(1.f, 0.f);
-      if (a < max_pos) c = cs[(int64_t)a * RH + j];
-      s_cs[t * RH + (j % E) * kr + j / E] = make_float2(c.x, delta < 0 ? -c.y : c.y);
+  for (int t = tid; t < S; t += kGatherThreads) {
+    s_src_page[t] = -1;
+    s_src_off[t] = 0;
+    s_rot[t] = 0;
+    s_delta[t] = 0;
+  }
+  if (tid == 0) s_n_store = 0;
+  __syncthreads();
+  for (int m = tid; m < mb.count; m += kGatherThreads) {
+    const MoveItem mv = moves[mb.first + m];
+    const bool ok = mv.src_page >= 0 && mv.src_page < g.max_pages && mv.dst_page == mb.dst_page &&
+                    mv.src_off >= 0 && mv.src_off < S && mv.dst_off >= 0 && mv.dst_off < S &&
+                    mv.delta > -max_pos && mv.delta < max_pos;
+    if (!ok) {
+      flag(err, AKV_DERR_PAGE);
+      continue;
     }
+    s_src_page[mv.dst_off] = mv.src_page;
+    s_src_off[mv.dst_off] = mv.src_off;
+    s_rot[mv.dst_off] = mv.delta != 0;
+    s_delta[mv.dst_off] = mv.delta;
+    atomicMax(&s_n_store, mv.dst_off + 1);
   }
   __syncthreads();
-  constexpr int E = Vec<T>::E;
-  constexpr int B = 4;               // units in flight per thread
-  const int kr = RH / E, kc = (D - R) / E, vu = D / E, per_row = kr + kc + vu;
-  const int units = g.hkv * nm * per_row;
-  const T* __restrict__ ks = static_cast<const T*>(g.k);
-  const T* __restrict__ vs = static_cast<const T*>(g.v);
-  T* __restrict__ kd = static_cast<T*>(g.k);
-  T* __restrict__ vd = static_cast<T*>(g.v);
-  for (int w0 = tid; w0 < nl * units; w0 += B * bs) {
-    uint4 lo[B], hi[B];
-    int64_t so[B], dof[B];
-    int rr[B], tt[B];
-#pragma unroll
-    for (int j = 0; j < B; ++j) {
-      const int w = w0 + j * bs;
-      rr[j] = -1;
-      if (w >= nl * units) continue;
-      const int u = w % units;
-      const int64_t slab = (int64_t)(layer0 + w / units) * g.layer_stride;
-      const int r = u % per_row;
-      const int t = (u / per_row) % nm;
-      const int h = u / (per_row * nm);
-      const MoveItem mv = s_mv[t];
-      if (mv.src_page < 0) continue;
-      rr[j] = r;
-      tt[j] = t;
-      so[j] = slab + (int64_t)mv.src_page * g.page_stride + (int64_t)h * g.head_stride +
-              (int64_t)mv.src_off * D;
-      dof[j] = slab + (int64_t)mv.dst_page * g.page_stride + (int64_t)h * g.head_stride +
-               (int64_t)mv.dst_off * D;
-      if (r < kr) {
-        lo[j] = ld16(ks + so[j] + r * E);
-        hi[j] = ld16(ks + so[j] + RH + r * E);
-      } else if (r < kr + kc) {
-        lo[j] = ld16(ks + so[j] + R + (r - kr) * E);
-      } else {
-        lo[j] = ld16(vs + so[j] + (r - kr - kc) * E);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < B; ++j) {
-      const int r = rr[j];
-      if (r < 0) continue;
-      if (r < kr) {
-        if (s_mv[tt[j]].delta == 0) {
-          st16(kd + dof[j] + r * E, lo[j]);
-          st16(kd + dof[j] + RH + r * E, hi[j]);
-        } else {
-          rotate_regs<T>(lo[j], hi[j], kd + dof[j], r, RH, s_cs + tt[j] * RH, kr);
-        }
-      } else if (r < kr + kc) {
-        st16(kd + dof[j] + R + (r - kr) * E, lo[j]);
-      } else {
-        st16(vd + dof[j] + (r - kr - kc) * E, lo[j]);
-      }
-    }
+  const int n_store = s_n_store;
+  for (int i = tid; i < n_store * RH; i += kGatherThreads) {
+    const int t = i / RH, j = i % RH;
+    const int delta = s_delta[t];
+    const int a = delta < 0 ? -delta : delta;
+    const float2 c = a < max_pos ? cs[(int64_t)a * RH + j] : make_float2(1.f, 0.f);
+    s_cs[t * RH + (j % E) * kr + j / E] = make_float2(c.x, delta < 0 ? -c.y : c.y);
   }
+  if (tid == 0) {
+    for (int st = 0; st < n_stages; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm32(&s_full[st])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    find_runs(n_store, s_src_page, s_src_off, row_bytes, s_run_t0, s_run_len, &s_n_runs, &s_bytes);
+  }
+  __syncthreads();
+  const int lper = (g.phys_layers + gridDim.y - 1) / gridDim.y;   // slabs of this block
+  tile_pipeline<T>(g, blockIdx.y * lper, min(g.phys_layers, (int)(blockIdx.y + 1) * lper), stage0,
+                   s_cs, s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes,
+                   mb.dst_page, n_store, n_stages, s_full, err, wait_limit);
 }
 
 }  // namespace
@@ -691,16 +686,39 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
 // launchers
 // ---------------------------------------------------------------------------
 
-cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves, const float2* cs,
-                              int max_pos, uint32_t* err, cudaStream_t st) {
-  if (n_moves <= 0) return cudaSuccess;
-  const dim3 grid((n_moves + kMoveTokens - 1) / kMoveTokens,
-                  (g.phys_layers + kMoveLayers - 1) / kMoveLayers);
-  const size_t smem = (size_t)kMoveTokens * (g.rope / 2) * sizeof(float2);
-  if (g.dtype == AKV_DTYPE_BF16)
-    k_transplant<__nv_bfloat16><<<grid, 256, smem, st>>>(g, moves, n_moves, cs, max_pos, err);
-  else
-    k_transplant<float><<<grid, 256, smem, st>>>(g, moves, n_moves, cs, max_pos, err);
+// Layer groups per destination page: enough (page, layer group) blocks for
+// about 32 per SM, so small calls still fill the GPU evenly; at most one
+// group per layer.
+inline int layer_groups(int n_blocks, int n_layers) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int want = (32 * sms + n_blocks - 1) / n_blocks;
+  return std::max(1, std::min(n_layers, want));
+}
+
+cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves,
+                              const MoveBlock* blocks, int n_blocks, const float2* cs, int max_pos,
+                              uint32_t* err, uint32_t wait_limit, cudaStream_t st) {
+  if (n_blocks <= 0) return cudaSuccess;
+  const size_t elem = g.dtype == AKV_DTYPE_BF16 ? 2 : 4;
+  const size_t tile = (size_t)g.s * g.d * elem;
+  const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
+  const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
+  const dim3 grid(n_blocks, layer_groups(n_blocks, g.phys_layers));
+  if (g.dtype == AKV_DTYPE_BF16) {
+    cudaFuncSetAttribute(k_transplant<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k_transplant<__nv_bfloat16><<<grid, kGatherThreads, smem, st>>>(
+        g, moves, n_moves, blocks, cs, max_pos, err, n_stages, wait_limit);
+  } else {
+    cudaFuncSetAttribute(k_transplant<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k_transplant<float><<<grid, kGatherThreads, smem, st>>>(
+        g, moves, n_moves, blocks, cs, max_pos, err, n_stages, wait_limit);
+  }
   return cudaGetLastError();
 }
 
@@ -756,14 +774,15 @@ cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* i
   const size_t tile = (size_t)g.s * g.d * elem;             // one (layer, head) tile, one tensor
   const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
   const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
+  const dim3 grid(n_blocks, layer_groups(n_blocks, g.layers));
   if (g.dtype == AKV_DTYPE_BF16) {
     cudaFuncSetAttribute(k_gather<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_gather<__nv_bfloat16><<<n_blocks, kGatherThreads, smem, st>>>(g, sa, items, n_items, cs, err,
-                                                                   n_stages, wait_limit);
+    k_gather<__nv_bfloat16><<<grid, kGatherThreads, smem, st>>>(g, sa, items, n_items, cs, err,
+                                                               n_stages, wait_limit);
   } else {
     cudaFuncSetAttribute(k_gather<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_gather<float><<<n_blocks, kGatherThreads, smem, st>>>(g, sa, items, n_items, cs, err,
-                                                           n_stages, wait_limit);
+    k_gather<float><<<grid, kGatherThreads, smem, st>>>(g, sa, items, n_items, cs, err,
+                                                       n_stages, wait_limit);
   }
   return cudaGetLastError();
 }
