@@ -112,10 +112,10 @@ struct DecodeArgs {
   int32_t max_seqs;     // device rows of the per-sequence arrays
   int32_t counter_rows; // rows of `counters`
 };
-constexpr int kDecodeMaxTiles = 512;// bound of the waits that let a kernel's own copies / MMAs land before it
+constexpr int kDecodeMaxTiles = 512;   // 16-token tiles in one split of the tensor-core path
+// bound of the waits that let a kernel's own copies / MMAs land before it
 // exits after a failed wait (independent of the user's wait limit)
 constexpr uint32_t kDrainPolls = 1u << 22;
-   // 16-token tiles in one split of the tensor-core path
 
 // ---- segment-batch restore attention -------------------------------------------
 struct RestoreKey { int32_t tok, pos, birth, death; };      // one era key row
