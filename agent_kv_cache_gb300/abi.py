@@ -117,6 +117,9 @@ SIGNATURES = {
     "akv_kernel_launches": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "akv_set_decode_waves": (ctypes.c_int, [_P, _I32]),
     "akv_set_restore_tensor_cores": (ctypes.c_int, [_P, _I32]),
+    "akv_set_decode_sharing": (ctypes.c_int, [_P, _I32]),
+    "akv_decode_plan_stats": (ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32),
+                                              ctypes.POINTER(_I32)]),
     "akv_set_layer_window": (ctypes.c_int, [_P, _I32, _I32]),
     "akv_restore_attention": (ctypes.c_int, [_P, ctypes.POINTER(AkvOp), _I32, _I32, _P, _P, _P,
                                              _I32, _P]),
@@ -353,6 +356,18 @@ def akv_set_decode_waves(cache, waves):
 
 def akv_set_restore_tensor_cores(cache, enable):
     _check(lib().akv_set_restore_tensor_cores(cache, 1 if enable else 0), cache)
+
+
+def akv_set_decode_sharing(cache, mode):
+    """mode: False/0 off, True/1 automatic, 2..16 the most rows per shared item."""
+    _check(lib().akv_set_decode_sharing(cache, int(mode)), cache)
+
+
+def akv_decode_plan_stats(cache):
+    items, shared, members = _I32(), _I32(), _I32()
+    _check(lib().akv_decode_plan_stats(cache, ctypes.byref(items), ctypes.byref(shared),
+                                       ctypes.byref(members)), cache)
+    return {"items": items.value, "shared_items": shared.value, "members": members.value}
 
 
 def akv_kernel_launches(cache):

@@ -95,6 +95,15 @@ class Cache:
     def set_restore_tensor_cores(self, enable):
         abi.akv_set_restore_tensor_cores(self.handle, enable)
 
+    def set_decode_sharing(self, mode):
+        """Rows holding the same pages read them once per decode call: False /
+        0 off, True / 1 automatic (default), 2..16 the most rows per item."""
+        abi.akv_set_decode_sharing(self.handle, mode)
+
+    def decode_plan_stats(self):
+        """Work items of the last decode call: {"items", "shared_items", "members"}."""
+        return abi.akv_decode_plan_stats(self.handle)
+
     def set_layer_window(self, layer, window):
         abi.akv_set_layer_window(self.handle, layer, window)
 

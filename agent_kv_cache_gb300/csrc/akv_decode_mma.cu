@@ -112,7 +112,20 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-template <int D>
+// A member (query row) must name memory this call owns.
+__device__ __forceinline__ bool member_ok(const DecodeMember& m, const DecodeArgs& a) {
+  return m.row >= 0 && m.row < a.n_rows && m.row < a.counter_rows && m.n_splits >= 1 &&
+         m.item0 >= 0 && m.item0 + m.n_splits <= a.part_cap && m.part >= m.item0 &&
+         m.part < m.item0 + m.n_splits && m.n_tiles >= 0;
+}
+
+// SHARE: the plan has items whose pages several rows hold (same pages, same
+// keep bits).  Such an item reads its range once for all of them: its query
+// columns are the members' GQA groups side by side, nb blocks of 8 columns,
+// and warp w computes column block w % nb on every (4/nb)-th tile.  A member
+// holds a leading part of the range (n_tiles tiles); its columns mask the
+// tiles after it.  Without SHARE the kernel is the one-row form (nb = 1).
+template <int D, bool SHARE>
 __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__ DecodeArgs a) {
   constexpr int KS = D / 16;                    // k-steps of Q K^T, m-tiles of V^T P^T
   constexpr int TILE_BYTES = kTile * D * 2;     // one K (or V) tile
@@ -121,13 +134,14 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // The stage ring also holds, before the tile loop, the rotated query
-  // [8][D] and, after it, the consumer warps' partials [4][8][D+2].
+  // [8 nb][D] and, after it, the consumer warps' partials [4][8][D+2].
   float* s_q = reinterpret_cast<float*>(smem);
   float* s_merge = reinterpret_cast<float*>(smem);
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
   __shared__ int s_row[kMaxTiles];              // TMA row of each tile, -1 = unusable
   __shared__ uint16_t s_bits[kMaxTiles];        // keep bits of each tile's 16 slots
-  __shared__ int s_last;
+  __shared__ DecodeMember s_mem[SHARE ? kDecodeMaxMembers : 1];
+  __shared__ int s_lastm[SHARE ? kDecodeMaxMembers : 1];
 
   // the next decode call may be scheduled now: its blocks start as this
   // grid's blocks retire and wait (griddepcontrol.wait) before writing
@@ -140,15 +154,33 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   const int t0 = it.p0 * tpp;
   int n = it.p1 * tpp - t0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // column blocks and members (rows) of this item
+  const int nb = SHARE ? it.nb : 1;
+  const int n_mem = SHARE && it.n_mem > 0 ? it.n_mem : 1;
   // the work item must describe memory this call owns (uniform per block)
-  const bool bad_item =
-      it.dslot < 0 || it.dslot >= a.max_seqs || it.row < 0 || it.row >= a.n_rows ||
-      it.p0 < 0 || it.p1 < it.p0 || it.p1 > a.sa.seq_pages || it.n_splits < 1 ||
-      it.item0 < 0 || it.item0 + it.n_splits > a.n_items || (int)blockIdx.x < it.item0 ||
-      (int)blockIdx.x >= it.item0 + it.n_splits || it.row >= a.counter_rows;
-  if (bad_item) {
-    if (tid == 0) atomicOr(a.err, AKV_DERR_INDEX);
-    return;
+  bool bad = it.dslot < 0 || it.dslot >= a.max_seqs || it.p0 < 0 || it.p1 < it.p0 ||
+             it.p1 > a.sa.seq_pages;
+  // the one-row form keeps its member in registers (no start-up barrier)
+  const DecodeMember me{it.row, it.pos_q, it.item0, it.n_splits, it.part, kMaxTiles};
+  auto member = [&](int m) -> const DecodeMember& { return SHARE ? s_mem[m] : me; };
+  if constexpr (SHARE) {
+    bad |= !(nb == 1 || nb == 2 || nb == 4) || n_mem > kDecodeMaxMembers ||
+           n_mem * G > 8 * nb ||
+           (it.n_mem > 0 && (it.mem0 < 0 || it.mem0 + it.n_mem > a.n_members));
+    if (!bad && tid < n_mem) {
+      const DecodeMember m = it.n_mem > 0 ? a.members[it.mem0 + tid] : me;
+      bad = !member_ok(m, a);
+      s_mem[tid] = m;
+    }
+    if (__syncthreads_or(bad)) {
+      if (tid == 0) atomicOr(a.err, AKV_DERR_INDEX);
+      return;
+    }
+  } else {
+    if (bad || !member_ok(me, a)) {
+      if (tid == 0) atomicOr(a.err, AKV_DERR_INDEX);
+      return;
+    }
   }
   if (n > kMaxTiles) {                          // the planner never makes such a split
     if (tid == 0) atomicOr(a.err, AKV_DERR_INDEX);
@@ -157,9 +189,10 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   const int64_t slab_rows = (int64_t)g.max_pages * g.hkv * g.s;
 
   if (tid == 0) {
+    // a stage is released by the nb warps (one per column block) that read it
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&s_empty[s]), 1);
+      mbar_init(smem_u32(&s_empty[s]), nb);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -188,37 +221,40 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
       s_bits[i] = (uint16_t)bits;
     }
   }
-  // rotated, scaled query of the group (heads >= G stay zero); the first R
-  // dims rotate in pairs (d, d + R/2), dims R.. are only scaled
+  // rotated, scaled queries: column c is head c % G of member c / G
+  // (columns past the members stay zero); the first R dims rotate in pairs
+  // (d, d + R/2), dims R.. are only scaled
   {
     const int R = g.rope, RH = R / 2;
-    const bool have_q = it.pos_q >= 0 && it.pos_q < a.sa.max_slots;
-    for (int i = tid; i < 8 * D; i += kThreads) {
-      const int gq = i / D, d = i % D;
+    for (int i = tid; i < 8 * nb * D; i += kThreads) {
+      const int c = i / D, d = i % D, m = c / G, gq = c % G;
+      const DecodeMember& mm = member(m < n_mem ? m : 0);
+      const bool have_q = m < n_mem && mm.pos_q >= 0 && mm.pos_q < a.sa.max_slots;
       const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) +
-                               ((int64_t)it.row * g.hq + (int64_t)kvh * G + gq) * D;
+                               ((int64_t)mm.row * g.hq + (int64_t)kvh * G + gq) * D;
       if (d < RH) {
         float x = 0.f, y = 0.f;
-        if (gq < G && have_q) {
+        if (have_q) {
           const float qx = __bfloat162float(q[d]), qy = __bfloat162float(q[d + RH]);
-          const float2 t = a.cs[(int64_t)it.pos_q * RH + d];
+          const float2 t = a.cs[(int64_t)mm.pos_q * RH + d];
           x = fmaf(qx, t.x, -qy * t.y) * a.scale_log2;
           y = fmaf(qx, t.y, qy * t.x) * a.scale_log2;
         }
-        s_q[gq * D + d] = x;
-        s_q[gq * D + d + RH] = y;
+        s_q[c * D + d] = x;
+        s_q[c * D + d + RH] = y;
       } else if (d >= R) {
-        s_q[gq * D + d] = (gq < G && have_q) ? __bfloat162float(q[d]) * a.scale_log2 : 0.f;
+        s_q[c * D + d] = have_q ? __bfloat162float(q[d]) * a.scale_log2 : 0.f;
       }
     }
   }
   __syncthreads();
-  // Q^T fragments (B operand of the score MMA): lane holds head lane/4,
-  // dims 2*(lane%4)+{0,1} and +8 of each 16-dim k-step
+  // Q^T fragments (B operand of the score MMA) of the warp's column block:
+  // lane holds column lane/4, dims 2*(lane%4)+{0,1} and +8 of each k-step
+  const int nblk = warp % nb, phase = warp / nb, n_phase = kConsumers / nb;
   uint32_t qf[KS][2];
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
-    const int h = lane >> 2, c = ks * 16 + (lane & 3) * 2;
+    const int h = (warp < kConsumers ? nblk * 8 : 0) + (lane >> 2), c = ks * 16 + (lane & 3) * 2;
     qf[ks][0] = pack_bf16(s_q[h * D + c], s_q[h * D + c + 1]);
     qf[ks][1] = pack_bf16(s_q[h * D + c + 8], s_q[h * D + c + 9]);
   }
@@ -229,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
 
   const int slab = (a.layer >= 0 ? a.layer : 0) % g.phys_layers;
   float o[KS][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2*(lane%4), +1
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // columns 2*(lane%4), +1
 
   if (warp == kConsumers) {
     // ---------------- producer ----------------
@@ -277,7 +313,14 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
     const int r0 = lane >> 2;
     const int tk = (lane & 3) * 2;
 
-    for (int i = warp; i < n; i += kConsumers) {
+    // tiles of the lane's two columns (shared items: the member's part)
+    int end0 = n, end1 = n;
+    if (SHARE) {
+      const int c0 = nblk * 8 + (lane & 3) * 2;
+      if (c0 / G < n_mem) end0 = member(c0 / G).n_tiles;
+      if ((c0 + 1) / G < n_mem) end1 = member((c0 + 1) / G).n_tiles;
+    }
+    for (int i = phase; i < n; i += n_phase) {
       const int s = i % kStages;
       // every lane waits (acquire for its own reads); the outcome is made
       // warp-uniform before the warp-synchronous MMAs
@@ -292,14 +335,34 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
         const uint32_t bits = s_bits[i];
         // S^T = K Q^T
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (SHARE) {
+          // two accumulation chains (even / odd k-steps) halve the dependent
+          // MMA latency of a tile, which bounds items whose warps read every
+          // tile; the one-row form waits on memory instead
+          float sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t af[4];
-          ldsm_x4(kb + swz(k_row, ks * 2 + k_cb), af);
-          mma16816(sc, af, qf[ks][0], qf[ks][1]);
+          for (int ks = 0; ks < KS; ks += 2) {
+            uint32_t af[4], ag[4];
+            ldsm_x4(kb + swz(k_row, ks * 2 + k_cb), af);
+            ldsm_x4(kb + swz(k_row, ks * 2 + 2 + k_cb), ag);
+            mma16816(sc, af, qf[ks][0], qf[ks][1]);
+            mma16816(sd, ag, qf[ks + 1][0], qf[ks + 1][1]);
+          }
+          sc[0] += sd[0]; sc[1] += sd[1]; sc[2] += sd[2]; sc[3] += sd[3];
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t af[4];
+            ldsm_x4(kb + swz(k_row, ks * 2 + k_cb), af);
+            mma16816(sc, af, qf[ks][0], qf[ks][1]);
+          }
         }
         if (!((bits >> r0) & 1u)) sc[0] = sc[1] = -INFINITY;
         if (!((bits >> (r0 + 8)) & 1u)) sc[2] = sc[3] = -INFINITY;
+        if (SHARE) {
+          if (i >= end0) sc[0] = sc[2] = -INFINITY;
+          if (i >= end1) sc[1] = sc[3] = -INFINITY;
+        }
         // online softmax over the tile (columns = heads)
         float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
@@ -358,7 +421,7 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   }
   __syncthreads();   // every tile consumed and every copy landed: the ring is free
   if (warp < kConsumers) {
-    // per-warp partial -> shared: [warp][head][D] then m, l at [D], [D+1]
+    // per-warp partial -> shared: [warp][column][D] then m, l at [D], [D+1]
     float* wm = s_merge + warp * 8 * (D + 2);
     const int h0 = (lane & 3) * 2;
 #pragma unroll
@@ -383,67 +446,159 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   // block's first global write waits until that grid has finished.  Nothing
   // above reads memory a decode call writes.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // merge the consumer warps: the output (one split) or this split's partial
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int gq = i / D, d = i % D;
+  // merge the consumer warps of each column (the n_phase warps of its
+  // block): the member's output (its only split) or this split's partial
+  bool multi = false;
+  for (int m = 0; m < n_mem; ++m) multi |= member(m).n_splits > 1;
+  for (int i = tid; i < n_mem * G * D; i += kThreads) {
+    const int c = i / D, d = i % D, hc = c & 7, cb = c >> 3;
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, s_merge[(w * 8 + gq) * (D + 2) + D]);
+    for (int ph = 0; ph < n_phase; ++ph)
+      M = fmaxf(M, s_merge[((ph * nb + cb) * 8 + hc) * (D + 2) + D]);
     float L = 0.f, A = 0.f;
     if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumers; ++w) {
-        const float* wm = s_merge + (w * 8 + gq) * (D + 2);
+      for (int ph = 0; ph < n_phase; ++ph) {
+        const float* wm = s_merge + ((ph * nb + cb) * 8 + hc) * (D + 2);
         const float f = exp2f(wm[D] - M);
         L = fmaf(wm[D + 1], f, L);
         A = fmaf(wm[d], f, A);
       }
     }
-    const int hq = kvh * G + gq;
-    if (it.n_splits == 1) {
-      a.out[((int64_t)it.row * g.hq + hq) * D + d] = L > 0.f ? A / L : 0.f;
+    const DecodeMember& mm = member(c / G);
+    const int gq = c % G, hq = kvh * G + gq;
+    if (mm.n_splits == 1) {
+      a.out[((int64_t)mm.row * g.hq + hq) * D + d] = L > 0.f ? A / L : 0.f;
     } else {
-      const int64_t pi = ((int64_t)blockIdx.x * g.hkv + kvh) * G + gq;
+      const int64_t pi = ((int64_t)mm.part * g.hkv + kvh) * G + gq;
       a.part_acc[pi * D + d] = A;
       if (d == 0) a.part_ml[pi] = make_float2(M, L);
     }
   }
-  if (it.n_splits == 1) return;
+  if (!multi) return;
 
-  // the last split of (row, kv head) to finish merges all of them
+  // for each member, the last split of (row, kv head) to finish merges all
+  // of that row's splits
   __threadfence();
   __syncthreads();
-  if (tid == 0) {
-    const int old = atomicAdd(&a.counters[it.row * g.hkv + kvh], 1);
-    s_last = old == it.n_splits - 1;
+  if (tid < n_mem) {
+    const DecodeMember& mm = member(tid);
+    int last = 0;
+    if (mm.n_splits > 1)
+      last = atomicAdd(&a.counters[mm.row * g.hkv + kvh], 1) == mm.n_splits - 1;
+    s_lastm[tid] = last;
   }
   __syncthreads();
-  if (!s_last) return;
+  int n_fin = 0;
+  for (int m = 0; m < n_mem; ++m) n_fin += s_lastm[m];
+  if (n_fin == 0) return;
   __threadfence();
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int gq = i / D, d = i % D;
-    float M = -INFINITY;
-    for (int c = 0; c < it.n_splits; ++c)
-      M = fmaxf(M, __ldcg(&a.part_ml[((int64_t)(it.item0 + c) * g.hkv + kvh) * G + gq]).x);
-    float L = 0.f, A = 0.f;
+  // k-th member whose merge falls to this block
+  auto fin_member = [&](int k) {
+    int m = 0;
+    for (; m < n_mem; ++m)
+      if (s_lastm[m] && k-- == 0) break;
+    return m;
+  };
+  // pass 1, one warp per (row, head): maximum and sum over the row's splits,
+  // the splits spread over the lanes (the stage ring is free: (M, L) there)
+  float2* s_ml = reinterpret_cast<float2*>(s_merge);
+  for (int p = warp; p < n_fin * G; p += kThreads / 32) {
+    const DecodeMember& mm = member(fin_member(p / G));
+    const int gq = p % G;
+    const float2* ml = a.part_ml + ((int64_t)mm.item0 * g.hkv + kvh) * G + gq;
+    const int64_t stride = (int64_t)g.hkv * G;
+    // lane c holds split c (and c + 32, ... past 32 splits)
+    const float2 v0 = lane < mm.n_splits ? __ldcg(ml + lane * stride) : make_float2(-INFINITY, 0.f);
+    float M = v0.x;
+    for (int c = lane + 32; c < mm.n_splits; c += 32) M = fmaxf(M, __ldcg(ml + c * stride).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
     if (M != -INFINITY) {
-      for (int c = 0; c < it.n_splits; ++c) {
-        const int64_t pi = ((int64_t)(it.item0 + c) * g.hkv + kvh) * G + gq;
-        const float2 ml = __ldcg(&a.part_ml[pi]);
-        const float f = exp2f(ml.x - M);
-        L = fmaf(ml.y, f, L);
-        A = fmaf(__ldcg(&a.part_acc[pi * D + d]), f, A);
+      if (lane < mm.n_splits) L = v0.y * exp2f(v0.x - M);
+      for (int c = lane + 32; c < mm.n_splits; c += 32) {
+        const float2 v = __ldcg(ml + c * stride);
+        L = fmaf(v.y, exp2f(v.x - M), L);
       }
     }
-    a.out[((int64_t)it.row * g.hq + kvh * G + gq) * D + d] = L > 0.f ? A / L : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) s_ml[p] = make_float2(M, L);
   }
-  if (tid == 0) a.counters[it.row * g.hkv + kvh] = 0;   // ready for the next call
+  if (tid < n_mem && s_lastm[tid])
+    a.counters[member(tid).row * g.hkv + kvh] = 0;   // ready for the next call
+  __syncthreads();
+  // pass 2: the weighted sum of the partials, four dims per output; a thread
+  // takes up to kPer outputs at once so that their loads are in flight
+  // together
+  constexpr int kPer = SHARE ? 8 : 1;
+  const int n_out = n_fin * G * (D / 4);
+  const bool vec_out = (reinterpret_cast<uintptr_t>(a.out) & 15) == 0;
+  for (int e0 = tid; e0 < n_out; e0 += kThreads * kPer) {
+    float4 A[kPer];
+    int64_t base[kPer];
+    int nsp[kPer];
+    float Mx[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = e0 + k * kThreads;
+      A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      nsp[k] = 0;
+      base[k] = 0;
+      Mx[k] = -INFINITY;
+      if (e < n_out) {
+        const int p = e / (D / 4);
+        const DecodeMember& mm = member(fin_member(p / G));
+        base[k] = ((int64_t)mm.item0 * g.hkv + kvh) * G + p % G;
+        Mx[k] = s_ml[p].x;
+        nsp[k] = Mx[k] == -INFINITY ? 0 : mm.n_splits;
+      }
+    }
+    int most = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) most = max(most, nsp[k]);
+    const int64_t stride = (int64_t)g.hkv * G;
+    for (int c = 0; c < most; ++c) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        if (c < nsp[k]) {
+          const int e = e0 + k * kThreads, d = (e % (D / 4)) * 4;
+          const int64_t pi = base[k] + c * stride;
+          const float f = exp2f(__ldcg(&a.part_ml[pi]).x - Mx[k]);
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_acc + pi * D + d));
+          A[k].x = fmaf(v.x, f, A[k].x);
+          A[k].y = fmaf(v.y, f, A[k].y);
+          A[k].z = fmaf(v.z, f, A[k].z);
+          A[k].w = fmaf(v.w, f, A[k].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = e0 + k * kThreads;
+      if (e >= n_out) continue;
+      const int p = e / (D / 4), d = (e % (D / 4)) * 4;
+      const DecodeMember& mm = member(fin_member(p / G));
+      const int gq = p % G;
+      const float L = s_ml[p].y;
+      const float4 o = L > 0.f ? make_float4(A[k].x / L, A[k].y / L, A[k].z / L, A[k].w / L)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      float* dst = a.out + ((int64_t)mm.row * g.hq + kvh * G + gq) * D + d;
+      if (vec_out) {
+        *reinterpret_cast<float4*>(dst) = o;
+      } else {                                  // the caller's output need only be 4-byte aligned
+        dst[0] = o.x; dst[1] = o.y; dst[2] = o.z; dst[3] = o.w;
+      }
+    }
+  }
 }
 
 template <int D>
 constexpr size_t mma_smem() {
   static_assert((size_t)kConsumers * 8 * (D + 2) * 4 <= (size_t)kStages * 2 * kTile * D * 2,
                 "the partials must fit in the stage ring");
+  static_assert((size_t)4 * 8 * D * 4 <= (size_t)kStages * 2 * kTile * D * 2,
+                "the queries of four column blocks must fit in the stage ring");
   return 1024 + (size_t)kStages * 2 * kTile * D * 2;
 }
 
@@ -451,7 +606,9 @@ template <int D>
 void set_smem_attr() {
   static bool done = false;
   if (!done) {
-    cudaFuncSetAttribute(k_decode_mma<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(k_decode_mma<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)mma_smem<D>());
+    cudaFuncSetAttribute(k_decode_mma<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)mma_smem<D>());
     done = true;
   }
@@ -511,21 +668,23 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
   if (a.g.d == 64) {
     set_smem_attr<64>();
     cfg.dynamicSmemBytes = mma_smem<64>();
-    return cudaLaunchKernelEx(&cfg, k_decode_mma<64>, a);
+    return a.shared ? cudaLaunchKernelEx(&cfg, k_decode_mma<64, true>, a)
+                    : cudaLaunchKernelEx(&cfg, k_decode_mma<64, false>, a);
   }
   set_smem_attr<128>();
   cfg.dynamicSmemBytes = mma_smem<128>();
-  return cudaLaunchKernelEx(&cfg, k_decode_mma<128>, a);
+  return a.shared ? cudaLaunchKernelEx(&cfg, k_decode_mma<128, true>, a)
+                  : cudaLaunchKernelEx(&cfg, k_decode_mma<128, false>, a);
 }
 
 int decode_mma_blocks_per_sm(int d) {
   int n = 0;
   if (d == 64) {
     set_smem_attr<64>();
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_mma<64>, kThreads, mma_smem<64>());
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_mma<64, false>, kThreads, mma_smem<64>());
   } else {
     set_smem_attr<128>();
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_mma<128>, kThreads, mma_smem<128>());
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_mma<128, false>, kThreads, mma_smem<128>());
   }
   return n;
 }

@@ -19,6 +19,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <queue>
 #include <string>
 #include <unordered_map>
@@ -36,7 +37,9 @@ struct Interval { int64_t a, b; };        // half-open
 struct Run { int64_t slot0, log0, len; }; // slots [slot0, slot0+len) hold logical [log0, ...)
 
 constexpr int kStages = 32;
-constexpr int kMaxItems = 4096;            // decode work items per call
+constexpr int kMaxItems = 4096;            // decode work items (and partial slots) per call
+constexpr int kMaxMembers = 16384;         // members of shared decode items per call
+constexpr int kMinSharedPages = 4;         // shorter runs of common pages are read per row
 
 // 128-bit key of an operation history: two independent 64-bit chains, each
 // step finished with the MurmurHash3 64-bit finaliser (Appleby).
@@ -67,6 +70,8 @@ struct HostSeq {
   bool gather_identity = true;     // last reposition moved nothing
   HKey key;
   bool frozen = false;             // snapshot of a published prefix entry
+  int64_t family = 0;              // pages are shared only within a family: a created
+                                   // sequence starts one, forks inherit it
 };
 
 struct Stage { char* h = nullptr; char* d = nullptr; cudaEvent_t ev = nullptr; bool used = false; };
@@ -168,6 +173,10 @@ struct akv_cache {
     int32_t window = -1;
     int items = 0;
     bool combine = false;
+    bool shared = false;      // has items whose pages several rows read
+    int shared_items = 0;
+    int members = 0;
+    size_t o_members = 0;
     uint64_t used = 0;
   };
   static constexpr int kPlans = 4;
@@ -189,6 +198,9 @@ struct akv_cache {
   bool use_mma = false;
   int mma_blocks_per_sm = 0;
   int32_t decode_waves = 1;
+  int32_t decode_share = 1;        // rows holding the same pages read them once (0 off,
+                                   // 1 automatic, else the most rows per item)
+  int32_t last_items = 0, last_shared = 0, last_members = 0;   // plan of the last decode call
   int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
   void* d_restore = nullptr;       // temporary key/value versions of restore attention
   size_t restore_cap = 0;
@@ -404,7 +416,8 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   CKC(cudaMalloc(&c->d_part_ml, (size_t)kMaxItems * f.hq * sizeof(float2)));
   CKC(cudaMalloc(&c->d_err, sizeof(uint32_t)));
   CKC(cudaMemset(c->d_err, 0, sizeof(uint32_t)));
-  c->plan_cap = kMaxItems * sizeof(DecodeItem) + 2 * ns * sizeof(int32_t) + 64;
+  c->plan_cap = kMaxItems * sizeof(DecodeItem) + 2 * ns * sizeof(int32_t) +
+                kMaxMembers * sizeof(DecodeMember) + 64;
   for (auto& pl : c->plans) CKC(cudaMalloc(&pl.d, c->plan_cap));
   c->stage_bytes = std::max<size_t>(1 << 20, 8 * (size_t)f.max_pages + 96 * ns +
                                                  kMaxItems * sizeof(DecodeItem) + 65536);
@@ -452,6 +465,7 @@ int akv_seq_create(akv_cache* c, int64_t* seq) {
   s.dslot = c->free_dslots.back();
   c->free_dslots.pop_back();
   const int64_t id = c->next_id++;
+  s.family = id;
   c->seqs.emplace(id, std::move(s));
   ++c->epoch;
   *seq = id;
@@ -829,6 +843,149 @@ int akv_reposition(akv_cache* c, const int64_t* seqs, int32_t n_seqs) {
 
 // ---- decode ------------------------------------------------------------------
 
+namespace {
+
+struct ActivePage { int32_t kidx, page; uint64_t mask; };
+
+// A sequence's active slot pages in ascending order (the device's active
+// list), each with its pool page and the keep bits of its slots.
+void active_pages(const HostSeq& sq, int S, std::vector<ActivePage>* out) {
+  out->clear();
+  for (const Interval& iv : sq.alive)
+    for (int64_t k = iv.a / S; k * S < iv.b; ++k) {
+      const int64_t lo = std::max(iv.a, k * S) - k * S, hi = std::min(iv.b, (k + 1) * S) - k * S;
+      const uint64_t bits = (hi - lo >= 64 ? ~0ULL : ((1ULL << (hi - lo)) - 1)) << lo;
+      if (!out->empty() && out->back().kidx == k) out->back().mask |= bits;
+      else out->push_back({(int32_t)k, sq.pages[k], bits});
+    }
+}
+
+// A range of one row's active list that the decode reads for one or more
+// rows: `rows` are the members (rows[0] is the row whose active list
+// [a0, a1) the kernel walks); member k holds the same pool pages at the same
+// slot pages with the same keep bits over the first lens[k] pages of it.
+struct Segment {
+  int32_t a0, a1;
+  std::vector<int32_t> rows, lens;
+  int32_t ns = 1;
+};
+
+// Shared segments: walking the rows in order, an active page that other rows
+// hold identically (same pool page, slot page and keep bits) and that none
+// of them has read yet starts a segment.  Each such row joins for as long as
+// its next active pages stay identical (at consecutive places of both
+// lists); rows that stay fewer than kMinSharedPages pages read privately.
+// The members are then taken longest first in chunks of at most `cap`, each
+// chunk a segment walked along its longest member's list.  Every page not
+// covered this way is read per row.
+void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap,
+                   std::vector<Segment>* segs) {
+  const int n = (int)hs.size(), S = c->cfg.page_size;
+  std::vector<std::vector<ActivePage>> ap(n);
+  std::vector<std::vector<int32_t>> gid(n);        // entry -> group of >= 2 rows, or -1
+  std::vector<std::vector<char>> covered(n);
+  struct Key {
+    int32_t page, kidx; uint64_t mask;
+    bool operator==(const Key& o) const { return page == o.page && kidx == o.kidx && mask == o.mask; }
+  };
+  struct KeyHash {
+    size_t operator()(const Key& k) const {
+      return std::hash<uint64_t>()(((uint64_t)(uint32_t)k.page << 32 | (uint32_t)k.kidx) ^
+                                   (k.mask * 0x9E3779B97F4A7C15ULL));
+    }
+  };
+  std::unordered_map<Key, int32_t, KeyHash> index;
+  std::vector<std::vector<std::pair<int32_t, int32_t>>> groups;   // (row, active index)
+  bool any = false;
+  for (int i = 0; i < n; ++i) {
+    active_pages(*hs[i], S, &ap[i]);
+    gid[i].assign(ap[i].size(), -1);
+    covered[i].assign(ap[i].size(), 0);
+    if ((int64_t)ap[i].size() != hs[i]->n_active_pages) continue;   // never share then
+    for (int32_t a = 0; a < (int32_t)ap[i].size(); ++a) {
+      const ActivePage& e = ap[i][a];
+      if (e.page < 0 || c->refcnt[e.page] < 2) continue;
+      auto it = index.emplace(Key{e.page, e.kidx, e.mask}, (int32_t)groups.size());
+      if (it.second) groups.emplace_back();
+      groups[it.first->second].push_back({i, a});
+      gid[i][a] = it.first->second;
+      any |= groups[it.first->second].size() > 1;
+    }
+  }
+  if (any) {
+    struct Cand { int32_t row, start, len; };
+    std::vector<Cand> cand;
+    for (int i = 0; i < n; ++i)
+      for (int32_t a = 0; a < (int32_t)ap[i].size();) {
+        const int32_t g0 = gid[i][a];
+        if (g0 < 0 || covered[i][a] || groups[g0].size() < 2) { ++a; continue; }
+        // how long each other row that holds this page stays identical
+        cand.clear();
+        int32_t longest = 0;
+        for (const auto& m : groups[g0]) {
+          if (m.first == i || covered[m.first][m.second]) continue;
+          const int j = m.first;
+          int32_t len = 0;
+          while (a + len < (int32_t)ap[i].size() && m.second + len < (int32_t)ap[j].size() &&
+                 gid[i][a + len] >= 0 && gid[i][a + len] == gid[j][m.second + len] &&
+                 !covered[i][a + len] && !covered[j][m.second + len])
+            ++len;
+          if (len >= kMinSharedPages) {
+            cand.push_back({j, m.second, len});
+            longest = std::max(longest, len);
+          }
+        }
+        if (cand.empty()) { ++a; continue; }
+        cand.push_back({i, a, longest});
+        std::stable_sort(cand.begin(), cand.end(),
+                         [](const Cand& x, const Cand& y) { return x.len > y.len; });
+        const int nm = (int)cand.size(), nch = (nm + cap - 1) / cap;
+        for (int ch = 0, k0 = 0; ch < nch; ++ch) {
+          const int k1 = k0 + (nm - k0 + (nch - ch) - 1) / (nch - ch);
+          Segment sg;
+          sg.a0 = cand[k0].start;
+          sg.a1 = sg.a0 + cand[k0].len;
+          for (int k = k0; k < k1; ++k) {
+            sg.rows.push_back(cand[k].row);
+            sg.lens.push_back(cand[k].len);
+            for (int32_t t = 0; t < cand[k].len; ++t) covered[cand[k].row][cand[k].start + t] = 1;
+          }
+          segs->push_back(std::move(sg));
+          k0 = k1;
+        }
+        a += longest;
+      }
+  }
+  // everything else, per row: maximal uncovered ranges (a row with no
+  // active page still gets one empty segment for its output)
+  for (int i = 0; i < n; ++i) {
+    const int32_t na = hs[i]->n_active_pages;
+    bool any_seg = false;
+    for (int32_t a = 0; a < na;) {
+      if (a < (int32_t)covered[i].size() && covered[i][a]) { ++a; any_seg = true; continue; }
+      int32_t b = a + 1;
+      while (b < na && !(b < (int32_t)covered[i].size() && covered[i][b])) ++b;
+      Segment sg;
+      sg.a0 = a;
+      sg.a1 = b;
+      sg.rows = {i};
+      sg.lens = {b - a};
+      segs->push_back(std::move(sg));
+      any_seg = true;
+      a = b;
+    }
+    if (!any_seg) {
+      Segment sg;
+      sg.a0 = sg.a1 = 0;
+      sg.rows = {i};
+      sg.lens = {0};
+      segs->push_back(std::move(sg));
+    }
+  }
+}
+
+}  // namespace
+
 int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64_t* seqs,
                          int32_t n_seqs, float* out) {
   if (!c || n_seqs < 0 || (n_seqs > 0 && (!seqs || !q || !out))) return AKV_EINVAL;
@@ -857,8 +1014,9 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       total += hs[i]->n_active_pages - first[i];
     }
     std::vector<DecodeItem> items;
+    std::vector<DecodeMember> members;
     std::vector<int32_t> item0(n_seqs), splits(n_seqs);
-    bool combine = false;
+    bool combine = false, shared = false;
     auto emit = [&](int i, int32_t ns, bool even) {
       const HostSeq* sq = hs[i];
       const int64_t f0 = first[i], na = sq->n_active_pages - f0;
@@ -876,46 +1034,155 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
         it.n_splits = ns;
         it.item0 = item0[i];
         it.win_lo = win_lo[i];
+        it.part = (int32_t)items.size();
+        it.nb = 1;
         items.push_back(it);
       }
     };
     if (c->use_mma) {
-      // Tensor-core path: blocks for a quarter of what fits the GPU at once
-      // (times decode_waves), the splits of each sequence proportional to its
-      // pages to read and equal within it; one split holds at most
-      // kDecodeMaxTiles tiles.  Leaving most block slots free lets the next
-      // decode call's blocks start while this call runs (programmatic
-      // dependent launch): back to back, a quarter wave beat a whole wave by
-      // 2-45% depending on the batch.
+      // Tensor-core path: the work is a list of segments (ranges of one
+      // row's active pages, read for one row or for several rows that hold
+      // them identically); blocks for a quarter of what fits the GPU at once
+      // (times decode_waves), the splits of each segment proportional to its
+      // pages and equal within it; one split holds at most kDecodeMaxTiles
+      // tiles.  Leaving most block slots free lets the next decode call's
+      // blocks start while this call runs (programmatic dependent launch):
+      // back to back, a quarter wave beat a whole wave by 2-45% depending on
+      // the batch.
       const int64_t tpp = c->cfg.page_size / 16;
-      const int64_t resident = (int64_t)c->sm_count * c->mma_blocks_per_sm;
-      const int64_t quarter = std::max<int64_t>(1, resident / 4);
-      const int64_t pairs = (int64_t)n_seqs * c->cfg.hkv;
-      const int64_t waves = std::max<int64_t>(c->decode_waves, (pairs + quarter - 1) / quarter);
-      int64_t target = std::max<int64_t>(n_seqs, waves * quarter / c->cfg.hkv);
-      std::vector<int32_t> ns(n_seqs);
-      int64_t sum = 0;
-      using Entry = std::pair<int64_t, int>;        // (pages per split, seq)
-      std::priority_queue<Entry> pq;
-      for (int i = 0; i < n_seqs; ++i) {
-        const int64_t na = hs[i]->n_active_pages - first[i];
-        ns[i] = (int32_t)std::max<int64_t>(1, (na * tpp + kDecodeMaxTiles - 1) / kDecodeMaxTiles);
-        sum += ns[i];
-        pq.push({(na + ns[i] - 1) / ns[i], i});
+      const int G = c->cfg.hq / c->cfg.hkv;
+      std::vector<Segment> segs;
+      auto plan_mma = [&](bool share) -> int {
+        segs.clear();
+        if (share) {
+          // automatic: at most two column blocks (16 columns) per item; with
+          // four, every consumer warp reads every tile and the item runs at
+          // the latency of one warp's tile chain
+          const int cap = c->decode_share > 1 ? c->decode_share : std::max(1, 16 / G);
+          plan_segments(c, hs, std::min(kDecodeMaxMembers, std::min(cap, 32 / G)), &segs);
+        } else {
+          for (int i = 0; i < n_seqs; ++i) {
+            Segment sg;
+            sg.a0 = first[i];
+            sg.a1 = hs[i]->n_active_pages;
+            sg.rows = {i};
+            sg.lens = {sg.a1 - sg.a0};
+            segs.push_back(std::move(sg));
+          }
+        }
+        const int64_t resident = (int64_t)c->sm_count * c->mma_blocks_per_sm;
+        const int64_t quarter = std::max<int64_t>(1, resident / 4);
+        const int64_t pairs = (int64_t)segs.size() * c->cfg.hkv;
+        const int64_t waves = std::max<int64_t>(c->decode_waves, (pairs + quarter - 1) / quarter);
+        int64_t target = std::max<int64_t>((int64_t)segs.size(), waves * quarter / c->cfg.hkv);
+        // A consumer warp of an item with nb column blocks reads nb/4 of the
+        // tiles (one row: a quarter), so the work of a split, the cap of
+        // kDecodeMaxTiles tiles for a one-row split and the balancing all
+        // count pages * nb.
+        auto nb_of = [&](const Segment& sg) -> int64_t {
+          const int cols = ((int)sg.rows.size() * G + 7) / 8;
+          return sg.rows.size() < 2 || cols <= 1 ? 1 : cols <= 2 ? 2 : 4;
+        };
+        int64_t sum = 0, parts = 0;
+        using Entry = std::pair<int64_t, int>;        // (work per split, segment)
+        std::priority_queue<Entry> pq;
+        for (int k = 0; k < (int)segs.size(); ++k) {
+          const int64_t w = (segs[k].a1 - segs[k].a0) * nb_of(segs[k]);
+          segs[k].ns = (int32_t)std::max<int64_t>(1, (w * tpp + kDecodeMaxTiles - 1) / kDecodeMaxTiles);
+          segs[k].ns = (int32_t)std::min<int64_t>(segs[k].ns, std::max<int64_t>(1, segs[k].a1 - segs[k].a0));
+          sum += segs[k].ns;
+          parts += (int64_t)segs[k].ns * segs[k].rows.size();
+          pq.push({(w + segs[k].ns - 1) / segs[k].ns, k});
+        }
+        target = std::min<int64_t>(std::max(target, sum), kMaxItems);
+        while (sum < target && !pq.empty()) {
+          Entry e = pq.top();
+          pq.pop();
+          Segment& sg = segs[e.second];
+          const int64_t na = sg.a1 - sg.a0;
+          if ((na + sg.ns - 1) / sg.ns <= 2) break;     // splits of 1-2 pages gain nothing
+          if (parts + (int64_t)sg.rows.size() > kMaxItems) continue;
+          ++sg.ns;
+          ++sum;
+          parts += sg.rows.size();
+          pq.push({(na * nb_of(sg) + sg.ns - 1) / sg.ns, e.second});
+        }
+        if (sum > kMaxItems || parts > kMaxItems) return AKV_ECAPACITY;
+        // the members of split k of a segment: those whose part reaches
+        // into it; a row's partial slots are side by side
+        auto split_range = [](const Segment& sg, int32_t k, int64_t* s0, int64_t* s1) {
+          const int64_t na = sg.a1 - sg.a0;
+          *s0 = na * k / sg.ns;
+          *s1 = na * (k + 1) / sg.ns;
+        };
+        for (auto& sg : segs)
+          for (int32_t k = 0; k < sg.ns; ++k) {
+            int64_t s0, s1;
+            split_range(sg, k, &s0, &s1);
+            for (size_t m = 0; m < sg.rows.size(); ++m)
+              if (m == 0 || sg.lens[m] > s0) ++splits[sg.rows[m]];
+          }
+        std::vector<int32_t> cursor(n_seqs, 0);
+        for (int i = 0, acc = 0; i < n_seqs; ++i) {
+          item0[i] = acc;
+          acc += splits[i];
+        }
+        items.clear();
+        members.clear();
+        shared = false;
+        for (auto& sg : segs) {
+          const int r0 = sg.rows[0];
+          for (int32_t k = 0; k < sg.ns; ++k) {
+            int64_t s0, s1;
+            split_range(sg, k, &s0, &s1);
+            int nm = 0;
+            for (size_t m = 0; m < sg.rows.size(); ++m) nm += m == 0 || sg.lens[m] > s0;
+            DecodeItem it{};
+            it.dslot = hs[r0]->dslot;
+            it.row = r0;
+            it.p0 = (int32_t)(sg.a0 + s0);
+            it.p1 = (int32_t)(sg.a0 + s1);
+            it.pos_q = (int32_t)(hs[r0]->n_slots - 1);
+            it.n_splits = splits[r0];
+            it.item0 = item0[r0];
+            it.win_lo = win_lo[r0];
+            it.part = item0[r0] + cursor[r0];
+            const int cols = (nm * G + 7) / 8;
+            it.nb = cols <= 1 ? 1 : cols <= 2 ? 2 : 4;
+            if (nm > 1) {
+              if (members.size() + nm > (size_t)kMaxMembers) return AKV_ECAPACITY;
+              it.mem0 = (int32_t)members.size();
+              it.n_mem = nm;
+              for (size_t m = 0; m < sg.rows.size(); ++m) {
+                if (m > 0 && sg.lens[m] <= s0) continue;
+                const int32_t r = sg.rows[m];
+                const int64_t pages = std::min<int64_t>(sg.lens[m], s1) - s0;
+                members.push_back(DecodeMember{r, (int32_t)(hs[r]->n_slots - 1), item0[r], splits[r],
+                                               item0[r] + cursor[r]++, (int32_t)(pages * tpp)});
+              }
+              shared = true;
+            } else {
+              ++cursor[r0];
+            }
+            items.push_back(it);
+          }
+        }
+        return AKV_OK;
+      };
+      // rows can hold the same pages only within a fork family
+      bool share = c->decode_share > 0 && window == 0 && n_seqs > 1;
+      if (share) {
+        std::vector<int64_t> fam(n_seqs);
+        for (int i = 0; i < n_seqs; ++i) fam[i] = hs[i]->family;
+        std::sort(fam.begin(), fam.end());
+        share = std::adjacent_find(fam.begin(), fam.end()) != fam.end();
       }
-      target = std::min<int64_t>(std::max(target, sum), kMaxItems);
-      while (sum < target && !pq.empty()) {
-        Entry e = pq.top();
-        pq.pop();
-        if (e.first <= 2) break;                      // splits of 1-2 pages gain nothing
-        const int i = e.second;
-        ++ns[i];
-        ++sum;
-        const int64_t na = hs[i]->n_active_pages - first[i];
-        pq.push({(na + ns[i] - 1) / ns[i], i});
+      int rc = plan_mma(share);
+      if (rc && share) {
+        std::fill(splits.begin(), splits.end(), 0);
+        rc = plan_mma(false);
       }
-      if (sum > kMaxItems) return fail(c, AKV_ECAPACITY, "decode needs %lld work items", (long long)sum);
-      for (int i = 0; i < n_seqs; ++i) emit(i, ns[i], true);
+      if (rc) return fail(c, AKV_ECAPACITY, "decode needs more than %d work items", kMaxItems);
       combine = false;                                 // merged inside the kernel
     } else {
       // split so that the (item, kv head) blocks fill the GPU a few times over
@@ -936,12 +1203,12 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
     blob.put(items.data(), items.size());
     blob.put(item0.data(), item0.size());
     blob.put(splits.data(), splits.size());
+    const size_t o_members = blob.put(members.data(), members.size());
     if (blob.b.size() > c->plan_cap) return fail(c, AKV_ECAPACITY, "decode plan too large");
     plan = &c->plans[0];
     for (auto& pl : c->plans)
       if (pl.used < plan->used) plan = &pl;
-    char* d = nullptr;
-    int rc = upload(c, blob, plan->d, &d);
+    int rc = upload_large(c, blob, plan->d);
     if (rc) {
       plan->epoch = ~0ULL;
       return rc;
@@ -951,8 +1218,16 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
     plan->seqs.assign(seqs, seqs + n_seqs);
     plan->items = (int)items.size();
     plan->combine = combine;
+    plan->shared = shared;
+    plan->members = (int)members.size();
+    plan->shared_items = 0;
+    for (const DecodeItem& it : items) plan->shared_items += it.n_mem > 0;
+    plan->o_members = o_members;
   }
   plan->used = ++c->plan_clock;
+  c->last_items = plan->items;
+  c->last_shared = plan->shared_items;
+  c->last_members = plan->members;
   const size_t n_items = (size_t)plan->items;
   const size_t o_item0 = (n_items * sizeof(DecodeItem) + 15) & ~size_t(15);
   const size_t o_splits = (o_item0 + n_seqs * sizeof(int32_t) + 15) & ~size_t(15);
@@ -977,6 +1252,10 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   a.n_rows = n_seqs;
   a.max_seqs = c->cfg.max_seqs;
   a.counter_rows = kMaxItems;
+  a.part_cap = kMaxItems;
+  a.members = reinterpret_cast<const DecodeMember*>(plan->d + plan->o_members);
+  a.n_members = plan->members;
+  a.shared = plan->shared;
   CK(launch_decode(a, plan->combine, n_seqs, reinterpret_cast<const int32_t*>(plan->d + o_item0),
                    reinterpret_cast<const int32_t*>(plan->d + o_splits), c->stream));
   c->launches += plan->combine ? 2 : 1;
@@ -1250,6 +1529,7 @@ int akv_prefix_fork(akv_cache* c, akv_prefix_index* x, const akv_op* ops, int32_
 
   // plan the new sequence
   HostSeq s;
+  s.family = E->family;
   s.pages.assign((size_t)n_pages, -1);
   std::vector<int32_t> fresh = peek_pages(c, n_fresh);
   size_t fi = 0;
@@ -1490,6 +1770,21 @@ int akv_set_decode_waves(akv_cache* c, int32_t waves) {
   if (!c || waves < 1 || waves > 64) return AKV_EINVAL;
   c->decode_waves = waves;
   for (auto& pl : c->plans) pl.epoch = ~0ULL;   // re-plan on the next call
+  return AKV_OK;
+}
+
+int akv_set_decode_sharing(akv_cache* c, int32_t mode) {
+  if (!c || mode < 0 || mode > kDecodeMaxMembers) return AKV_EINVAL;
+  c->decode_share = mode;
+  for (auto& pl : c->plans) pl.epoch = ~0ULL;   // re-plan on the next call
+  return AKV_OK;
+}
+
+int akv_decode_plan_stats(akv_cache* c, int32_t* items, int32_t* shared_items, int32_t* members) {
+  if (!c || !items || !shared_items || !members) return AKV_EINVAL;
+  *items = c->last_items;
+  *shared_items = c->last_shared;
+  *members = c->last_members;
   return AKV_OK;
 }
 

@@ -88,7 +88,19 @@ struct DecodeItem {
   int32_t n_splits;     // splits of this row
   int32_t item0;        // first item of this row
   int32_t win_lo;       // sliding window: slots below are not read (0 = none)
+  // tensor-core path: this item's partial slot; the row's partials are
+  // [item0, item0 + n_splits)
+  int32_t part;
+  // pages shared by several rows: members [mem0, mem0 + n_mem) of
+  // DecodeArgs::members read the range once (n_mem 0: the item's own row);
+  // nb = blocks of 8 head columns (1, 2 or 4)
+  int32_t mem0, n_mem, nb;
 };
+// one row of a shared item: the query's row and position, the row's partial
+// slots [item0, item0 + n_splits), this item's slot among them, and the
+// item's leading tiles that hold the row's pages (its columns see no others)
+struct DecodeMember { int32_t row, pos_q, item0, n_splits, part, n_tiles; };
+constexpr int kDecodeMaxMembers = 16;
 
 struct DecodeArgs {
   CUtensorMap tm_k;     // TMA maps over the pools (tensor-core path only)
@@ -111,6 +123,10 @@ struct DecodeArgs {
   int32_t n_rows;       // rows of q / out in this call
   int32_t max_seqs;     // device rows of the per-sequence arrays
   int32_t counter_rows; // rows of `counters`
+  int32_t part_cap;     // partial slots of part_acc / part_ml
+  const DecodeMember* members;   // shared items (tensor-core path)
+  int32_t n_members;
+  int32_t shared;       // the plan has shared items
 };
 constexpr int kDecodeMaxTiles = 512;   // 16-token tiles in one split of the tensor-core path
 // bound of the waits that let a kernel's own copies / MMAs land before it

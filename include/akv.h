@@ -307,6 +307,25 @@ int akv_sync_errors(akv_cache* cache, uint32_t* word);
  * call's blocks to start early; 1..64). */
 int akv_set_decode_waves(akv_cache* cache, int32_t waves);
 
+/* Tuning: in a decode call, rows that hold the same pool pages at the same
+ * slot pages with the same keep bits (branches forked from one prefix:
+ * "Cache Engineering for Agents" paper review, 3.2, copy-on-write branches)
+ * may read those pages once for all of them, as one tensor-core work item
+ * whose query columns are the rows' GQA groups side by side (runs of at
+ * least 4 such pages).  mode 0 = every row reads its own pages; 1 (default)
+ * = automatic (up to 32 / (hq/hkv) rows per item); 2..16 = at most that many
+ * rows per item.  The split boundaries differ between plans, and the
+ * softmax weights are rounded to bf16 against each split's running maximum,
+ * so results differ by bf16 roundings of those weights.  Applies to
+ * full-attention layers of the tensor-core decode; AKV_EINVAL for other
+ * values. */
+int akv_set_decode_sharing(akv_cache* cache, int32_t mode);
+
+/* The plan of the most recent decode call: work items, items read for
+ * several rows, and the rows of those items (host values; no GPU work). */
+int akv_decode_plan_stats(akv_cache* cache, int32_t* items, int32_t* shared_items,
+                          int32_t* members);
+
 /* Kernel choice for akv_restore_attention: 1 (default) = tensor-core
  * kernel where it applies (bf16 pool, D 64 or 128), 0 = the CUDA-core
  * kernel for every shape.  Both compute the same attention. */

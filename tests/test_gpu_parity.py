@@ -450,6 +450,67 @@ def test_copy_on_write_isolation():
     assert used == 0 and free == 512
 
 
+@pytest.mark.parametrize("G,D,n_kids", [(4, 128, 19), (8, 128, 9), (2, 64, 20), (1, 64, 18),
+                                         (4, 64, 37)])
+def test_branches_share_pages_in_decode(G, D, n_kids):
+    """Branches forked from one prefix hold the same pages: a decode call
+    reads them once for all rows that hold them identically (shared work
+    items, several chunks of members when there are many branches).  Every
+    row must still get exactly its own attention, including rows whose keep
+    bits on a shared page differ (dropped without reposition), rows that
+    repositioned (kept leading pages stay shared), rows that copied the tail
+    on append, and the partly filled shared tail page."""
+    hkv = 2
+    t = Twin(layers=2, hq=hkv * G, hkv=hkv, head_dim=D, page_size=16, dtype="bf16",
+             rope_theta=5e5 if D == 128 else 1e4, max_pages=4096, max_seqs=n_kids + 4,
+             max_slots=2048, seed=11)
+    root = t.create()
+    t.append([root], [1000])                    # 62 full pages and a partly filled tail
+    kids = [t.fork(root) for _ in range(n_kids)]
+    rng = np.random.default_rng(G * 100 + D)
+    for i, k in enumerate(kids):
+        kind = i % 5
+        if kind == 1:                            # keep bits differ on a few shared pages
+            b = int(rng.integers(200, 700))
+            t.drop(k, [(b, b + int(rng.integers(1, 60)))])
+        elif kind == 2:                          # leading pages stay shared
+            b = int(rng.integers(300, 900))
+            t.drop(k, [(b, b + int(rng.integers(20, 90)))])
+            t.reposition([k])
+        elif kind == 3:                          # tail copied on write
+            t.append([k], [int(rng.integers(1, 40))])
+    rows = [root] + kids + [kids[0]]             # the same sequence twice is allowed
+    t.decode(rows, 0)
+    st = t.gpu.decode_plan_stats()
+    assert st["shared_items"] > 0 and st["members"] > 0, st
+    # without sharing: against the oracle too, and close to the shared plan
+    # (the softmax weights are rounded to bf16 against each split's running
+    # maximum, so other split boundaries move the result by bf16 roundings)
+    t.gpu.set_decode_sharing(False)
+    t.decode(rows, 0)
+    assert t.gpu.decode_plan_stats()["shared_items"] == 0
+    outs = []
+    for share in (True, False):
+        t.gpu.set_decode_sharing(share)
+        q = torch.randn(len(rows), t.hq, D, generator=torch.Generator().manual_seed(5))
+        outs.append(t.gpu.decode_attention(1, q.to(torch.bfloat16).cuda(), rows).cpu())
+    diff = (outs[0] - outs[1]).abs()
+    assert diff.max() <= 1e-2 and diff.mean() <= 1e-3, (diff.max(), diff.mean())
+    t.gpu.set_decode_sharing(True)
+    # an output buffer that is only 4-byte aligned gets the same bits
+    q = torch.randn(len(rows), t.hq, D, generator=torch.Generator().manual_seed(5))
+    q = q.to(torch.bfloat16).cuda()
+    flat = torch.empty(len(rows) * t.hq * D + 1, dtype=torch.float32, device="cuda")
+    odd = flat[1:].view(len(rows), t.hq, D)
+    t.gpu.decode_attention(1, q, rows, odd)
+    assert torch.equal(odd.cpu(), outs[0])
+    t.append(rows[:-1], [1] * (len(rows) - 1))   # every row copies its tail
+    t.decode(rows[:-1], 1)
+    assert t.gpu.decode_plan_stats()["shared_items"] > 0
+    for s in rows[:-1]:
+        t.check(s)
+
+
 def test_errors_leave_state_unchanged():
     t = Twin(layers=1, hq=4, hkv=2, head_dim=64, page_size=16, dtype="bf16",
              rope_theta=1e4, max_pages=16, max_seqs=2, max_slots=400)
