@@ -773,11 +773,13 @@ def kernels_arm(args):
             torch.cuda.synchronize()
             del keep
 
-    def measure(name, cache, sh, bases, drops, seed, note, decode_steps=2):
+    def measure(name, cache, sh, bases, drops, seed, note, decode_steps=2, sharing=None):
         """Fork the prepared sequences, drop, time one batched reposition and
         decode_steps x (append + decode on every layer); repeated args.steps
-        times after args.warmup."""
+        times after args.warmup.  sharing: decode sharing mode (None: default)."""
         st = cache.stream
+        if sharing is not None:
+            cache.set_decode_sharing(sharing)
         L, Hq, H, D = sh.layers, sh.hq, sh.hkv, sh.head_dim
         w = synth.width_for(sh.dtype)
         B = len(bases)
@@ -830,8 +832,10 @@ def kernels_arm(args):
             "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
             "data": "synthetic (seeded SplitMix64 K/V/q, seeded trace structure)",
             "config": {"workload": note, "batch": B, "layers": L, "heads": f"{Hq}/{H}",
-                       "head_dim": D, "decode_steps_timed": decode_steps},
+                       "head_dim": D, "decode_steps_timed": decode_steps,
+                       "decode_sharing": {None: "default (on)", 0: "off", 1: "on"}.get(sharing, sharing)},
             "decode": {"avg_call_us": round(float(np.mean(dec_ms)) * 1e3, 2),
+                       "plan": cache.decode_plan_stats(),
                        "algorithmic_bytes_per_call": int(np.mean(dec_bytes)),
                        "gbs": round(dgbs, 1), "frac": round(dgbs / peak, 4),
                        "unique_page_bytes_per_call": int(np.mean(dec_ubytes)),
@@ -878,10 +882,27 @@ def kernels_arm(args):
                     else:
                         cache.reposition([k])
                 kids.append(k)
-            measure(name, cache, sh, kids, [None] * NB, seed,
-                    f"{sh.name}-shaped: one {P}-token prefix forked into {NB} of the 64 branches "
-                    "(1-6 drop / reposition operations each); every branch's last reposition "
-                    "batched and timed, then batched decode over the branches")
+            for sharing in (0, 1):
+                measure(name, cache, sh, kids, [None] * NB, seed,
+                        f"{sh.name}-shaped: one {P}-token prefix forked into {NB} of the 64 "
+                        "branches (1-6 drop / reposition operations each); every branch's last "
+                        "reposition batched and timed, then batched decode over the branches",
+                        sharing=sharing)
+        elif name == "branching_fork":
+            # the same workload at the moment of the fork, before any branch
+            # operation: all 64 branches hold every page of the prefix
+            sh, seed, P, NB = traces.LLAMA8B, traces.seed_for(3), 16384, 64
+            mp = P // 16 + 2 * NB + 512
+            cache = Cache(sh.layers, sh.hq, sh.hkv, sh.head_dim, sh.page_size, sh.dtype, mp,
+                          2 * NB + 4, P + 64, sh.rope_theta)
+            root = cache.seq_create()
+            append(cache, root, 1, 0, P, sh, seed)
+            kids = [cache.seq_fork(root) for _ in range(NB)]
+            for sharing in (0, 1):
+                measure(name, cache, sh, kids, [None] * NB, seed,
+                        f"{sh.name}-shaped: one {P}-token prefix forked into {NB} branches, "
+                        "decoded before any branch operation (every prefix page shared by "
+                        "all branches; the reposition is a no-op)", sharing=sharing)
         elif name == "llama70b":
             # turns 0..13 as scheduled, then turn 14's tool response; the timed
             # operation is turn 14's drop of the oldest tool spans + reposition
@@ -958,7 +979,7 @@ def main():
                     help="time segment-batch restore attention instead (its own line)")
     ap.add_argument("--restore-cuda-cores", action="store_true")
     ap.add_argument("--config-kernels", default=None,
-                    help="comma list of gptoss120b, branching, llama70b: decode and "
+                    help="comma list of gptoss120b, branching, branching_fork, llama70b: decode and "
                          "reposition bandwidth on those workloads (one line each)")
     ap.add_argument("--prefix", action="store_true",
                     help="time prefix matching / forks / eviction instead (its own line)")
