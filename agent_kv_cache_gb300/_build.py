@@ -16,8 +16,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libakv.so")
 
-SOURCES = ["akv_host.cpp", "akv_kernels.cu", "akv_decode.cu", "akv_decode_mma.cu", "akv_noalloc.cu",
-           "akv_restore.cu", "akv_prefix.cpp"]
+SOURCES = ["akv_host.cpp", "akv_kernels.cu", "akv_decode.cu", "akv_decode_mma.cu",
+           "akv_decode_share.cu", "akv_noalloc.cu", "akv_restore.cu", "akv_prefix.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]

@@ -40,6 +40,9 @@ constexpr int kStages = 32;
 constexpr int kMaxItems = 4096;            // decode work items (and partial slots) per call
 constexpr int kMaxMembers = 16384;         // members of shared decode items per call
 constexpr int kMinSharedPages = 4;         // shorter runs of common pages are read per row
+constexpr int kShareRows = 128;            // query rows of a shared-prefix (tensor-core) item
+constexpr int kShareMaxMembers = 128;
+constexpr int kSharePages = 32;            // pages per shared-prefix item
 
 // 128-bit key of an operation history: two independent 64-bit chains, each
 // step finished with the MurmurHash3 64-bit finaliser (Appleby).
@@ -176,6 +179,8 @@ struct akv_cache {
     bool shared = false;      // has items whose pages several rows read
     int shared_items = 0;
     int members = 0;
+    int sitems = 0;           // tensor-core shared-prefix items
+    size_t o_sitems = 0;
     size_t o_members = 0;
     uint64_t used = 0;
   };
@@ -417,7 +422,7 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   CKC(cudaMalloc(&c->d_err, sizeof(uint32_t)));
   CKC(cudaMemset(c->d_err, 0, sizeof(uint32_t)));
   c->plan_cap = kMaxItems * sizeof(DecodeItem) + 2 * ns * sizeof(int32_t) +
-                kMaxMembers * sizeof(DecodeMember) + 64;
+                kMaxMembers * sizeof(DecodeMember) + kMaxItems * sizeof(ShareItem) + 96;
   for (auto& pl : c->plans) CKC(cudaMalloc(&pl.d, c->plan_cap));
   c->stage_bytes = std::max<size_t>(1 << 20, 8 * (size_t)f.max_pages + 96 * ns +
                                                  kMaxItems * sizeof(DecodeItem) + 65536);
@@ -877,8 +882,10 @@ struct Segment {
 // lists); rows that stay fewer than kMinSharedPages pages read privately.
 // The members are then taken longest first in chunks of at most `cap`, each
 // chunk a segment walked along its longest member's list.  Every page not
-// covered this way is read per row.
-void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap,
+// covered this way is read per row.  full_only: share only pages whose every
+// slot has been written (below the row's held slots), so that no unwritten
+// pool memory is read for another row.
+void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap, bool full_only,
                    std::vector<Segment>* segs) {
   const int n = (int)hs.size(), S = c->cfg.page_size;
   std::vector<std::vector<ActivePage>> ap(n);
@@ -905,6 +912,7 @@ void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap,
     for (int32_t a = 0; a < (int32_t)ap[i].size(); ++a) {
       const ActivePage& e = ap[i][a];
       if (e.page < 0 || c->refcnt[e.page] < 2) continue;
+      if (full_only && (int64_t)(e.kidx + 1) * S > hs[i]->n_slots) continue;
       auto it = index.emplace(Key{e.page, e.kidx, e.mask}, (int32_t)groups.size());
       if (it.second) groups.emplace_back();
       groups[it.first->second].push_back({i, a});
@@ -1015,6 +1023,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
     }
     std::vector<DecodeItem> items;
     std::vector<DecodeMember> members;
+    std::vector<ShareItem> sitems;
     std::vector<int32_t> item0(n_seqs), splits(n_seqs);
     bool combine = false, shared = false;
     auto emit = [&](int i, int32_t ns, bool even) {
@@ -1051,15 +1060,18 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       // the batch.
       const int64_t tpp = c->cfg.page_size / 16;
       const int G = c->cfg.hq / c->cfg.hkv;
-      std::vector<Segment> segs;
-      auto plan_mma = [&](bool share) -> int {
+      std::vector<Segment> segs, tsegs;   // one-row kernel / tensor-core shared-prefix kernel
+      // share: 0 none, 1 tensor-core shared-prefix items, 2 shared items of
+      // the one-row kernel (at most `mcap` rows each)
+      auto plan_mma = [&](int share, int mcap) -> int {
         segs.clear();
+        tsegs.clear();
+        sitems.clear();
         if (share) {
-          // automatic: at most two column blocks (16 columns) per item; with
-          // four, every consumer warp reads every tile and the item runs at
-          // the latency of one warp's tile chain
-          const int cap = c->decode_share > 1 ? c->decode_share : std::max(1, 16 / G);
-          plan_segments(c, hs, std::min(kDecodeMaxMembers, std::min(cap, 32 / G)), &segs);
+          std::vector<Segment> all;
+          plan_segments(c, hs, share == 1 ? std::min(kShareRows / G, kShareMaxMembers) : mcap,
+                        share == 1, &all);
+          for (auto& sg : all) (share == 1 && sg.rows.size() > 1 ? tsegs : segs).push_back(std::move(sg));
         } else {
           for (int i = 0; i < n_seqs; ++i) {
             Segment sg;
@@ -1069,6 +1081,22 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
             sg.lens = {sg.a1 - sg.a0};
             segs.push_back(std::move(sg));
           }
+        }
+        // a row read by shared-prefix items is merged by a one-row item of
+        // the one-row kernel (launched after them): give it one if needed
+        {
+          std::vector<char> has(n_seqs, 0);
+          for (auto& sg : segs) has[sg.rows[0]] = 1;
+          for (auto& sg : tsegs)
+            for (int32_t r : sg.rows)
+              if (!has[r]) {
+                Segment e;
+                e.a0 = e.a1 = 0;
+                e.rows = {r};
+                e.lens = {0};
+                segs.push_back(std::move(e));
+                has[r] = 1;
+              }
         }
         const int64_t resident = (int64_t)c->sm_count * c->mma_blocks_per_sm;
         const int64_t quarter = std::max<int64_t>(1, resident / 4);
@@ -1094,6 +1122,15 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
           parts += (int64_t)segs[k].ns * segs[k].rows.size();
           pq.push({(w + segs[k].ns - 1) / segs[k].ns, k});
         }
+        // shared-prefix items: kSharePages pages each
+        for (auto& sg : tsegs) {
+          sg.ns = (int32_t)std::max<int64_t>(1, (sg.a1 - sg.a0 + kSharePages - 1) / kSharePages);
+          parts += (int64_t)sg.ns * sg.rows.size();
+        }
+        // next to shared-prefix items the one-row items are what is left of
+        // each row (its own pages, often long): a full wave of blocks keeps
+        // the longest of them off the critical path
+        if (!tsegs.empty()) target = std::max<int64_t>(target, resident / c->cfg.hkv);
         target = std::min<int64_t>(std::max(target, sum), kMaxItems);
         while (sum < target && !pq.empty()) {
           Entry e = pq.top();
@@ -1115,13 +1152,19 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
           *s0 = na * k / sg.ns;
           *s1 = na * (k + 1) / sg.ns;
         };
-        for (auto& sg : segs)
-          for (int32_t k = 0; k < sg.ns; ++k) {
-            int64_t s0, s1;
-            split_range(sg, k, &s0, &s1);
-            for (size_t m = 0; m < sg.rows.size(); ++m)
-              if (m == 0 || sg.lens[m] > s0) ++splits[sg.rows[m]];
-          }
+        auto n_in = [&](const Segment& sg, int64_t s0) {
+          int nm = 0;
+          for (size_t m = 0; m < sg.rows.size(); ++m) nm += m == 0 || sg.lens[m] > s0;
+          return nm;
+        };
+        for (auto* list : {&segs, &tsegs})
+          for (auto& sg : *list)
+            for (int32_t k = 0; k < sg.ns; ++k) {
+              int64_t s0, s1;
+              split_range(sg, k, &s0, &s1);
+              for (size_t m = 0; m < sg.rows.size(); ++m)
+                if (m == 0 || sg.lens[m] > s0) ++splits[sg.rows[m]];
+            }
         std::vector<int32_t> cursor(n_seqs, 0);
         for (int i = 0, acc = 0; i < n_seqs; ++i) {
           item0[i] = acc;
@@ -1130,36 +1173,63 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
         items.clear();
         members.clear();
         shared = false;
+        auto add_members = [&](const Segment& sg, int64_t s0, int64_t s1) -> int {
+          for (size_t m = 0; m < sg.rows.size(); ++m) {
+            if (m > 0 && sg.lens[m] <= s0) continue;
+            if (members.size() >= (size_t)kMaxMembers) return AKV_ECAPACITY;
+            const int32_t r = sg.rows[m];
+            const int64_t pages = std::min<int64_t>(sg.lens[m], s1) - s0;
+            members.push_back(DecodeMember{r, (int32_t)(hs[r]->n_slots - 1), item0[r], splits[r],
+                                           item0[r] + cursor[r]++, (int32_t)(pages * tpp)});
+          }
+          return AKV_OK;
+        };
+        auto one_row = [&](int r0, int64_t p0, int64_t p1) {
+          DecodeItem it{};
+          it.dslot = hs[r0]->dslot;
+          it.row = r0;
+          it.p0 = (int32_t)p0;
+          it.p1 = (int32_t)p1;
+          it.pos_q = (int32_t)(hs[r0]->n_slots - 1);
+          it.n_splits = splits[r0];
+          it.item0 = item0[r0];
+          it.win_lo = win_lo[r0];
+          it.part = item0[r0] + cursor[r0];
+          it.nb = 1;
+          return it;
+        };
+        for (auto& sg : tsegs) {
+          for (int32_t k = 0; k < sg.ns; ++k) {
+            int64_t s0, s1;
+            split_range(sg, k, &s0, &s1);
+            if (n_in(sg, s0) < 2) {                      // only the first row left
+              items.push_back(one_row(sg.rows[0], sg.a0 + s0, sg.a0 + s1));
+              ++cursor[sg.rows[0]];
+              continue;
+            }
+            ShareItem si{};
+            si.dslot = hs[sg.rows[0]]->dslot;
+            si.p0 = (int32_t)(sg.a0 + s0);
+            si.p1 = (int32_t)(sg.a0 + s1);
+            si.mem0 = (int32_t)members.size();
+            if (add_members(sg, s0, s1)) return AKV_ECAPACITY;
+            si.n_mem = (int32_t)members.size() - si.mem0;
+            sitems.push_back(si);
+          }
+        }
         for (auto& sg : segs) {
           const int r0 = sg.rows[0];
           for (int32_t k = 0; k < sg.ns; ++k) {
             int64_t s0, s1;
             split_range(sg, k, &s0, &s1);
-            int nm = 0;
-            for (size_t m = 0; m < sg.rows.size(); ++m) nm += m == 0 || sg.lens[m] > s0;
-            DecodeItem it{};
-            it.dslot = hs[r0]->dslot;
-            it.row = r0;
-            it.p0 = (int32_t)(sg.a0 + s0);
-            it.p1 = (int32_t)(sg.a0 + s1);
-            it.pos_q = (int32_t)(hs[r0]->n_slots - 1);
-            it.n_splits = splits[r0];
-            it.item0 = item0[r0];
-            it.win_lo = win_lo[r0];
-            it.part = item0[r0] + cursor[r0];
+            const int nm = n_in(sg, s0);
+            DecodeItem it = one_row(r0, sg.a0 + s0, sg.a0 + s1);
             const int cols = (nm * G + 7) / 8;
             it.nb = cols <= 1 ? 1 : cols <= 2 ? 2 : 4;
             if (nm > 1) {
-              if (members.size() + nm > (size_t)kMaxMembers) return AKV_ECAPACITY;
               it.mem0 = (int32_t)members.size();
               it.n_mem = nm;
-              for (size_t m = 0; m < sg.rows.size(); ++m) {
-                if (m > 0 && sg.lens[m] <= s0) continue;
-                const int32_t r = sg.rows[m];
-                const int64_t pages = std::min<int64_t>(sg.lens[m], s1) - s0;
-                members.push_back(DecodeMember{r, (int32_t)(hs[r]->n_slots - 1), item0[r], splits[r],
-                                               item0[r] + cursor[r]++, (int32_t)(pages * tpp)});
-              }
+              if (add_members(sg, s0, s1)) return AKV_ECAPACITY;
               shared = true;
             } else {
               ++cursor[r0];
@@ -1167,6 +1237,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
             items.push_back(it);
           }
         }
+        if ((int64_t)items.size() > kMaxItems || (int64_t)sitems.size() > kMaxItems) return AKV_ECAPACITY;
         return AKV_OK;
       };
       // rows can hold the same pages only within a fork family
@@ -1177,10 +1248,12 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
         std::sort(fam.begin(), fam.end());
         share = std::adjacent_find(fam.begin(), fam.end()) != fam.end();
       }
-      int rc = plan_mma(share);
-      if (rc && share) {
+      const int mode = !share ? 0 : (c->decode_share == 1 && decode_share_supported(c->g)) ? 1 : 2;
+      const int mcap = c->decode_share > 1 ? c->decode_share : std::max(1, 16 / G);
+      int rc = plan_mma(mode, std::min(mcap, 32 / G));
+      if (rc && mode) {
         std::fill(splits.begin(), splits.end(), 0);
-        rc = plan_mma(false);
+        rc = plan_mma(0, 1);
       }
       if (rc) return fail(c, AKV_ECAPACITY, "decode needs more than %d work items", kMaxItems);
       combine = false;                                 // merged inside the kernel
@@ -1204,6 +1277,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
     blob.put(item0.data(), item0.size());
     blob.put(splits.data(), splits.size());
     const size_t o_members = blob.put(members.data(), members.size());
+    const size_t o_sitems = blob.put(sitems.data(), sitems.size());
     if (blob.b.size() > c->plan_cap) return fail(c, AKV_ECAPACITY, "decode plan too large");
     plan = &c->plans[0];
     for (auto& pl : c->plans)
@@ -1220,12 +1294,14 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
     plan->combine = combine;
     plan->shared = shared;
     plan->members = (int)members.size();
-    plan->shared_items = 0;
+    plan->shared_items = (int)sitems.size();
     for (const DecodeItem& it : items) plan->shared_items += it.n_mem > 0;
     plan->o_members = o_members;
+    plan->sitems = (int)sitems.size();
+    plan->o_sitems = o_sitems;
   }
   plan->used = ++c->plan_clock;
-  c->last_items = plan->items;
+  c->last_items = plan->items + plan->sitems;
   c->last_shared = plan->shared_items;
   c->last_members = plan->members;
   const size_t n_items = (size_t)plan->items;
@@ -1256,6 +1332,12 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   a.members = reinterpret_cast<const DecodeMember*>(plan->d + plan->o_members);
   a.n_members = plan->members;
   a.shared = plan->shared;
+  a.share_items = reinterpret_cast<const ShareItem*>(plan->d + plan->o_sitems);
+  a.n_share_items = plan->sitems;
+  if (plan->sitems > 0) {
+    CK(launch_decode_share(a, c->stream));
+    ++c->launches;
+  }
   CK(launch_decode(a, plan->combine, n_seqs, reinterpret_cast<const int32_t*>(plan->d + o_item0),
                    reinterpret_cast<const int32_t*>(plan->d + o_splits), c->stream));
   c->launches += plan->combine ? 2 : 1;

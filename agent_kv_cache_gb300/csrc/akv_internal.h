@@ -102,6 +102,16 @@ struct DecodeItem {
 struct DecodeMember { int32_t row, pos_q, item0, n_splits, part, n_tiles; };
 constexpr int kDecodeMaxMembers = 16;
 
+// shared-prefix decode on the tensor cores (page size 16): one CTA per
+// (item, KV head) computes up to 128 query rows (members x GQA heads) over a
+// range of the first member's active pages and writes every member's
+// partial; members are DecodeArgs::members, n_tiles = the member's pages
+struct ShareItem {
+  int32_t dslot;        // sequence whose active list is walked
+  int32_t p0, p1;       // its active-list range (pages)
+  int32_t mem0, n_mem;
+};
+
 struct DecodeArgs {
   CUtensorMap tm_k;     // TMA maps over the pools (tensor-core path only)
   CUtensorMap tm_v;
@@ -127,6 +137,8 @@ struct DecodeArgs {
   const DecodeMember* members;   // shared items (tensor-core path)
   int32_t n_members;
   int32_t shared;       // the plan has shared items
+  const ShareItem* share_items;   // tensor-core shared-prefix items (before the others)
+  int32_t n_share_items;
 };
 constexpr int kDecodeMaxTiles = 512;   // 16-token tiles in one split of the tensor-core path
 // bound of the waits that let a kernel's own copies / MMAs land before it
@@ -200,5 +212,9 @@ bool decode_mma_supported(const Geom& g);
 bool make_pool_tensor_maps(const Geom& g, CUtensorMap* tk, CUtensorMap* tv);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st);
 int decode_mma_blocks_per_sm(int head_dim);
+// Shared-prefix decode (akv_decode_share.cu): bf16 pools, page size 16,
+// head dim 64 / 128, GQA group <= 8.
+bool decode_share_supported(const Geom& g);
+cudaError_t launch_decode_share(const DecodeArgs& a, cudaStream_t st);
 
 }  // namespace akv

@@ -450,16 +450,18 @@ def test_copy_on_write_isolation():
     assert used == 0 and free == 512
 
 
+@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("G,D,n_kids", [(4, 128, 19), (8, 128, 9), (2, 64, 20), (1, 64, 18),
                                          (4, 64, 37)])
-def test_branches_share_pages_in_decode(G, D, n_kids):
+def test_branches_share_pages_in_decode(G, D, n_kids, mode):
     """Branches forked from one prefix hold the same pages: a decode call
-    reads them once for all rows that hold them identically (shared work
-    items, several chunks of members when there are many branches).  Every
-    row must still get exactly its own attention, including rows whose keep
-    bits on a shared page differ (dropped without reposition), rows that
-    repositioned (kept leading pages stay shared), rows that copied the tail
-    on append, and the partly filled shared tail page."""
+    reads them once for all rows that hold them identically (mode 1: the
+    tensor-core shared-prefix items of up to 128 query rows; mode 2: shared
+    items of the one-row kernel, two rows each).  Every row must still get
+    exactly its own attention, including rows whose keep bits on a shared
+    page differ (dropped without reposition), rows that repositioned (kept
+    leading pages stay shared), rows that copied the tail on append, and the
+    partly filled shared tail page."""
     hkv = 2
     t = Twin(layers=2, hq=hkv * G, hkv=hkv, head_dim=D, page_size=16, dtype="bf16",
              rope_theta=5e5 if D == 128 else 1e4, max_pages=4096, max_seqs=n_kids + 4,
@@ -480,6 +482,7 @@ def test_branches_share_pages_in_decode(G, D, n_kids):
         elif kind == 3:                          # tail copied on write
             t.append([k], [int(rng.integers(1, 40))])
     rows = [root] + kids + [kids[0]]             # the same sequence twice is allowed
+    t.gpu.set_decode_sharing(mode)
     t.decode(rows, 0)
     st = t.gpu.decode_plan_stats()
     assert st["shared_items"] > 0 and st["members"] > 0, st
@@ -490,13 +493,13 @@ def test_branches_share_pages_in_decode(G, D, n_kids):
     t.decode(rows, 0)
     assert t.gpu.decode_plan_stats()["shared_items"] == 0
     outs = []
-    for share in (True, False):
+    for share in (mode, 0):
         t.gpu.set_decode_sharing(share)
         q = torch.randn(len(rows), t.hq, D, generator=torch.Generator().manual_seed(5))
         outs.append(t.gpu.decode_attention(1, q.to(torch.bfloat16).cuda(), rows).cpu())
     diff = (outs[0] - outs[1]).abs()
     assert diff.max() <= 1e-2 and diff.mean() <= 1e-3, (diff.max(), diff.mean())
-    t.gpu.set_decode_sharing(True)
+    t.gpu.set_decode_sharing(mode)
     # an output buffer that is only 4-byte aligned gets the same bits
     q = torch.randn(len(rows), t.hq, D, generator=torch.Generator().manual_seed(5))
     q = q.to(torch.bfloat16).cuda()
@@ -504,7 +507,14 @@ def test_branches_share_pages_in_decode(G, D, n_kids):
     odd = flat[1:].view(len(rows), t.hq, D)
     t.gpu.decode_attention(1, q, rows, odd)
     assert torch.equal(odd.cpu(), outs[0])
+    # and a query that is only 2-byte aligned
+    qflat = torch.empty(q.numel() + 1, dtype=torch.bfloat16, device="cuda")
+    qodd = qflat[1:].view_as(q)
+    qodd.copy_(q)
+    got = t.gpu.decode_attention(1, qodd, rows)
+    assert torch.equal(got.cpu(), outs[0])
     t.append(rows[:-1], [1] * (len(rows) - 1))   # every row copies its tail
+    t.gpu.set_decode_sharing(mode)
     t.decode(rows[:-1], 1)
     assert t.gpu.decode_plan_stats()["shared_items"] > 0
     for s in rows[:-1]:
