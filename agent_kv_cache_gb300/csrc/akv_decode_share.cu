@@ -141,16 +141,54 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
     }
   }
 
+  const uint32_t mbS0 = smem_u32(mbar), mbO = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 3),
+                 mbV0 = smem_u32(mbar + 5), mbP0 = smem_u32(mbar + 7), mbX0 = smem_u32(mbar + 9);
+  if (control) {
+    if (lane == 0) {
+      for (int i = 0; i < 17; ++i) {
+        // P: one arrival per softmax warp; X: one per warp of the pair
+        const uint32_t cnt = (i == 7 || i == 8) ? kSoftmaxWarps : (i >= 9 ? 2 : 1);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar + i)), "r"(cnt) : "memory");
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      *s_abort = 0;
+    }
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(&tslot)), "r"(kCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  const int n_kt = (n_pages + kTilePages - 1) / kTilePages;
+  const int slab = (a.layer >= 0 ? a.layer : 0) % g.phys_layers;
+  int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1};   // control warp: copies in flight
+  // control lane 0: the four pages of tile kt into K (or V) buffer kt & 1
+  auto tma_tile = [&](int kt, bool is_k) {
+    const int b = kt & 1;
+    const uint32_t bar = (is_k ? mbK0 : mbV0) + 8 * b;
+    uint8_t* dst = (is_k ? sK : sV) + b * kBN * D * 2;
+    mbar_expect_tx(bar, KV_BYTES);
+#pragma unroll
+    for (int at = 0; at < D / 64; ++at)
+#pragma unroll
+      for (int j = 0; j < kTilePages; ++j)
+        tma_load_3d(smem_u32(dst + at * kBN * 128 + j * kPageRows * 128), is_k ? &a.tm_k : &a.tm_v,
+                    at * 64, s_prow[kt * kTilePages + j < kMaxItemPages ? kt * kTilePages + j : 0],
+                    slab, bar);
+    if (is_k) k_pend[b] = kt;
+    else v_pend[b] = kt;
+  };
+
   // rotated, scaled queries in the swizzled K-major layout; the first R dims
   // rotate in pairs (d, d + R/2), the rest are only scaled.  The raw rows
-  // are staged in the K buffers first (free until the first copy), with
-  // independent 16-byte loads; the rotation then reads them from shared
-  // memory and issues its table loads kBatch at a time.
+  // are staged in the V buffers first (free until their first copy), with
+  // independent 16-byte loads; the first two K tiles are already on their way
+  // (nothing reads the K buffers before them) while the rotation reads the
+  // staged rows and issues its table loads kBatch at a time.
   {
     const int R = g.rope, RH = R / 2;
     constexpr int kChunks = D / 8;                // 16-byte chunks of a row
     if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
-      uint4* stage = reinterpret_cast<uint4*>(sK);  // [kBM][kChunks]
+      uint4* stage = reinterpret_cast<uint4*>(sV);  // [kBM][kChunks]
       const uint4* qg = static_cast<const uint4*>(a.q);
       for (int i = tid; i < n_used * kChunks; i += kThreads) {
         const int row = i / kChunks, ch = i % kChunks;
@@ -158,7 +196,7 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
         stage[i] = qg[((int64_t)mm.row * g.hq + (int64_t)kvh * G + row % G) * kChunks + ch];
       }
     } else {                                        // the caller's q need only be 2-byte aligned
-      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sK);
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sV);
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
       for (int i = tid; i < n_used * D; i += kThreads) {
         const int row = i / D, d = i % D;
@@ -166,10 +204,14 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
         stage[i] = qg[((int64_t)mm.row * g.hq + (int64_t)kvh * G + row % G) * D + d];
       }
     }
-    __syncthreads();
+    __syncthreads();   // staged rows, page rows and the barriers' initialisation are visible
+    if (control && lane == 0 && n_kt > 0) {
+      tma_tile(0, true);
+      if (n_kt > 1) tma_tile(1, true);
+    }
     // one (member, pair) per step: one table load, then the member's G
     // heads; kBatch steps' loads are in flight together
-    const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(sK);
+    const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(sV);
     constexpr int kBatch = 8;
     auto put = [&](int row, int dx, float x) {
       *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dx / 8, kBM)) + dx % 8) = __float2bfloat16_rn(x);
@@ -224,31 +266,12 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
       put(row, dy, 0.f);
     }
   }
-  const uint32_t mbS0 = smem_u32(mbar), mbO = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 3),
-                 mbV0 = smem_u32(mbar + 5), mbP0 = smem_u32(mbar + 7), mbX0 = smem_u32(mbar + 9);
-  if (control) {
-    if (lane == 0) {
-      for (int i = 0; i < 17; ++i) {
-        // P: one arrival per softmax warp; X: one per warp of the pair
-        const uint32_t cnt = (i == 7 || i == 8) ? kSoftmaxWarps : (i >= 9 ? 2 : 1);
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar + i)), "r"(cnt) : "memory");
-      }
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      *s_abort = 0;
-    }
-    __syncwarp();
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 ::"r"(smem_u32(&tslot)), "r"(kCols) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
   proxy_fence();
   tc_before();
   __syncthreads();
   tc_after();
   const uint32_t tbase = tslot;
   const uint32_t tO = tbase + 2 * kBN;          // S buffers at 0 and kBN
-  const int n_kt = (n_pages + kTilePages - 1) / kTilePages;
-  const int slab = (a.layer >= 0 ? a.layer : 0) % g.phys_layers;
   auto fail = [&]() {
     *s_abort = 1;
     atomicOr(a.err, AKV_DERR_WAIT);
@@ -258,23 +281,7 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
   if (control) {
     // ---- control warp: page rows and keep bits, TMA copies, MMAs (lane 0) ----
     const uint32_t id_s = idesc_bf16(kBM, kBN, 0), id_o = idesc_bf16(kBM, D, 1);
-    int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1}, s_pend = -1, o_pend = -1;
-    // lane 0: the four pages of tile kt into K (or V) buffer kt & 1
-    auto tma_tile = [&](int kt, bool is_k) {
-      const int b = kt & 1;
-      const uint32_t bar = (is_k ? mbK0 : mbV0) + 8 * b;
-      uint8_t* dst = (is_k ? sK : sV) + b * kBN * D * 2;
-      mbar_expect_tx(bar, KV_BYTES);
-#pragma unroll
-      for (int at = 0; at < D / 64; ++at)
-#pragma unroll
-        for (int j = 0; j < kTilePages; ++j)
-          tma_load_3d(smem_u32(dst + at * kBN * 128 + j * kPageRows * 128), is_k ? &a.tm_k : &a.tm_v,
-                      at * 64, s_prow[kt * kTilePages + j < kMaxItemPages ? kt * kTilePages + j : 0],
-                      slab, bar);
-      if (is_k) k_pend[b] = kt;
-      else v_pend[b] = kt;
-    };
+    int s_pend = -1, o_pend = -1;
     // descriptors built once; a k step or a buffer adds a constant to the
     // start-address field (addresses stay below 256 KB: no carry)
     const uint64_t dq = sdesc(smem_u32(sQ), 16, 1024);
@@ -293,10 +300,9 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
     };
     bool ok = true;
     if (n_kt > 0) {
-      if (lane == 0) {
-        tma_tile(0, true);
+      if (lane == 0) {                          // K(0), K(1) went out before the rotation
         tma_tile(0, false);
-        if (n_kt > 1) { tma_tile(1, true); tma_tile(1, false); }
+        if (n_kt > 1) tma_tile(1, false);
       }
       if (lane == 0) {
         ok = wait_phase(mbK0, 0, a.wait_limit);

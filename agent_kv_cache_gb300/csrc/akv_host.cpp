@@ -1340,7 +1340,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   }
   CK(launch_decode(a, plan->combine, n_seqs, reinterpret_cast<const int32_t*>(plan->d + o_item0),
                    reinterpret_cast<const int32_t*>(plan->d + o_splits), c->stream));
-  c->launches += plan->combine ? 2 : 1;
+  if (plan->items > 0) c->launches += plan->combine ? 2 : 1;
   return AKV_OK;
 }
 
