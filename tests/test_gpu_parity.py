@@ -451,9 +451,10 @@ def test_copy_on_write_isolation():
 
 
 @pytest.mark.parametrize("mode", [1, 2])
-@pytest.mark.parametrize("G,D,n_kids", [(4, 128, 19), (8, 128, 9), (2, 64, 20), (1, 64, 18),
-                                         (4, 64, 37)])
-def test_branches_share_pages_in_decode(G, D, n_kids, mode):
+@pytest.mark.parametrize("G,D,n_kids,rope", [(4, 128, 19, 0), (8, 128, 9, 0), (2, 64, 20, 0),
+                                              (1, 64, 18, 0), (4, 64, 37, 0), (4, 128, 11, 64),
+                                              (8, 64, 7, 32)])
+def test_branches_share_pages_in_decode(G, D, n_kids, rope, mode):
     """Branches forked from one prefix hold the same pages: a decode call
     reads them once for all rows that hold them identically (mode 1: the
     tensor-core shared-prefix items of up to 128 query rows; mode 2: shared
@@ -461,11 +462,11 @@ def test_branches_share_pages_in_decode(G, D, n_kids, mode):
     exactly its own attention, including rows whose keep bits on a shared
     page differ (dropped without reposition), rows that repositioned (kept
     leading pages stay shared), rows that copied the tail on append, and the
-    partly filled shared tail page."""
+    partly filled shared tail page; rope > 0: only the first rope dims rotate."""
     hkv = 2
     t = Twin(layers=2, hq=hkv * G, hkv=hkv, head_dim=D, page_size=16, dtype="bf16",
              rope_theta=5e5 if D == 128 else 1e4, max_pages=4096, max_seqs=n_kids + 4,
-             max_slots=2048, seed=11)
+             max_slots=2048, seed=11, rope_dim=rope)
     root = t.create()
     t.append([root], [1000])                    # 62 full pages and a partly filled tail
     kids = [t.fork(root) for _ in range(n_kids)]
