@@ -19,7 +19,6 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
-#include <map>
 #include <queue>
 #include <string>
 #include <unordered_map>
