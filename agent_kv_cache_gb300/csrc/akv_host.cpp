@@ -41,7 +41,8 @@ constexpr int kMaxMembers = 16384;         // members of shared decode items per
 constexpr int kMinSharedPages = 4;         // shorter runs of common pages are read per row
 constexpr int kShareRows = 128;            // query rows of a shared-prefix (tensor-core) item
 constexpr int kShareMaxMembers = 128;
-constexpr int kSharePages = 32;            // pages per shared-prefix item
+constexpr int kSharePagesMin = 32;         // pages per shared-prefix item (the kernel takes <= 64)
+constexpr int kSharePagesMax = 64;
 
 // 128-bit key of an operation history: two independent 64-bit chains, each
 // step finished with the MurmurHash3 64-bit finaliser (Appleby).
@@ -1121,10 +1122,21 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
           parts += (int64_t)segs[k].ns * segs[k].rows.size();
           pq.push({(w + segs[k].ns - 1) / segs[k].ns, k});
         }
-        // shared-prefix items: kSharePages pages each
-        for (auto& sg : tsegs) {
-          sg.ns = (int32_t)std::max<int64_t>(1, (sg.a1 - sg.a0 + kSharePages - 1) / kSharePages);
-          parts += (int64_t)sg.ns * sg.rows.size();
+        // shared-prefix items: 32..64 pages each, longer when that keeps all
+        // of them within about 90% of one wave of CTAs (two per SM): a CTA's
+        // set-up and epilogue weigh like a few tiles, and a second, partial
+        // wave costs a whole CTA's time
+        if (!tsegs.empty()) {
+          int64_t tp = 0;
+          for (auto& sg : tsegs) tp += sg.a1 - sg.a0;
+          const int64_t wave = std::max<int64_t>(1, 2 * c->sm_count * 9 / 10);
+          const int64_t per = std::min<int64_t>(
+              kSharePagesMax,
+              std::max<int64_t>(kSharePagesMin, (tp * c->cfg.hkv + wave - 1) / wave));
+          for (auto& sg : tsegs) {
+            sg.ns = (int32_t)std::max<int64_t>(1, (sg.a1 - sg.a0 + per - 1) / per);
+            parts += (int64_t)sg.ns * sg.rows.size();
+          }
         }
         // next to shared-prefix items the one-row items are what is left of
         // each row (its own pages, often long): a full wave of blocks keeps
