@@ -206,6 +206,7 @@ struct akv_cache {
   int32_t decode_share = 1;        // rows holding the same pages read them once (0 off,
                                    // 1 automatic, else the most rows per item)
   int32_t last_items = 0, last_shared = 0, last_members = 0;   // plan of the last decode call
+  std::vector<int32_t> share_head;  // decode planner scratch: first group of each pool page (-1)
   int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
   void* d_restore = nullptr;       // temporary key/value versions of restore attention
   size_t restore_cap = 0;
@@ -891,19 +892,14 @@ void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap,
   std::vector<std::vector<ActivePage>> ap(n);
   std::vector<std::vector<int32_t>> gid(n);        // entry -> group of >= 2 rows, or -1
   std::vector<std::vector<char>> covered(n);
-  struct Key {
-    int32_t page, kidx; uint64_t mask;
-    bool operator==(const Key& o) const { return page == o.page && kidx == o.kidx && mask == o.mask; }
-  };
-  struct KeyHash {
-    size_t operator()(const Key& k) const {
-      return std::hash<uint64_t>()(((uint64_t)(uint32_t)k.page << 32 | (uint32_t)k.kidx) ^
-                                   (k.mask * 0x9E3779B97F4A7C15ULL));
-    }
-  };
-  std::unordered_map<Key, int32_t, KeyHash> index;
-  std::vector<std::vector<std::pair<int32_t, int32_t>>> groups;   // (row, active index)
-  bool any = false;
+  // groups of identical entries: a reused page-indexed head, chained when a
+  // page appears under another slot page or other keep bits; members laid
+  // out flat by group (rows ascending)
+  struct Group { int32_t kidx; uint64_t mask; int32_t next, count, start; };
+  std::vector<Group> gk;
+  std::vector<int32_t> touched;
+  if ((int)c->share_head.size() < c->cfg.max_pages) c->share_head.assign(c->cfg.max_pages, -1);
+  std::vector<int32_t>& head = c->share_head;
   for (int i = 0; i < n; ++i) {
     active_pages(*hs[i], S, &ap[i]);
     gid[i].assign(ap[i].size(), -1);
@@ -911,26 +907,49 @@ void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap,
     if ((int64_t)ap[i].size() != hs[i]->n_active_pages) continue;   // never share then
     for (int32_t a = 0; a < (int32_t)ap[i].size(); ++a) {
       const ActivePage& e = ap[i][a];
-      if (e.page < 0 || c->refcnt[e.page] < 2) continue;
+      if (e.page < 0 || e.page >= c->cfg.max_pages || c->refcnt[e.page] < 2) continue;
       if (full_only && (int64_t)(e.kidx + 1) * S > hs[i]->n_slots) continue;
-      auto it = index.emplace(Key{e.page, e.kidx, e.mask}, (int32_t)groups.size());
-      if (it.second) groups.emplace_back();
-      groups[it.first->second].push_back({i, a});
-      gid[i][a] = it.first->second;
-      any |= groups[it.first->second].size() > 1;
+      int32_t g = head[e.page];
+      while (g >= 0 && !(gk[g].kidx == e.kidx && gk[g].mask == e.mask)) g = gk[g].next;
+      if (g < 0) {
+        g = (int32_t)gk.size();
+        if (head[e.page] < 0) touched.push_back(e.page);
+        gk.push_back({e.kidx, e.mask, head[e.page], 0, 0});
+        head[e.page] = g;
+      }
+      gid[i][a] = g;
+      ++gk[g].count;
     }
   }
+  for (int32_t p : touched) head[p] = -1;
+  bool any = false;
+  int32_t total = 0;
+  for (Group& gr : gk) {
+    gr.start = total;
+    total += gr.count;
+    any |= gr.count > 1;
+    gr.count = 0;
+  }
+  std::vector<std::pair<int32_t, int32_t>> flat(total);   // (row, active index) by group
+  for (int i = 0; i < n; ++i)
+    for (int32_t a = 0; a < (int32_t)gid[i].size(); ++a)
+      if (gid[i][a] >= 0) {
+        Group& gr = gk[gid[i][a]];
+        flat[gr.start + gr.count++] = {i, a};
+      }
+  // the members of group g: flat[gk[g].start .. + gk[g].count)
   if (any) {
     struct Cand { int32_t row, start, len; };
     std::vector<Cand> cand;
     for (int i = 0; i < n; ++i)
       for (int32_t a = 0; a < (int32_t)ap[i].size();) {
         const int32_t g0 = gid[i][a];
-        if (g0 < 0 || covered[i][a] || groups[g0].size() < 2) { ++a; continue; }
+        if (g0 < 0 || covered[i][a] || gk[g0].count < 2) { ++a; continue; }
         // how long each other row that holds this page stays identical
         cand.clear();
         int32_t longest = 0;
-        for (const auto& m : groups[g0]) {
+        for (int32_t f = gk[g0].start; f < gk[g0].start + gk[g0].count; ++f) {
+          const auto& m = flat[f];
           if (m.first == i || covered[m.first][m.second]) continue;
           const int j = m.first;
           int32_t len = 0;
