@@ -75,6 +75,20 @@ struct HostSeq {
   bool frozen = false;             // snapshot of a published prefix entry
   int64_t family = 0;              // pages are shared only within a family: a created
                                    // sequence starts one, forks inherit it
+  // changes whenever a held page below the tail or a held slot changes
+  // (drop, reposition, a new sequence); an append does not change it
+  uint64_t layout = 0;
+};
+
+// A range of one row's active list that the decode reads for one or more
+// rows of a call: `rows` are the members (rows[0] is the row whose active
+// list [a0, a1) the kernel walks); member k holds the same pool pages at the
+// same slot pages with the same keep bits over the first lens[k] pages of it,
+// at its own active indices starts[k]...
+struct Segment {
+  int32_t a0, a1;
+  std::vector<int32_t> rows, lens, starts;
+  int32_t ns = 1;
 };
 
 struct Stage { char* h = nullptr; char* d = nullptr; cudaEvent_t ev = nullptr; bool used = false; };
@@ -207,6 +221,16 @@ struct akv_cache {
                                    // 1 automatic, else the most rows per item)
   int32_t last_items = 0, last_shared = 0, last_members = 0;   // plan of the last decode call
   std::vector<int32_t> share_head;  // decode planner scratch: first group of each pool page (-1)
+  uint64_t layout_clock = 0;
+  // the shared segments of the last call planned with them: valid while the
+  // call has the same rows, each with the same layout version
+  struct ShareCache {
+    std::vector<int64_t> seqs;
+    std::vector<uint64_t> layout;
+    int cap = 0;
+    bool full_only = false;
+    std::vector<Segment> shared;
+  } share_cache;
   int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
   void* d_restore = nullptr;       // temporary key/value versions of restore attention
   size_t restore_cap = 0;
@@ -472,6 +496,7 @@ int akv_seq_create(akv_cache* c, int64_t* seq) {
   c->free_dslots.pop_back();
   const int64_t id = c->next_id++;
   s.family = id;
+  s.layout = ++c->layout_clock;
   c->seqs.emplace(id, std::move(s));
   ++c->epoch;
   *seq = id;
@@ -503,6 +528,7 @@ int akv_seq_fork(akv_cache* c, int64_t parent, int64_t* child) {
   for (int32_t pg : s.pages)
     if (pg >= 0) ++c->refcnt[pg];
   const int64_t id = c->next_id++;
+  s.layout = ++c->layout_clock;
   c->seqs.emplace(id, std::move(s));
   ++c->epoch;
   *child = id;
@@ -721,6 +747,7 @@ int akv_drop(akv_cache* c, int64_t seq, const int64_t* ranges, int32_t n_ranges)
 
   // commit
   s->alive.swap(alive);
+  s->layout = ++c->layout_clock;
   s->n_alive -= n_removed;
   s->n_active_pages = n_active;
   for (int64_t k : dead_pages) { decref(c, s->pages[k]); s->pages[k] = -1; }
@@ -829,6 +856,7 @@ int akv_reposition(akv_cache* c, const int64_t* seqs, int32_t n_seqs) {
     s->runs.swap(nr);
     s->alive.clear();
     if (it.r > 0) s->alive.push_back({0, it.r});
+    s->layout = ++c->layout_clock;
     s->n_slots = it.r;
     s->n_alive = it.r;
     s->n_active_pages = it.new_pages;
@@ -866,16 +894,6 @@ void active_pages(const HostSeq& sq, int S, std::vector<ActivePage>* out) {
     }
 }
 
-// A range of one row's active list that the decode reads for one or more
-// rows: `rows` are the members (rows[0] is the row whose active list
-// [a0, a1) the kernel walks); member k holds the same pool pages at the same
-// slot pages with the same keep bits over the first lens[k] pages of it.
-struct Segment {
-  int32_t a0, a1;
-  std::vector<int32_t> rows, lens;
-  int32_t ns = 1;
-};
-
 // Shared segments: walking the rows in order, an active page that other rows
 // hold identically (same pool page, slot page and keep bits) and that none
 // of them has read yet starts a segment.  Each such row joins for as long as
@@ -886,8 +904,8 @@ struct Segment {
 // covered this way is read per row.  full_only: share only pages whose every
 // slot has been written (below the row's held slots), so that no unwritten
 // pool memory is read for another row.
-void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap, bool full_only,
-                   std::vector<Segment>* segs) {
+void find_shared(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap, bool full_only,
+                 std::vector<Segment>* segs) {
   const int n = (int)hs.size(), S = c->cfg.page_size;
   std::vector<std::vector<ActivePage>> ap(n);
   std::vector<std::vector<int32_t>> gid(n);        // entry -> group of >= 2 rows, or -1
@@ -975,6 +993,7 @@ void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap,
           for (int k = k0; k < k1; ++k) {
             sg.rows.push_back(cand[k].row);
             sg.lens.push_back(cand[k].len);
+            sg.starts.push_back(cand[k].start);
             for (int32_t t = 0; t < cand[k].len; ++t) covered[cand[k].row][cand[k].start + t] = 1;
           }
           segs->push_back(std::move(sg));
@@ -983,29 +1002,46 @@ void plan_segments(akv_cache* c, const std::vector<const HostSeq*>& hs, int cap,
         a += longest;
       }
   }
-  // everything else, per row: maximal uncovered ranges (a row with no
-  // active page still gets one empty segment for its output)
+}
+
+// Every active page of a row not covered by the shared segments, as per-row
+// segments (maximal uncovered ranges; a row with no active page still gets
+// one empty segment for its output).
+void complete_segments(const std::vector<const HostSeq*>& hs, const std::vector<Segment>& shared,
+                       std::vector<Segment>* segs) {
+  const int n = (int)hs.size();
+  std::vector<std::vector<std::pair<int32_t, int32_t>>> cov(n);   // covered [start, end) per row
+  for (const Segment& sg : shared)
+    for (size_t k = 0; k < sg.rows.size(); ++k)
+      cov[sg.rows[k]].push_back({sg.starts[k], sg.starts[k] + sg.lens[k]});
   for (int i = 0; i < n; ++i) {
+    std::sort(cov[i].begin(), cov[i].end());
     const int32_t na = hs[i]->n_active_pages;
-    bool any_seg = false;
-    for (int32_t a = 0; a < na;) {
-      if (a < (int32_t)covered[i].size() && covered[i][a]) { ++a; any_seg = true; continue; }
-      int32_t b = a + 1;
-      while (b < na && !(b < (int32_t)covered[i].size() && covered[i][b])) ++b;
-      Segment sg;
-      sg.a0 = a;
-      sg.a1 = b;
-      sg.rows = {i};
-      sg.lens = {b - a};
-      segs->push_back(std::move(sg));
-      any_seg = true;
-      a = b;
+    bool any_seg = !cov[i].empty();
+    int32_t a = 0;
+    auto gap = [&](int32_t b) {
+      if (b > a) {
+        Segment sg;
+        sg.a0 = a;
+        sg.a1 = b;
+        sg.rows = {i};
+        sg.lens = {b - a};
+        sg.starts = {a};
+        segs->push_back(std::move(sg));
+        any_seg = true;
+      }
+    };
+    for (const auto& iv : cov[i]) {
+      gap(std::min(iv.first, na));
+      a = std::max(a, iv.second);
     }
+    gap(na);
     if (!any_seg) {
       Segment sg;
       sg.a0 = sg.a1 = 0;
       sg.rows = {i};
       sg.lens = {0};
+      sg.starts = {0};
       segs->push_back(std::move(sg));
     }
   }
@@ -1087,10 +1123,32 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
         tsegs.clear();
         sitems.clear();
         if (share) {
-          std::vector<Segment> all;
-          plan_segments(c, hs, share == 1 ? std::min(kShareRows / G, kShareMaxMembers) : mcap,
-                        share == 1, &all);
-          for (auto& sg : all) (share == 1 && sg.rows.size() > 1 ? tsegs : segs).push_back(std::move(sg));
+          const int cap = share == 1 ? std::min(kShareRows / G, kShareMaxMembers) : mcap;
+          const bool full_only = share == 1;
+          // the shared segments found for the same rows at the same layout
+          // versions are still exact (appends change only pages past them)
+          auto& sc = c->share_cache;
+          bool hit = full_only && sc.full_only && sc.cap == cap && (int)sc.seqs.size() == n_seqs &&
+                     std::equal(sc.seqs.begin(), sc.seqs.end(), seqs);
+          for (int i = 0; hit && i < n_seqs; ++i) hit = sc.layout[i] == hs[i]->layout;
+          std::vector<Segment> shared;
+          if (hit) {
+            shared = sc.shared;
+          } else {
+            find_shared(c, hs, cap, full_only, &shared);
+            if (full_only) {
+              sc.seqs.assign(seqs, seqs + n_seqs);
+              sc.layout.resize(n_seqs);
+              for (int i = 0; i < n_seqs; ++i) sc.layout[i] = hs[i]->layout;
+              sc.cap = cap;
+              sc.full_only = true;
+              sc.shared = shared;
+            }
+          }
+          std::vector<Segment> rest;
+          complete_segments(hs, shared, &rest);
+          for (auto& sg : shared) (share == 1 && sg.rows.size() > 1 ? tsegs : segs).push_back(sg);
+          for (auto& sg : rest) segs.push_back(std::move(sg));
         } else {
           for (int i = 0; i < n_seqs; ++i) {
             Segment sg;
@@ -1098,6 +1156,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
             sg.a1 = hs[i]->n_active_pages;
             sg.rows = {i};
             sg.lens = {sg.a1 - sg.a0};
+            sg.starts = {sg.a0};
             segs.push_back(std::move(sg));
           }
         }
@@ -1642,6 +1701,7 @@ int akv_prefix_fork(akv_cache* c, akv_prefix_index* x, const akv_op* ops, int32_
   // plan the new sequence
   HostSeq s;
   s.family = E->family;
+  s.layout = ++c->layout_clock;
   s.pages.assign((size_t)n_pages, -1);
   std::vector<int32_t> fresh = peek_pages(c, n_fresh);
   size_t fi = 0;

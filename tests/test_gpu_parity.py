@@ -518,6 +518,15 @@ def test_branches_share_pages_in_decode(G, D, n_kids, rope, mode):
     t.gpu.set_decode_sharing(mode)
     t.decode(rows[:-1], 1)
     assert t.gpu.decode_plan_stats()["shared_items"] > 0
+    # appends only: the shared part of the plan is reused, the tails grow
+    for step in (2, 3):
+        t.append(rows[:-1], [1 + step] * (len(rows) - 1))
+        t.decode(rows[:-1], step)
+    # a drop in one branch changes its layout: the plan is found again
+    t.drop(kids[1], [(100, 140)])
+    t.append(rows[:-1], [1] * (len(rows) - 1))
+    t.decode(rows[:-1], 4)
+    assert t.gpu.decode_plan_stats()["shared_items"] > 0
     for s in rows[:-1]:
         t.check(s)
 
