@@ -23,9 +23,11 @@
 // row's split counter; the one-row decode kernel of the same call, launched
 // after this grid, merges all partials of a row.
 //
-// Only pages whose every slot has been written are shared (the planner keeps
-// a sequence's partly filled tail page out), so every V row read here is a
-// finite value and P = 0 rows contribute exactly zero.
+// Pool memory of a slot that no row sees may hold any bits (a prefix fork's
+// empty tail page is held but never written, and appends may later fill the
+// rest of it): its score is masked, and its V row is zeroed in shared memory
+// before the PV MMA, since P = 0 does not cancel a NaN there.  The planner
+// also keeps each sequence's partly filled tail page out of shared items.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -338,10 +340,43 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
         }
       }
       if (lane == 0 && ok) {
-        // O += P(kt) V(kt)
         ok = wait_phase(mbV0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
-        if (ok) {
-          v_pend[b] = -1;
+        if (ok) v_pend[b] = -1;
+        else fail();
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      {
+        // V rows of slots no row sees (keep bit clear: the same for every
+        // member) may hold any bits -- a prefix fork's empty tail page, for
+        // one, is held but never written -- and 0 * NaN is NaN in the MMA:
+        // zero them in shared memory first (rare; pages past the range were
+        // filled with zeros by the copy)
+        uint64_t dead = 0;
+#pragma unroll
+        for (int j = 0; j < kTilePages; ++j) {
+          const int pg = kt * kTilePages + j;
+          if (pg < n_pages) dead |= (uint64_t)(~s_pbits[pg] & 0xffffu) << (16 * j);
+        }
+        if (dead) {
+          // every lane observes the copy's completion before writing over it
+          if (!__all_sync(0xffffffffu, wait_phase(mbV0 + 8 * b, (kt >> 1) & 1, kDrainPolls))) {
+            if (lane == 0) fail();
+            break;
+          }
+          uint8_t* vt = sV + b * kBN * D * 2;
+          for (int u = lane; u < kBN * (D / 64) * 8; u += 32) {
+            const int r = u / ((D / 64) * 8), at = (u / 8) % (D / 64), c = u % 8;
+            if ((dead >> r) & 1)
+              *reinterpret_cast<uint4*>(vt + at * kBN * 128 + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          proxy_fence();
+          __syncwarp();
+        }
+      }
+      if (lane == 0) {
+        // O += P(kt) V(kt)
+        {
           tc_after();
           const uint64_t vb = dv + (uint64_t)((b * kBN * D * 2) >> 4);
           const uint32_t tSb = tbase + b * kBN;
@@ -350,12 +385,9 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
             umma_ts(tO, tSb + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), id_o, kt > 0 || kk > 0);
           umma_commit(mbO);
           o_pend = kt;
-        } else {
-          fail();
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      __syncwarp();
     }
     if (lane == 0 && *s_abort) {
       // let work still in flight finish before the CTA's memory goes

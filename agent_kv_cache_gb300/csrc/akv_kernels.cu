@@ -432,7 +432,9 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, uint32_t li
 // t of the stage receive source rows (s_src_page[t], s_src_off[t]) through
 // one bulk copy per run, keys with s_rot[t] are rotated in place with the
 // row's cos/sin (s_cs, unit-minor), and rows [0, n_store) go out with one
-// bulk copy per tensor.  Layers l_begin..l_end-1 map to slab l % phys_layers.
+// bulk copy per tensor.  Rows without a source (dead slots of a prefix fork)
+// are written as zeros, so that a stored slot never holds stale bits.  Layers
+// l_begin..l_end-1 map to slab l % phys_layers.
 template <typename T>
 __device__ __forceinline__ void tile_pipeline(
     const Geom& g, int l_begin, int l_end, unsigned char* stage0, const float2* s_cs, const int* s_src_page,
@@ -447,6 +449,7 @@ __device__ __forceinline__ void tile_pipeline(
   const int n = (l_end - l_begin) * g.hkv;       // tiles: (layer, KV head)
   T* kp = static_cast<T*>(g.k);
   T* vp = static_cast<T*>(g.v);
+  const int n_dead = __syncthreads_count(tid < n_store && s_src_page[tid] < 0);   // n_store <= 64
   auto issue = [&](int i) {                      // thread 0: loads of tile i into its stage
     const int st = i % n_stages;
     const int l = l_begin + i / g.hkv, h = i % g.hkv;
@@ -486,6 +489,16 @@ __device__ __forceinline__ void tile_pipeline(
       const uint4 lo = *reinterpret_cast<const uint4*>(row + c * E);
       const uint4 hi = *reinterpret_cast<const uint4*>(row + RH + c * E);
       rotate_regs<T>(lo, hi, row, c, RH, s_cs + t * RH, kr);
+    }
+    if (n_dead > 0) {
+      const int ch = (int)(row_bytes / 16);      // 16-byte chunks of a row
+      for (int u = tid; u < n_store * ch; u += blockDim.x) {
+        const int t = u / ch, c = u % ch;
+        if (s_src_page[t] >= 0) continue;
+        unsigned char* r = reinterpret_cast<unsigned char*>(kt) + (size_t)t * row_bytes + (size_t)c * 16;
+        *reinterpret_cast<uint4*>(r) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(r + tile_bytes) = make_uint4(0, 0, 0, 0);
+      }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();

@@ -136,6 +136,17 @@ def _remaining(program, m):
     return rest
 
 
+def _poison_free_pages(f):
+    """NaN bit patterns in every free pool page (any slot a fork leaves
+    unwritten would show them)."""
+    free = [p for p in range(f.gpu.k_pool.shape[1]) if f.gpu.refcount(p) == 0]
+    if free:
+        idx = torch.tensor(free, dtype=torch.int64, device="cuda")
+        f.gpu.k_pool[:, idx] = float("nan")
+        f.gpu.v_pool[:, idx] = float("nan")
+        torch.cuda.synchronize()
+
+
 def _check_child(f, child, req, m, entry_recs):
     n = m["n_records"]
     plan = P.fork_plan(entry_recs, req, n, f.S)
@@ -195,6 +206,7 @@ def test_prefix_fork_matches_oracle(dtype, D, G, S, seed):
         prog, m = _branch(rng, base, nb)
         req = P.records(prog, ids[:m])
         want = P.match(f.entries, req, S)
+        _poison_free_pages(f)
         child, got = f.gpu.prefix_fork(f.idx, prog, ids[:m])
         assert {k: got[k] for k in want} == want, (got, want)
         kinds.append(got["kind"])
@@ -311,6 +323,7 @@ def test_retrigger_fork_rotates_keys(dtype):
     entry = [("append", 60), ("drop", [(10, 30)]), ("repos",), ("append", 8)]
     req = [("append", 60), ("drop", [(10, 30)]), ("append", 5)]
     e = f.publish(entry, ids[:68])
+    _poison_free_pages(f)
     child, m = f.gpu.prefix_fork(f.idx, req, ids[:65])
     assert m == dict(kind="retrigger", entry=e, n_records=61, n_tokens=60, n_rotated=30,
                      op_index=2, op_tokens=0)
@@ -328,4 +341,41 @@ def test_retrigger_fork_rotates_keys(dtype):
         err = np.abs(out.double().cpu().numpy() - oc.attention(l, q, [osid]))
         tmax, tmean = ATTN_TOL[dtype]
         assert err.max() <= tmax and err.mean() <= tmean
+    assert f.gpu.sync_errors() == 0
+
+
+def test_shared_decode_over_held_unwritten_slots():
+    """A prefix fork whose tail page holds no needed token gets a fresh page
+    whose held rows are never written (here NaN patterns: free pages were
+    poisoned); appends then fill the page, and forks of that sequence hold it
+    as a full page.  The tensor-core shared decode over those forks must mask
+    the unwritten rows in the scores and the values alike."""
+    f = Family("bf16", 128, 4, 16)
+    ids = list(range(1000, 1200))
+    entry = [("append", 120), ("drop", [(112, 120)])]
+    f.publish(entry, ids[:120])
+    _poison_free_pages(f)
+    req = entry + [("append", 8)]
+    child, m = f.gpu.prefix_fork(f.idx, req, ids[:128])
+    assert m["kind"] == "exact" and m["n_tokens"] == 120, m
+    f.run(child, _remaining(req, m), ids[:128], t0=120)
+    assert f.gpu.info(child)["n_held"] == 128
+    pages, _ = f.gpu.page_table(child)
+    # the held, dropped slots 112..119 of the last page were never written
+    assert torch.isnan(f.gpu.v_pool[:, int(pages[7]), :, :8].float()).any()
+    kids = [f.gpu.seq_fork(child) for _ in range(3)]
+    oc, osid = f.oracle(P.records(req, ids[:128]))
+    for mode in (1, 2, 0):
+        f.gpu.set_decode_sharing(mode)
+        for l in range(f.L):
+            q = np.stack([synth.query(f.seed, 700 + i, l, 0, f.hq, f.D, f.width)
+                          for i in range(len(kids))])
+            out = f.gpu.decode_attention(l, torch.from_numpy(q).to(f.tdtype).cuda(), kids)
+            got = out.double().cpu().numpy()
+            assert np.isfinite(got).all(), (mode, l)
+            err = np.abs(got - oc.attention(l, q, [osid] * len(kids)))
+            tmax, tmean = ATTN_TOL["bf16"]
+            assert err.max() <= tmax and err.mean() <= tmean, (mode, l, err.max())
+            if mode:
+                assert f.gpu.decode_plan_stats()["shared_items"] > 0
     assert f.gpu.sync_errors() == 0
