@@ -71,12 +71,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, uint32_t 
     if (mbar_try_wait(a, parity)) return true;
   return false;
 }
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t* r) {
@@ -284,12 +284,11 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
           mbar_arrive(full);
         } else {
           mbar_expect_tx(full, STAGE_BYTES);
+          // one copy per tensor: both 64-column atoms of the 16 rows, laid
+          // out [atom][row][64] (the same bytes as one 64 x 16 box per atom)
           const uint32_t dk = smem_u32(smem + s * STAGE_BYTES);
-#pragma unroll
-          for (int b = 0; b < D / 64; ++b) {
-            tma_load_3d(dk + b * 2048, &a.tm_k, b * 64, row, slab, full);
-            tma_load_3d(dk + TILE_BYTES + b * 2048, &a.tm_v, b * 64, row, slab, full);
-          }
+          tma_load_4d(dk, &a.tm_k4, 0, row, 0, slab, full);
+          tma_load_4d(dk + TILE_BYTES, &a.tm_v4, 0, row, 0, slab, full);
         }
         ++issued;
       }
@@ -675,6 +674,33 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
   cfg.dynamicSmemBytes = mma_smem<128>();
   return a.shared ? cudaLaunchKernelEx(&cfg, k_decode_mma<128, true>, a)
                   : cudaLaunchKernelEx(&cfg, k_decode_mma<128, false>, a);
+}
+
+// The same pools as 4-D maps (64 columns, rows, D / 64 atoms, slab): the atom
+// dimension steps 128 bytes inside a row, so one box (64 x 16 x D/64) lands
+// a 16-row tile's atoms one after the other, each in the 128-byte swizzled
+// layout of a 64 x 16 box.
+bool make_pool_tensor_maps4(const Geom& g, CUtensorMap* tk, CUtensorMap* tv) {
+  if (!decode_mma_supported(g)) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&encode),
+                                       12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !encode)
+    return false;
+  const uint64_t rows = (uint64_t)g.max_pages * g.hkv * g.s;
+  const cuuint64_t dims[4] = {64, rows, (cuuint64_t)(g.d / 64), (cuuint64_t)g.phys_layers};
+  const cuuint64_t strides[3] = {(cuuint64_t)g.d * 2, 128, (cuuint64_t)(rows * g.d * 2)};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kTile, (cuuint32_t)(g.d / 64), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = encode(i == 0 ? tk : tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                        i == 0 ? g.k : g.v, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+  }
+  return true;
 }
 
 int decode_mma_blocks_per_sm(int d) {

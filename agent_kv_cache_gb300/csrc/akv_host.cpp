@@ -213,7 +213,7 @@ struct akv_cache {
   uint32_t wait_limit = 1u << 22;
   int sm_count = 148;
   uint64_t launches = 0;
-  CUtensorMap tm_k{}, tm_v{};
+  CUtensorMap tm_k{}, tm_v{}, tm_k4{}, tm_v4{};
   bool use_mma = false;
   int mma_blocks_per_sm = 0;
   int32_t decode_waves = 1;
@@ -459,7 +459,8 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   }
   CKC(cudaMalloc(&c->d_counters, (size_t)kMaxItems * f.hkv * sizeof(int32_t)));
   CKC(cudaMemset(c->d_counters, 0, (size_t)kMaxItems * f.hkv * sizeof(int32_t)));
-  c->use_mma = make_pool_tensor_maps(g, &c->tm_k, &c->tm_v);
+  c->use_mma = make_pool_tensor_maps(g, &c->tm_k, &c->tm_v) &&
+               make_pool_tensor_maps4(g, &c->tm_k4, &c->tm_v4);
   if (c->use_mma) {
     c->mma_blocks_per_sm = decode_mma_blocks_per_sm(f.head_dim);
     if (c->mma_blocks_per_sm < 1) c->use_mma = false;
@@ -1399,6 +1400,8 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   DecodeArgs a{};
   a.tm_k = c->tm_k;
   a.tm_v = c->tm_v;
+  a.tm_k4 = c->tm_k4;
+  a.tm_v4 = c->tm_v4;
   a.use_mma = c->use_mma;
   a.g = c->g;
   a.sa = c->sa;

@@ -113,8 +113,10 @@ struct ShareItem {
 };
 
 struct DecodeArgs {
-  CUtensorMap tm_k;     // TMA maps over the pools (tensor-core path only)
-  CUtensorMap tm_v;
+  CUtensorMap tm_k;     // TMA maps over the pools (tensor-core paths): (D, rows, slab),
+  CUtensorMap tm_v;     // 64 x 16 boxes
+  CUtensorMap tm_k4;    // the same pools as (64, rows, D / 64, slab): both 64-column
+  CUtensorMap tm_v4;    // atoms of a 16-row tile in one copy (one-row kernel)
   Geom g;
   SeqArrays sa;
   const DecodeItem* items;
@@ -210,6 +212,7 @@ cudaError_t launch_decode(const DecodeArgs& a, bool need_combine, int n_rows,
 // Tensor-core decode (akv_decode_mma.cu).
 bool decode_mma_supported(const Geom& g);
 bool make_pool_tensor_maps(const Geom& g, CUtensorMap* tk, CUtensorMap* tv);
+bool make_pool_tensor_maps4(const Geom& g, CUtensorMap* tk, CUtensorMap* tv);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st);
 int decode_mma_blocks_per_sm(int head_dim);
 // Shared-prefix decode (akv_decode_share.cu): bf16 pools, page size 16,
