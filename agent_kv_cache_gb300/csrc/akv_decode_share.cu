@@ -14,9 +14,11 @@
 //   O += P V       M=128, N=D, K=64, A = P from TMEM
 //
 // The item's page ids and keep bits (at most kMaxItemPages pages) are read
-// into shared memory first.  The control warp copies each tile's four pages
-// of K and V with TMA (a page past the range is read at an out-of-range row,
-// which TMA fills with zeros) and issues the MMAs from one thread; eight
+// into shared memory first.  A load warp copies each tile's four pages of K
+// and V with TMA (a page past the range is read at an out-of-range row,
+// which TMA fills with zeros) and an MMA warp issues the MMAs, each from one
+// thread: the SM's TMA unit takes its requests one after another, so copies
+// and MMAs issued by one thread would make a tile wait for both; eight
 // softmax warps, two per TMEM lane quarter, split the tile's tokens and O's
 // columns in halves.  Every wait is bounded.  The epilogue writes each
 // member's partial (unnormalised O, reference max, sum) and counts it in the
@@ -43,7 +45,9 @@ constexpr int kBN = 64;                     // tokens per tile
 constexpr int kPageRows = 16;               // the page size this kernel reads
 constexpr int kTilePages = kBN / kPageRows;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 1);   // + one control warp
+constexpr int kMmaWarp = kSoftmaxWarps;      // issues the MMAs (one thread)
+constexpr int kLoadWarp = kSoftmaxWarps + 1; // issues the tile copies (one thread)
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kHalf = kBN / 2;              // tokens per softmax warp and tile
 constexpr int kCols = 256;                  // TMEM: two S buffers (2 x 64) and O (<= 128)
 constexpr int kMaxItemPages = 64;           // pages of one item (the planner takes 32)
@@ -89,8 +93,8 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
   __shared__ int s_prow[kMaxItemPages];         // TMA row of each page (past the pool: zeros)
   __shared__ uint32_t s_pbits[kMaxItemPages];   // keep bits of each page's 16 slots
   __shared__ int s_abort_v;
-  // S[2] O K[2] V[2] P[2], then X[4 quarters][2]: row-max exchange of a pair
-  __shared__ __align__(8) uint64_t mbar[17];
+  // S[2] O[2] K[2] V[2] P[2], then X[4 quarters][2]: row-max exchange of a pair
+  __shared__ __align__(8) uint64_t mbar[18];
   __shared__ uint32_t tslot;
   volatile int* s_abort = &s_abort_v;
 
@@ -102,7 +106,7 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
   const Geom& g = a.g;
   const int G = g.hq / g.hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool control = warp == kSoftmaxWarps;
+  const bool control = warp == kMmaWarp, loader = warp == kLoadWarp;
   // the item and its members must describe memory this call owns
   bool bad = it.dslot < 0 || it.dslot >= a.max_seqs || it.p0 < 0 || it.p1 < it.p0 ||
              it.p1 > a.sa.seq_pages || it.p1 - it.p0 > kMaxItemPages || it.n_mem < 1 ||
@@ -143,13 +147,13 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
     }
   }
 
-  const uint32_t mbS0 = smem_u32(mbar), mbO = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 3),
-                 mbV0 = smem_u32(mbar + 5), mbP0 = smem_u32(mbar + 7), mbX0 = smem_u32(mbar + 9);
+  const uint32_t mbS0 = smem_u32(mbar), mbO0 = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 4),
+                 mbV0 = smem_u32(mbar + 6), mbP0 = smem_u32(mbar + 8), mbX0 = smem_u32(mbar + 10);
   if (control) {
     if (lane == 0) {
-      for (int i = 0; i < 17; ++i) {
+      for (int i = 0; i < 18; ++i) {
         // P: one arrival per softmax warp; X: one per warp of the pair
-        const uint32_t cnt = (i == 7 || i == 8) ? kSoftmaxWarps : (i >= 9 ? 2 : 1);
+        const uint32_t cnt = (i == 8 || i == 9) ? kSoftmaxWarps : (i >= 10 ? 2 : 1);
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar + i)), "r"(cnt) : "memory");
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -162,8 +166,8 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
   }
   const int n_kt = (n_pages + kTilePages - 1) / kTilePages;
   const int slab = (a.layer >= 0 ? a.layer : 0) % g.phys_layers;
-  int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1};   // control warp: copies in flight
-  // control lane 0: the four pages of tile kt into K (or V) buffer kt & 1
+  int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1};   // load warp: copies in flight
+  // load lane 0: the four pages of tile kt into K (or V) buffer kt & 1
   auto tma_tile = [&](int kt, bool is_k) {
     const int b = kt & 1;
     const uint32_t bar = (is_k ? mbK0 : mbV0) + 8 * b;
@@ -207,7 +211,7 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
       }
     }
     __syncthreads();   // staged rows, page rows and the barriers' initialisation are visible
-    if (control && lane == 0 && n_kt > 0) {
+    if (loader && lane == 0 && n_kt > 0) {
       tma_tile(0, true);
       if (n_kt > 1) tma_tile(1, true);
     }
@@ -280,10 +284,35 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
   };
 
   float m_r = -INFINITY, l_r = 0.f;
-  if (control) {
-    // ---- control warp: page rows and keep bits, TMA copies, MMAs (lane 0) ----
+  if (loader) {
+    // ---- load warp: K(kt + 2) once softmax(kt) has read S(kt), V(kt + 2)
+    // once PV(kt) has read V(kt) (lane 0) ----
+    if (lane == 0 && n_kt > 0) {
+      tma_tile(0, false);                       // K(0), K(1) went out before the rotation
+      if (n_kt > 1) tma_tile(1, false);
+      bool ok = true;
+      for (int kt = 0; kt + 2 < n_kt && ok && !*s_abort; ++kt) {
+        const int b = kt & 1;
+        ok = wait_phase(mbP0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
+        if (ok) tma_tile(kt + 2, true);
+        if (ok) ok = wait_phase(mbO0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
+        if (ok) tma_tile(kt + 2, false);
+        if (!ok) fail();
+      }
+      if (*s_abort) {
+        // this warp's copies land before the CTA's memory goes (bounded by a
+        // fixed limit, independent of the user's wait limit)
+        for (int b = 0; b < 2; ++b) {
+          if (k_pend[b] >= 0) wait_phase(mbK0 + 8 * b, (k_pend[b] >> 1) & 1, kDrainPolls);
+          if (v_pend[b] >= 0) wait_phase(mbV0 + 8 * b, (v_pend[b] >> 1) & 1, kDrainPolls);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (control) {
+    // ---- MMA warp: S(kt + 1) while softmax(kt) runs, then PV(kt) (lane 0) ----
     const uint32_t id_s = idesc_bf16(kBM, kBN, 0), id_o = idesc_bf16(kBM, D, 1);
-    int s_pend = -1, o_pend = -1;
+    int s_pend = -1, o_pend[2] = {-1, -1};
     // descriptors built once; a k step or a buffer adds a constant to the
     // start-address field (addresses stay below 256 KB: no carry)
     const uint64_t dq = sdesc(smem_u32(sQ), 16, 1024);
@@ -301,15 +330,9 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
       s_pend = kt;
     };
     bool ok = true;
-    if (n_kt > 0) {
-      if (lane == 0) {                          // K(0), K(1) went out before the rotation
-        tma_tile(0, false);
-        if (n_kt > 1) tma_tile(1, false);
-      }
-      if (lane == 0) {
-        ok = wait_phase(mbK0, 0, a.wait_limit);
-        if (ok) { k_pend[0] = -1; tc_after(); issue_s(0); } else fail();
-      }
+    if (n_kt > 0 && lane == 0) {
+      ok = wait_phase(mbK0, 0, a.wait_limit);
+      if (ok) { tc_after(); issue_s(0); } else fail();
     }
     for (int kt = 0; kt < n_kt; ++kt) {
       const int b = kt & 1;
@@ -319,30 +342,22 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
         // S(kt+1) into the other S buffer once PV(kt-1) has read its P
         if (kt + 1 < n_kt) {
           if (kt > 0) {
-            ok = wait_phase(mbO, (kt - 1) & 1, a.wait_limit);
-            if (ok) o_pend = -1;
+            ok = wait_phase(mbO0 + 8 * (b ^ 1), ((kt - 1) >> 1) & 1, a.wait_limit);
+            if (ok) o_pend[b ^ 1] = -1;
           }
           if (ok) ok = wait_phase(mbK0 + 8 * (b ^ 1), ((kt + 1) >> 1) & 1, a.wait_limit);
           if (ok) {
-            k_pend[b ^ 1] = -1;
             tc_after();
             issue_s(kt + 1);
-            if (kt + 1 >= 2) tma_tile(kt + 1, false);   // V buffer b^1 was read by PV(kt-1)
           }
         }
-        // softmax of tile kt done: S(kt) is consumed
+        // softmax of tile kt done (S(kt) consumed, P(kt) written) and V(kt) in
         if (ok) ok = wait_phase(mbP0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
         if (ok) {
           s_pend = s_pend == kt ? -1 : s_pend;
-          if (kt + 2 < n_kt) tma_tile(kt + 2, true);   // K buffer b is free
-        } else {
-          fail();
+          ok = wait_phase(mbV0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
         }
-      }
-      if (lane == 0 && ok) {
-        ok = wait_phase(mbV0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
-        if (ok) v_pend[b] = -1;
-        else fail();
+        if (!ok) fail();
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
@@ -376,28 +391,22 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
       }
       if (lane == 0) {
         // O += P(kt) V(kt)
-        {
-          tc_after();
-          const uint64_t vb = dv + (uint64_t)((b * kBN * D * 2) >> 4);
-          const uint32_t tSb = tbase + b * kBN;
+        tc_after();
+        const uint64_t vb = dv + (uint64_t)((b * kBN * D * 2) >> 4);
+        const uint32_t tSb = tbase + b * kBN;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(tO, tSb + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), id_o, kt > 0 || kk > 0);
-          umma_commit(mbO);
-          o_pend = kt;
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(tO, tSb + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), id_o, kt > 0 || kk > 0);
+        umma_commit(mbO0 + 8 * b);
+        o_pend[b] = kt;
       }
       __syncwarp();
     }
     if (lane == 0 && *s_abort) {
-      // let work still in flight finish before the CTA's memory goes
-      // (bounded by a fixed limit, independent of the user's wait limit)
-      for (int b = 0; b < 2; ++b) {
-        if (k_pend[b] >= 0) wait_phase(mbK0 + 8 * b, (k_pend[b] >> 1) & 1, kDrainPolls);
-        if (v_pend[b] >= 0) wait_phase(mbV0 + 8 * b, (v_pend[b] >> 1) & 1, kDrainPolls);
-      }
+      // this warp's MMAs finish before the CTA's memory goes (bounded)
       if (s_pend >= 0) wait_phase(mbS0 + 8 * (s_pend & 1), (s_pend >> 1) & 1, kDrainPolls);
-      if (o_pend >= 0) wait_phase(mbO, o_pend & 1, kDrainPolls);
+      for (int b = 0; b < 2; ++b)
+        if (o_pend[b] >= 0) wait_phase(mbO0 + 8 * b, (o_pend[b] >> 1) & 1, kDrainPolls);
     }
   } else {
     // ---- softmax warps: row = TMEM lane, tokens and O columns split in halves ----
@@ -474,7 +483,8 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
       tmem_st16(tSb + lane_off + half * (kHalf / 2), pk);   // P(kt) over S(kt)
       if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O is stable once PV(kt-1) is done; this half rescales its columns
-        const bool okv = __all_sync(0xffffffffu, wait_phase(mbO, (kt - 1) & 1, a.wait_limit));
+        const bool okv = __all_sync(0xffffffffu, wait_phase(mbO0 + 8 * ((kt - 1) & 1), ((kt - 1) >> 1) & 1,
+                                                             a.wait_limit));
         if (!okv) {
           if (lane == 0) fail();
           break;
@@ -497,7 +507,8 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
     }
     // the last PV
     if (n_kt > 0 && !*s_abort) {
-      const bool okv = __all_sync(0xffffffffu, wait_phase(mbO, (n_kt - 1) & 1, a.wait_limit));
+      const bool okv = __all_sync(0xffffffffu, wait_phase(mbO0 + 8 * ((n_kt - 1) & 1),
+                                                           ((n_kt - 1) >> 1) & 1, a.wait_limit));
       if (!okv && lane == 0) fail();
     }
     // this half's row sum, combined in the epilogue
@@ -512,7 +523,7 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
   // global write waits until that grid has finished.  Nothing above reads
   // memory a decode call writes.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (!control && !*s_abort) {
+  if (warp < kSoftmaxWarps && !*s_abort) {
     // epilogue: this half's columns of the unnormalised O, and (max, sum)
     const int quarter = warp & 3, half = warp >> 2;
     const int row = 32 * quarter + lane;
