@@ -193,8 +193,9 @@ cudaError_t launch_simple_g(const RestoreArgs& a, int G, cudaStream_t st) {
 // Q, K and V live in shared memory in the 128-byte swizzled layout (rows of
 // 128 bytes, 16-byte chunk c of row r at c ^ (r % 8), 64-element atoms of
 // rows*128 bytes): Q and K K-major, V (the same bytes as K's layout) read
-// MN-major.  A control warp issues the TMA copies and the MMAs (one thread)
-// and loads the keys' death times; eight softmax warps, two per TMEM lane
+// MN-major.  A load warp issues the TMA copies and loads the keys' death
+// times, an MMA warp issues the MMAs (each from one thread, so that neither
+// waits behind the other's issue); eight softmax warps, two per TMEM lane
 // quarter, split each tile's keys and O's columns in halves.  Hand-offs are
 // bounded mbarrier waits.  Two CTAs share an SM (about 103 KB of shared
 // memory and 256 TMEM columns each for D = 128).
@@ -212,14 +213,16 @@ template <int D>
 constexpr size_t restore_tc_smem() {
   return 1024 /* alignment slack */ + (size_t)kBM * D * 2 + 4 * (size_t)kBN * D * 2 +
          2 * kBN * sizeof(int) + 6 * kBM * sizeof(float) + 4 * sizeof(int) +
-         19 * sizeof(uint64_t) + 16;
+         20 * sizeof(uint64_t) + 16;
 }
 
 // softmax warps: warp w reads TMEM lanes 32 (w % 4) .. (its rows) and the
 // key half w / 4 of every S tile (and of O's columns); rows are shared by
 // warps w and w + 4, which combine their row maxima through shared memory
 constexpr int kSoftmaxWarps = 8;
-constexpr int kRestoreThreads = 32 * (kSoftmaxWarps + 1);   // + one control warp
+constexpr int kMmaWarp = kSoftmaxWarps;                     // issues the MMAs (one thread)
+constexpr int kLoadWarp = kSoftmaxWarps + 1;                // copies, key deaths
+constexpr int kRestoreThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kHalf = kBN / 2;                              // keys per softmax warp and tile
 
 template <int D, int NH>
@@ -237,15 +240,15 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
   float* s_mx = reinterpret_cast<float*>(s_death + 2 * kBN);     // [3][2 halves][kBM]
   int* s_dmin = reinterpret_cast<int*>(s_mx + 6 * kBM);           // [2]
   volatile int* s_abort = s_dmin + 2;
-  // S[2] O K[2] V[2] P[2] D[2], then X[4 quarters][2]: row-max exchange of a pair
+  // S[2] O[2] K[2] V[2] P[2] D[2], then X[4 quarters][2]: row-max exchange of a pair
   uint64_t* mbar = reinterpret_cast<uint64_t*>(s_dmin + 4);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 19);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 20);
 
   const RestoreTile tl = a.tiles[blockIdx.x];
   const int kvh = blockIdx.y;
   const int G = a.g.hq / a.g.hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool control = warp == kSoftmaxWarps;
+  const bool control = warp == kMmaWarp, loader = warp == kLoadWarp;
   const int tend = tl.tok0 + tl.n_tok;
   const int R = a.g.rope, RH = R / 2;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
@@ -279,14 +282,14 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
     *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dx / 8, kBM)) + dx % 8) = __float2bfloat16_rn(x);
     *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dy / 8, kBM)) + dy % 8) = __float2bfloat16_rn(y);
   }
-  const uint32_t mbS0 = smem_u32(mbar), mbO = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 3),
-                 mbV0 = smem_u32(mbar + 5), mbP0 = smem_u32(mbar + 7), mbD0 = smem_u32(mbar + 9),
-                 mbX0 = smem_u32(mbar + 11);
+  const uint32_t mbS0 = smem_u32(mbar), mbO0 = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 4),
+                 mbV0 = smem_u32(mbar + 6), mbP0 = smem_u32(mbar + 8), mbD0 = smem_u32(mbar + 10),
+                 mbX0 = smem_u32(mbar + 12);
   if (control) {
     if (lane == 0) {
-      for (int i = 0; i < 19; ++i) {
+      for (int i = 0; i < 20; ++i) {
         // P: one arrival per softmax warp; X: one per warp of the pair
-        const uint32_t cnt = (i == 7 || i == 8) ? kSoftmaxWarps : (i >= 11 ? 2 : 1);
+        const uint32_t cnt = (i == 8 || i == 9) ? kSoftmaxWarps : (i >= 12 ? 2 : 1);
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar + i)), "r"(cnt) : "memory");
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -311,10 +314,10 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
 
   float m_r = -INFINITY, l_r = 0.f;
   int t_r = 0;
-  if (control) {
-    // ---- control warp: TMA copies, key deaths, MMAs (lane 0 issues) ----
-    const uint32_t id_s = idesc_bf16(kBM, kBN, 0), id_o = idesc_bf16(kBM, D, 1);
-    int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1}, s_pend = -1, o_pend = -1;
+  if (loader) {
+    // ---- load warp: K(kt + 2) and the key deaths of kt + 2 once softmax(kt)
+    // is done, V(kt + 2) once PV(kt) is done (lane 0 issues the copies) ----
+    int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1};
     auto tma_k = [&](int kt) {
       const int b = kt & 1;
       mbar_expect_tx(mbK0 + 8 * b, KV_BYTES);
@@ -360,6 +363,51 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
       fetch_deaths(kt, dd);
       store_deaths(kt, dd);
     };
+    bool ok = true;
+    if (n_kt > 0) {
+      if (lane == 0) {
+        tma_k(0);
+        tma_v(0);
+        if (n_kt > 1) { tma_k(1); tma_v(1); }
+      }
+      deaths(0);
+      if (n_kt > 1) deaths(1);
+    }
+    for (int kt = 0; kt + 2 < n_kt; ++kt) {
+      const int b = kt & 1;
+      ok = __shfl_sync(0xffffffffu, ok, 0) && !*s_abort;
+      if (!ok) break;
+      int dnext[kBN / 32];
+      fetch_deaths(kt + 2, dnext);      // in flight while lane 0 waits
+      if (lane == 0) {
+        // softmax of tile kt done: S(kt) has read K buffer b, deaths(kt) consumed
+        ok = mbar_wait(mbP0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
+        if (ok) tma_k(kt + 2);
+        else fail();
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      store_deaths(kt + 2, dnext);
+      if (lane == 0) {
+        // PV(kt) has read V buffer b
+        ok = mbar_wait(mbO0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
+        if (ok) tma_v(kt + 2);
+        else fail();
+      }
+    }
+    if (lane == 0 && *s_abort) {
+      // this warp's copies land before the CTA's memory goes (bounded by a
+      // fixed limit, independent of the user's wait limit)
+      for (int b = 0; b < 2; ++b) {
+        if (k_pend[b] >= 0) mbar_wait(mbK0 + 8 * b, (k_pend[b] >> 1) & 1, kDrainPolls);
+        if (v_pend[b] >= 0) mbar_wait(mbV0 + 8 * b, (v_pend[b] >> 1) & 1, kDrainPolls);
+      }
+    }
+    __syncwarp();
+  } else if (control) {
+    // ---- MMA warp: S(kt + 1) while softmax(kt) runs, then PV(kt) (lane 0) ----
+    const uint32_t id_s = idesc_bf16(kBM, kBN, 0), id_o = idesc_bf16(kBM, D, 1);
+    int s_pend = -1, o_pend[2] = {-1, -1};
     // descriptors built once; a k step or a buffer adds a constant to the
     // start-address field (addresses stay below 256 KB: no carry)
     const uint64_t dq = sdesc(smem_u32(sQ), 16, 1024);
@@ -377,80 +425,54 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
       s_pend = kt;
     };
     bool ok = true;
-    if (n_kt > 0) {
-      if (lane == 0) {
-        tma_k(0);
-        tma_v(0);
-        if (n_kt > 1) { tma_k(1); tma_v(1); }
-      }
-      deaths(0);
-      if (n_kt > 1) deaths(1);
-      if (lane == 0) {
-        ok = mbar_wait(mbK0, 0, a.wait_limit);
-        if (ok) { k_pend[0] = -1; tc_after(); issue_s(0); } else fail();
-      }
+    if (n_kt > 0 && lane == 0) {
+      ok = mbar_wait(mbK0, 0, a.wait_limit);
+      if (ok) { tc_after(); issue_s(0); } else fail();
     }
     for (int kt = 0; kt < n_kt; ++kt) {
       const int b = kt & 1;
       ok = __shfl_sync(0xffffffffu, ok, 0) && !*s_abort;
       if (!ok) break;
-      int dnext[kBN / 32];
-      fetch_deaths(kt + 2, dnext);      // in flight while lane 0 waits
       if (lane == 0) {
         // S(kt+1) into the other S buffer once PV(kt-1) has read its P
         if (kt + 1 < n_kt) {
           if (kt > 0) {
-            ok = mbar_wait(mbO, (kt - 1) & 1, a.wait_limit);
-            if (ok) o_pend = -1;
+            ok = mbar_wait(mbO0 + 8 * (b ^ 1), ((kt - 1) >> 1) & 1, a.wait_limit);
+            if (ok) o_pend[b ^ 1] = -1;
           }
           if (ok) ok = mbar_wait(mbK0 + 8 * (b ^ 1), ((kt + 1) >> 1) & 1, a.wait_limit);
           if (ok) {
-            k_pend[b ^ 1] = -1;
             tc_after();
             issue_s(kt + 1);
-            if (kt + 1 >= 2) tma_v(kt + 1);   // V buffer b^1 was read by PV(kt-1)
           }
         }
-        // softmax of tile kt done: S(kt) and the deaths of kt are consumed
+        // O += P(kt) V(kt) once the softmax of kt is done and V(kt) is in
         if (ok) ok = mbar_wait(mbP0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
         if (ok) {
           s_pend = s_pend == kt ? -1 : s_pend;
-          if (kt + 2 < n_kt) tma_k(kt + 2);   // K buffer b is free
-        } else {
-          fail();
+          ok = mbar_wait(mbV0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
         }
-      }
-      if (lane == 0 && ok) {
-        // O += P(kt) V(kt)
-        ok = mbar_wait(mbV0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
         if (ok) {
-          v_pend[b] = -1;
           tc_after();
           const uint64_t vb = dv + (uint64_t)((b * kBN * D * 2) >> 4);
           const uint32_t tSb = tbase + b * kBN;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             umma_ts(tO, tSb + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), id_o, kt > 0 || kk > 0);
-          umma_commit(mbO);
-          o_pend = kt;
+          umma_commit(mbO0 + 8 * b);
+          o_pend[b] = kt;
         } else {
           fail();
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (kt + 2 < n_kt) store_deaths(kt + 2, dnext);   // buffer b: deaths(kt) consumed
     }
     if (lane == 0 && *s_abort) {
-      // let work still in flight finish before the CTA's memory goes
-      // (bounded by a fixed limit, independent of the user's wait limit)
-      for (int b = 0; b < 2; ++b) {
-        if (k_pend[b] >= 0) mbar_wait(mbK0 + 8 * b, (k_pend[b] >> 1) & 1, kDrainPolls);
-        if (v_pend[b] >= 0) mbar_wait(mbV0 + 8 * b, (v_pend[b] >> 1) & 1, kDrainPolls);
-      }
+      // this warp's MMAs finish before the CTA's memory goes (bounded)
       if (s_pend >= 0) mbar_wait(mbS0 + 8 * (s_pend & 1), (s_pend >> 1) & 1, kDrainPolls);
-      if (o_pend >= 0) mbar_wait(mbO, o_pend & 1, kDrainPolls);
+      for (int b = 0; b < 2; ++b)
+        if (o_pend[b] >= 0) mbar_wait(mbO0 + 8 * b, (o_pend[b] >> 1) & 1, kDrainPolls);
     }
+    __syncwarp();
   } else {
     // ---- softmax warps: row = TMEM lane, keys and O columns split in halves ----
     const int quarter = warp & 3, half = warp >> 2;
@@ -539,7 +561,8 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
       tmem_st16(tSb + lane_off + half * (kHalf / 2), pk);   // P(kt) over S(kt)
       if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O is stable once PV(kt-1) is done; this half rescales its columns
-        const bool okv = __all_sync(0xffffffffu, mbar_wait(mbO, (kt - 1) & 1, a.wait_limit));
+        const bool okv = __all_sync(0xffffffffu, mbar_wait(mbO0 + 8 * ((kt - 1) & 1), ((kt - 1) >> 1) & 1,
+                                                           a.wait_limit));
         if (!okv) {
           if (lane == 0) fail();
           break;
@@ -562,7 +585,8 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
     }
     // the last PV
     if (n_kt > 0 && !*s_abort) {
-      const bool okv = __all_sync(0xffffffffu, mbar_wait(mbO, (n_kt - 1) & 1, a.wait_limit));
+      const bool okv = __all_sync(0xffffffffu, mbar_wait(mbO0 + 8 * ((n_kt - 1) & 1),
+                                                         ((n_kt - 1) >> 1) & 1, a.wait_limit));
       if (!okv && lane == 0) fail();
     }
     // this half's row sum, combined in the epilogue
@@ -571,7 +595,7 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
   tc_before();
   __syncthreads();
   tc_after();
-  if (!control && n_kt > 0 && !*s_abort) {
+  if (warp < kSoftmaxWarps && n_kt > 0 && !*s_abort) {
     // epilogue: this half's columns of O / l
     const int quarter = warp & 3, half = warp >> 2;
     const int row = 32 * quarter + lane;
