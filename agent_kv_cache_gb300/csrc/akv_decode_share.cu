@@ -168,20 +168,30 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
   const int slab = (a.layer >= 0 ? a.layer : 0) % g.phys_layers;
   int k_pend[2] = {-1, -1}, v_pend[2] = {-1, -1};   // load warp: copies in flight
   // load lane 0: the four pages of tile kt into K (or V) buffer kt & 1
+  // K: [atom][64 rows][128 B] (the S MMA spans the tile's four pages), one
+  // 64 x 16 box per (atom, page); V: [page][atom][16 rows][128 B] (a PV
+  // MMA step is one page), one 64 x 16 x D/64 box per page over the pool
+  // seen as (64 columns, rows, atoms, slab)
   auto tma_tile = [&](int kt, bool is_k) {
     const int b = kt & 1;
     const uint32_t bar = (is_k ? mbK0 : mbV0) + 8 * b;
     uint8_t* dst = (is_k ? sK : sV) + b * kBN * D * 2;
     mbar_expect_tx(bar, KV_BYTES);
+    if (is_k) {
 #pragma unroll
-    for (int at = 0; at < D / 64; ++at)
+      for (int at = 0; at < D / 64; ++at)
+#pragma unroll
+        for (int j = 0; j < kTilePages; ++j)
+          tma_load_3d(smem_u32(dst + at * kBN * 128 + j * kPageRows * 128), &a.tm_k, at * 64,
+                      s_prow[kt * kTilePages + j < kMaxItemPages ? kt * kTilePages + j : 0], slab, bar);
+      k_pend[b] = kt;
+    } else {
 #pragma unroll
       for (int j = 0; j < kTilePages; ++j)
-        tma_load_3d(smem_u32(dst + at * kBN * 128 + j * kPageRows * 128), is_k ? &a.tm_k : &a.tm_v,
-                    at * 64, s_prow[kt * kTilePages + j < kMaxItemPages ? kt * kTilePages + j : 0],
-                    slab, bar);
-    if (is_k) k_pend[b] = kt;
-    else v_pend[b] = kt;
+        tma_load_4d(smem_u32(dst + j * kPageRows * D * 2), &a.tm_v4, 0,
+                    s_prow[kt * kTilePages + j < kMaxItemPages ? kt * kTilePages + j : 0], 0, slab, bar);
+      v_pend[b] = kt;
+    }
   };
 
   // rotated, scaled queries in the swizzled K-major layout; the first R dims
@@ -317,7 +327,7 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
     // start-address field (addresses stay below 256 KB: no carry)
     const uint64_t dq = sdesc(smem_u32(sQ), 16, 1024);
     const uint64_t dk = sdesc(smem_u32(sK), 16, 1024);
-    const uint64_t dv = sdesc(smem_u32(sV), kBN * 128, 1024);
+    const uint64_t dv = sdesc(smem_u32(sV), kPageRows * 128, 1024);   // atoms 2 KB apart in a page
     auto issue_s = [&](int kt) {
       const int b = kt & 1;
       const uint64_t kb = dk + (uint64_t)((b * kBN * D * 2) >> 4);
@@ -383,7 +393,8 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
           for (int u = lane; u < kBN * (D / 64) * 8; u += 32) {
             const int r = u / ((D / 64) * 8), at = (u / 8) % (D / 64), c = u % 8;
             if ((dead >> r) & 1)
-              *reinterpret_cast<uint4*>(vt + at * kBN * 128 + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vt + (r / kPageRows) * kPageRows * D * 2 + at * kPageRows * 128 +
+                                        (r % kPageRows) * 128 + c * 16) = make_uint4(0, 0, 0, 0);
           }
           proxy_fence();
           __syncwarp();
@@ -396,7 +407,7 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
         const uint32_t tSb = tbase + b * kBN;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tO, tSb + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), id_o, kt > 0 || kk > 0);
+          umma_ts(tO, tSb + kk * 8, vb + (uint64_t)((kk * kPageRows * D * 2) >> 4), id_o, kt > 0 || kk > 0);
         umma_commit(mbO0 + 8 * b);
         o_pend[b] = kt;
       }
