@@ -195,10 +195,11 @@ cudaError_t launch_simple_g(const RestoreArgs& a, int G, cudaStream_t st) {
 // rows*128 bytes): Q and K K-major, V (the same bytes as K's layout) read
 // MN-major.  A load warp issues the TMA copies and loads the keys' death
 // times, an MMA warp issues the MMAs (each from one thread, so that neither
-// waits behind the other's issue); eight softmax warps, two per TMEM lane
-// quarter, split each tile's keys and O's columns in halves.  Hand-offs are
-// bounded mbarrier waits.  Two CTAs share an SM (about 103 KB of shared
-// memory and 256 TMEM columns each for D = 128).
+// waits behind the other's issue); four softmax warps, one per TMEM lane
+// quarter, each thread owning a whole query row (all 64 scores of a tile:
+// no exchange between warps for the row maximum).  Hand-offs are bounded
+// mbarrier waits.  Two CTAs share an SM (about 100 KB of shared memory and
+// 256 TMEM columns each for D = 128).
 // ---------------------------------------------------------------------------
 
 constexpr int kBM = 128;   // query rows per CTA
@@ -212,18 +213,17 @@ static_assert(2 * kBN + 128 <= 256, "S buffers and O must fit the TMEM allocatio
 template <int D>
 constexpr size_t restore_tc_smem() {
   return 1024 /* alignment slack */ + (size_t)kBM * D * 2 + 4 * (size_t)kBN * D * 2 +
-         2 * kBN * sizeof(int) + 6 * kBM * sizeof(float) + 4 * sizeof(int) +
-         20 * sizeof(uint64_t) + 16;
+         2 * kBN * sizeof(int) + 4 * sizeof(int) + 12 * sizeof(uint64_t) + 16;
 }
 
-// softmax warps: warp w reads TMEM lanes 32 (w % 4) .. (its rows) and the
-// key half w / 4 of every S tile (and of O's columns); rows are shared by
-// warps w and w + 4, which combine their row maxima through shared memory
-constexpr int kSoftmaxWarps = 8;
+// softmax warps: warp w reads TMEM lanes 32 w .. 32 w + 31 (its rows), all
+// columns of every S tile and of O.  (Eight warps, two per lane quarter
+// splitting the keys and exchanging row maxima through shared memory, ran at
+// 865 against 894 TFLOP/s on the 8B-shaped restore workload.)
+constexpr int kSoftmaxWarps = 4;
 constexpr int kMmaWarp = kSoftmaxWarps;                     // issues the MMAs (one thread)
 constexpr int kLoadWarp = kSoftmaxWarps + 1;                // copies, key deaths
 constexpr int kRestoreThreads = 32 * (kSoftmaxWarps + 2);
-constexpr int kHalf = kBN / 2;                              // keys per softmax warp and tile
 
 template <int D, int NH>
 __global__ void __launch_bounds__(kRestoreThreads, 2)
@@ -236,13 +236,11 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
   uint8_t* sK = sQ + kBM * D * 2;             // [2] kBN x D, TMA 64-element atoms
   uint8_t* sV = sK + 2 * kBN * D * 2;         // [2] same layout, read MN-major
   int* s_death = reinterpret_cast<int*>(sV + 2 * kBN * D * 2);   // [2][kBN]
-  // row maxima of the two halves per tile parity, then the two row sums
-  float* s_mx = reinterpret_cast<float*>(s_death + 2 * kBN);     // [3][2 halves][kBM]
-  int* s_dmin = reinterpret_cast<int*>(s_mx + 6 * kBM);           // [2]
+  int* s_dmin = s_death + 2 * kBN;                                // [2]
   volatile int* s_abort = s_dmin + 2;
-  // S[2] O[2] K[2] V[2] P[2] D[2], then X[4 quarters][2]: row-max exchange of a pair
+  // S[2] O[2] K[2] V[2] P[2] D[2]
   uint64_t* mbar = reinterpret_cast<uint64_t*>(s_dmin + 4);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 20);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 12);
 
   const RestoreTile tl = a.tiles[blockIdx.x];
   const int kvh = blockIdx.y;
@@ -283,13 +281,12 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
     *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dy / 8, kBM)) + dy % 8) = __float2bfloat16_rn(y);
   }
   const uint32_t mbS0 = smem_u32(mbar), mbO0 = smem_u32(mbar + 2), mbK0 = smem_u32(mbar + 4),
-                 mbV0 = smem_u32(mbar + 6), mbP0 = smem_u32(mbar + 8), mbD0 = smem_u32(mbar + 10),
-                 mbX0 = smem_u32(mbar + 12);
+                 mbV0 = smem_u32(mbar + 6), mbP0 = smem_u32(mbar + 8), mbD0 = smem_u32(mbar + 10);
   if (control) {
     if (lane == 0) {
-      for (int i = 0; i < 20; ++i) {
-        // P: one arrival per softmax warp; X: one per warp of the pair
-        const uint32_t cnt = (i == 8 || i == 9) ? kSoftmaxWarps : (i >= 12 ? 2 : 1);
+      for (int i = 0; i < 12; ++i) {
+        // P: one arrival per softmax warp
+        const uint32_t cnt = (i == 8 || i == 9) ? kSoftmaxWarps : 1;
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar + i)), "r"(cnt) : "memory");
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -474,10 +471,9 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
     }
     __syncwarp();
   } else {
-    // ---- softmax warps: row = TMEM lane, keys and O columns split in halves ----
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = 32 * quarter + lane;
-    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    // ---- softmax warps: row = TMEM lane, all of its scores and O columns ----
+    const int row = 32 * warp + lane;
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
     // key j is visible iff lo_r <= j < kend_r and the key is still alive at
     // time_r (keys are born in slot order: "born by time_r" is j < kend_r);
     // padding rows see nothing
@@ -497,7 +493,7 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
     const int w_time = __reduce_max_sync(0xffffffffu, real ? time_r : INT32_MIN);
     for (int kt = 0; kt < n_kt; ++kt) {
       const int b = kt & 1;
-      const int k0 = tl.key_lo + kt * kBN + half * kHalf;
+      const int k0 = tl.key_lo + kt * kBN;
       const uint32_t tSb = tbase + b * kBN;
       bool ok = mbar_wait(mbD0 + 8 * b, (kt >> 1) & 1, a.wait_limit) &&
                 mbar_wait(mbS0 + 8 * b, (kt >> 1) & 1, a.wait_limit);
@@ -507,60 +503,56 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
         break;
       }
       tc_after();
-      uint32_t sr[kHalf];
-      tmem_ld32(tSb + lane_off + half * kHalf, sr);
+      uint32_t sr[kBN];
+#pragma unroll
+      for (int u = 0; u < kBN / 32; ++u) tmem_ld32(tSb + lane_off + 32 * u, sr + 32 * u);
       tmem_wait_ld();
-      const int* de = s_death + b * kBN + half * kHalf;
-      const bool full = k0 >= w_lo && k0 + kHalf <= w_kend && s_dmin[b] > w_time;   // warp-uniform
-      float sv[kHalf];
-      float mx = -INFINITY;
+      const int* de = s_death + b * kBN;
+      const bool full = k0 >= w_lo && k0 + kBN <= w_kend && s_dmin[b] > w_time;   // warp-uniform
+      float sv[kBN];
       if (full) {
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) sv[c] = __uint_as_float(sr[c]);
-#pragma unroll
-        for (int c = 0; c < kHalf; c += 2) mx = fmax3(mx, sv[c], sv[c + 1]);
+        for (int c = 0; c < kBN; ++c) sv[c] = __uint_as_float(sr[c]);
       } else {
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) {
+        for (int c = 0; c < kBN; ++c) {
           const int j = k0 + c;
           const bool vis = j >= lo_r && j < kend_r && de[c] > time_r;
           sv[c] = vis ? __uint_as_float(sr[c]) : -INFINITY;
-          mx = fmaxf(mx, sv[c]);
         }
       }
-      // row max over both halves (bounded exchange with the partner warp)
-      s_mx[(b * 2 + half) * kBM + row] = mx;
-      __syncwarp();
-      const uint32_t xb = mbX0 + 8 * (quarter * 2 + b);
-      if (lane == 0) mbar_arrive(xb);
-      if (!__all_sync(0xffffffffu, mbar_wait(xb, (kt >> 1) & 1, a.wait_limit))) {
-        if (lane == 0) fail();
-        break;
-      }
-      mx = fmaxf(mx, s_mx[(b * 2 + (half ^ 1)) * kBM + row]);
+      // the row maximum in four independent chains (a short dependence path)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < kBN; c += 8)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
+      const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
       // the reference max moves only when the row max grows by more than 2^8
       const float m_new = (mx > m_r + 8.f) ? mx : m_r;
       const float alpha = m_new == -INFINITY ? 1.f : ex2(m_r - m_new);
       const float msub = m_new == -INFINITY ? 0.f : m_new;
       // pairs of scores in packed f32x2 arithmetic: s - m, then the sums
-      uint64_t ps2 = 0;
+      uint64_t ps2[2] = {0, 0};   // two accumulators (a short dependence path)
       const uint64_t neg_m = pack_f32x2(-msub, -msub);
-      uint32_t pk[kHalf / 2];
+      uint32_t pk[kBN / 2];
 #pragma unroll
-      for (int c = 0; c < kHalf; c += 2) {
+      for (int c = 0; c < kBN; c += 2) {
         float d0, d1;
         unpack_f32x2(add_f32x2(pack_f32x2(sv[c], sv[c + 1]), neg_m), d0, d1);
         const float p0 = ex2(d0), p1 = ex2(d1);
-        ps2 = add_f32x2(ps2, pack_f32x2(p0, p1));
+        ps2[(c / 2) & 1] = add_f32x2(ps2[(c / 2) & 1], pack_f32x2(p0, p1));
         pk[c / 2] = pack_bf16x2(p0, p1);
       }
       float ps_lo, ps_hi;
-      unpack_f32x2(ps2, ps_lo, ps_hi);
-      l_r = fmaf(l_r, alpha, ps_lo + ps_hi);     // this half's share of the row sum
+      unpack_f32x2(add_f32x2(ps2[0], ps2[1]), ps_lo, ps_hi);
+      l_r = fmaf(l_r, alpha, ps_lo + ps_hi);
       m_r = m_new;
-      tmem_st16(tSb + lane_off + half * (kHalf / 2), pk);   // P(kt) over S(kt)
+#pragma unroll
+      for (int u = 0; u < kBN / 32; ++u)   // P(kt) over S(kt)
+        tmem_st16(tSb + lane_off + 16 * u, pk + 16 * u);
       if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O is stable once PV(kt-1) is done; this half rescales its columns
+        // O is stable once PV(kt-1) is done: rescale the row
         const bool okv = __all_sync(0xffffffffu, mbar_wait(mbO0 + 8 * ((kt - 1) & 1), ((kt - 1) >> 1) & 1,
                                                            a.wait_limit));
         if (!okv) {
@@ -569,13 +561,13 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
         }
         tc_after();
 #pragma unroll
-        for (int c = 0; c < D / 2; c += 32) {
+        for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
-          tmem_ld32(tO + lane_off + half * (D / 2) + c, o);
+          tmem_ld32(tO + lane_off + c, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + lane_off + half * (D / 2) + c, o);
+          tmem_st32(tO + lane_off + c, o);
         }
       }
       tmem_wait_st();
@@ -589,25 +581,21 @@ k_restore_attn_tc(const __grid_constant__ RestoreArgs a) {
                                                          ((n_kt - 1) >> 1) & 1, a.wait_limit));
       if (!okv && lane == 0) fail();
     }
-    // this half's row sum, combined in the epilogue
-    s_mx[(4 + half) * kBM + row] = l_r;
   }
   tc_before();
   __syncthreads();
   tc_after();
   if (warp < kSoftmaxWarps && n_kt > 0 && !*s_abort) {
-    // epilogue: this half's columns of O / l
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = 32 * quarter + lane;
-    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    // epilogue: the row of O / l (l_r: this thread's row sum)
+    const int row = 32 * warp + lane;
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
     const int hq = kvh * G + blockIdx.z * NH + row % NH;
-    float* po = a.out + ((int64_t)t_r * a.g.hq + hq) * D + half * (D / 2);
-    const float l = s_mx[4 * kBM + row] + s_mx[5 * kBM + row];
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float* po = a.out + ((int64_t)t_r * a.g.hq + hq) * D;
+    const float inv = l_r > 0.f ? 1.f / l_r : 0.f;
 #pragma unroll
-    for (int c = 0; c < D / 2; c += 32) {
+    for (int c = 0; c < D; c += 32) {
       uint32_t o[32];
-      tmem_ld32(tO + lane_off + half * (D / 2) + c, o);
+      tmem_ld32(tO + lane_off + c, o);
       tmem_wait_ld();
       if (t_r < tend) {
 #pragma unroll
