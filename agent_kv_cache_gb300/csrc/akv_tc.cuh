@@ -49,9 +49,10 @@ __device__ __forceinline__ void umma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                ::"r"(mbar) : "memory");
 }
-// Bounded wait for the phase of `parity` to complete; between polls the
-// warp sleeps briefly so that waiting warps leave the issue slots of their
-// sub-partition to the warps doing the softmax.
+// Bounded wait for the phase of `parity` to complete: at most `limit` polls
+// of try_wait, which itself suspends the thread in hardware for a while.  No
+// sleep between polls: each hand-off between the load, MMA and softmax warps
+// sits on a tile's critical path, and a sleep after a failed poll delays it.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i) {
     uint32_t ok;
@@ -59,7 +60,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32
                  "selp.u32 %0, 1, 0, p;\n}\n"
                  : "=r"(ok) : "r"(mbar), "r"(parity) : "memory");
     if (ok) return true;
-    __nanosleep(32);
   }
   return false;
 }
