@@ -206,10 +206,22 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
     if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
       uint4* stage = reinterpret_cast<uint4*>(sV);  // [kBM][kChunks]
       const uint4* qg = static_cast<const uint4*>(a.q);
-      for (int i = tid; i < n_used * kChunks; i += kThreads) {
-        const int row = i / kChunks, ch = i % kChunks;
-        const DecodeMember& mm = s_mem[row / G];
-        stage[i] = qg[((int64_t)mm.row * g.hq + (int64_t)kvh * G + row % G) * kChunks + ch];
+      // four loads in flight per thread before their stores
+      constexpr int kUnroll = 4;
+      for (int i0 = tid; i0 < n_used * kChunks; i0 += kThreads * kUnroll) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int i = i0 + u * kThreads;
+          if (i < n_used * kChunks) {
+            const int row = i / kChunks, ch = i % kChunks;
+            const DecodeMember& mm = s_mem[row / G];
+            v[u] = qg[((int64_t)mm.row * g.hq + (int64_t)kvh * G + row % G) * kChunks + ch];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          if (i0 + u * kThreads < n_used * kChunks) stage[i0 + u * kThreads] = v[u];
       }
     } else {                                        // the caller's q need only be 2-byte aligned
       __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sV);
@@ -228,7 +240,7 @@ k_decode_share_tc(const __grid_constant__ DecodeArgs a) {
     // one (member, pair) per step: one table load, then the member's G
     // heads; kBatch steps' loads are in flight together
     const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(sV);
-    constexpr int kBatch = 8;
+    constexpr int kBatch = 16;
     auto put = [&](int row, int dx, float x) {
       *(reinterpret_cast<__nv_bfloat16*>(sQ + sw128(row, dx / 8, kBM)) + dx % 8) = __float2bfloat16_rn(x);
     };
