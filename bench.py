@@ -299,6 +299,20 @@ class Bench:
         ``host``: pinned host inputs/outputs for the end-to-end variant."""
         c, torch = self.cache, self.torch
         L = SHAPE.layers
+        if host is not None:
+            # every decode step's inputs go up on a copy stream (each step has
+            # its own device slot), overlapping the fork / drop / reposition
+            # and the earlier decode steps; decode step t waits for its copy
+            if not hasattr(self, "_h2d"):
+                self._h2d = torch.cuda.Stream()
+                self._ready = [torch.cuda.Event() for _ in range(DECODE_STEPS)]
+            self._h2d.wait_stream(self.stream)   # the previous pass has read the slots
+            with torch.cuda.stream(self._h2d):
+                for t in range(DECODE_STEPS):
+                    self.q[t].copy_(host["q"][t], non_blocking=True)
+                    self.knew[t].copy_(host["k"][t], non_blocking=True)
+                    self.vnew[t].copy_(host["v"][t], non_blocking=True)
+                    self._ready[t].record(self._h2d)
         forks = [c.seq_fork(b) for b in self.base]
         for f, tr in zip(forks, self.trajs):
             c.drop(f, tr.drop_ranges)
@@ -309,9 +323,7 @@ class Bench:
             ev["repos"][1].record(self.stream)
         for t in range(DECODE_STEPS):
             if host is not None:
-                self.q[t].copy_(host["q"][t], non_blocking=True)
-                self.knew[t].copy_(host["k"][t], non_blocking=True)
-                self.vnew[t].copy_(host["v"][t], non_blocking=True)
+                self.stream.wait_event(self._ready[t])
             c.append(forks, [1] * BATCH, self.knew[t], self.vnew[t])
             # one event pair around the step's L decode calls: an event between
             # two decode calls would end the overlap of their launches
@@ -419,8 +431,9 @@ def gpu_arm(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ms2,
                "what": "public C-ABI calls (fork/drop/reposition/append/decode) with every "
-                       "decode step's q and new K/V copied from pinned host memory and the "
-                       "last layer's attention output copied back"}
+                       "decode step's q and new K/V copied from pinned host memory (on a "
+                       "copy stream, overlapping compute; each decode step waits for its "
+                       "inputs) and the last layer's attention output copied back"}
 
     if rank == 0:
         line = {
