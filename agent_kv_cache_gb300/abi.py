@@ -20,6 +20,8 @@ AKV_ENOPAGES = -4
 AKV_ECAPACITY = -5
 AKV_ECUDA = -6
 AKV_EDEVICE = -7
+AKV_NOALLOC_SCRATCH_BYTES = 8 << 20   # the allocation-free decode's device array
+AKV_NOALLOC_MAX_SEQS = 256
 AKV_DTYPE_BF16 = 0
 AKV_DTYPE_FP32 = 1
 AKV_DERR_PAGE = 0x1
@@ -109,6 +111,7 @@ SIGNATURES = {
     "akv_seq_logical": (ctypes.c_int, [_P, _I64, _PI64]),
     "akv_seq_gather_map": (ctypes.c_int, [_P, _I64, _PI32, _PI64]),
     "akv_seq_page_table": (ctypes.c_int, [_P, _I64, _PI32, _PI32, _PI32, _PI32]),
+    "akv_seq_host_pages": (ctypes.c_int, [_P, _I64, _PI32, _PI32]),
     "akv_history_key": (ctypes.c_int, [_P, _I64, ctypes.POINTER(ctypes.c_uint64)]),
     "akv_page_refcount": (ctypes.c_int, [_P, _I32, _PI32]),
     "akv_pool_stats": (ctypes.c_int, [_P, _PI32, _PI32]),
@@ -288,6 +291,16 @@ def akv_seq_page_table(cache, seq):
     return pages, act
 
 
+def akv_seq_host_pages(cache, seq):
+    """The planner's page table (host state; no wait)."""
+    n = ctypes.c_int32()
+    _check(lib().akv_seq_host_pages(cache, seq, None, ctypes.byref(n)), cache)
+    out = np.zeros(n.value, np.int32)
+    _check(lib().akv_seq_host_pages(cache, seq, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                    ctypes.byref(n)), cache)
+    return out
+
+
 def akv_history_key(cache, seq):
     k = (ctypes.c_uint64 * 2)()
     _check(lib().akv_history_key(cache, seq, k), cache)
@@ -383,7 +396,7 @@ def akv_decode_attention_noalloc(k_slab, v_slab, max_pages, hq, hkv, head_dim, p
     """Decode attention over caller-owned metadata; allocates nothing (see akv.h)."""
     na, pna = _arr(n_active_pages, np.int32, ctypes.c_int32)
     nh, pnh = _arr(n_held, np.int32, ctypes.c_int32)
-    dt = AKV_DTYPE_BF16 if dtype in ("bf16", AKV_DTYPE_BF16) else AKV_DTYPE_FP32
+    dt = {"bf16": AKV_DTYPE_BF16, "fp32": AKV_DTYPE_FP32}.get(dtype, dtype)
     _check(lib().akv_decode_attention_noalloc(
         k_slab, v_slab, max_pages, hq, hkv, head_dim, page_size, dt, float(rope_theta),
         page_table, active_pages, keep_bits, row_stride, keep_stride, pna, pnh, q, out,

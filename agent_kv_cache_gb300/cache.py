@@ -150,15 +150,16 @@ class Cache:
     def sync_errors(self):
         return abi.akv_sync_errors(self.handle)
 
-    def read_kv(self, seq, layer):
-        """Held tokens' stored K and V of one layer, [n_held, hkv, D] (host fp64).
+    def read_kv(self, seq, layer, lo=0, hi=None):
+        """Held tokens' stored K and V of one layer, [n_held, hkv, D] (host fp64);
+        with ``lo`` / ``hi``, only slots [lo, hi).
 
         Reads the pool through the device page table (test introspection).
         """
         torch = self.torch
         n = self.info(seq)["n_held"]
         pages, _ = self.page_table(seq)
-        slots = np.arange(n)
+        slots = np.arange(lo, n if hi is None else min(hi, n))
         pid = torch.from_numpy(pages[slots // self.page].astype(np.int64)).cuda()
         off = torch.from_numpy((slots % self.page).astype(np.int64)).cuda()
         slab = layer % self.phys

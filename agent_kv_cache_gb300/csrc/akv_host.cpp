@@ -175,6 +175,7 @@ struct akv_cache {
   SeqArrays sa{};
   cudaStream_t stream = nullptr;
   float2* d_cs = nullptr;
+  float2* d_cs_lo = nullptr;
   float* d_part_acc = nullptr;
   float2* d_part_ml = nullptr;
   uint32_t* d_err = nullptr;
@@ -343,6 +344,7 @@ void destroy(akv_cache* c) {
   cudaFree(c->sa.gather);
   cudaFree(c->sa.old_pages);
   cudaFree(c->d_cs);
+  cudaFree(c->d_cs_lo);
   cudaFree(c->d_part_acc);
   cudaFree(c->d_part_ml);
   cudaFree(c->d_err);
@@ -428,19 +430,26 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   CKC(cudaMalloc(&sa.gather, ns * (size_t)sa.max_slots * sizeof(int32_t)));
 
   // RoPE table cos/sin(m f_i), m < max_slots, f_i = theta^(-2i/R): fp64,
-  // rounded once to fp32.
+  // rounded once to fp32; and the low parts left by that rounding (fp32),
+  // which the stored-key kernels add back for rotations that nearly cancel.
   {
     const int H = g.rope / 2;
-    std::vector<float2> cs((size_t)f.max_slots * H);
+    std::vector<float2> cs((size_t)f.max_slots * H), lo((size_t)f.max_slots * H);
     std::vector<double> fr(H);
     for (int i = 0; i < H; ++i) fr[i] = std::pow(f.rope_theta, -2.0 * i / g.rope);
     for (int64_t m = 0; m < f.max_slots; ++m)
       for (int i = 0; i < H; ++i) {
         const double ang = (double)m * fr[i];
-        cs[m * H + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        const double co = std::cos(ang), si = std::sin(ang);
+        const float ch = (float)co, sh = (float)si;
+        cs[m * H + i] = make_float2(ch, sh);
+        lo[m * H + i] = make_float2((float)(co - (double)ch), (float)(si - (double)sh));
       }
     CKC(cudaMalloc(&c->d_cs, cs.size() * sizeof(float2)));
     CKC(cudaMemcpy(c->d_cs, cs.data(), cs.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    CKC(cudaMalloc(&c->d_cs_lo, lo.size() * sizeof(float2)));
+    CKC(cudaMemcpy(c->d_cs_lo, lo.data(), lo.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    g.cs_lo = c->d_cs_lo;
   }
   CKC(cudaMalloc(&c->d_part_acc, (size_t)kMaxItems * f.hq * f.head_dim * sizeof(float)));
   CKC(cudaMalloc(&c->d_part_ml, (size_t)kMaxItems * f.hq * sizeof(float2)));
@@ -1902,6 +1911,15 @@ int akv_seq_page_table(akv_cache* c, int64_t seq, int32_t* pages, int32_t* n_pag
     CK(cudaMemcpyAsync(active, c->sa.active + row, (size_t)s->n_active_pages * sizeof(int32_t),
                        cudaMemcpyDeviceToHost, c->stream));
   CK(cudaStreamSynchronize(c->stream));
+  return AKV_OK;
+}
+
+int akv_seq_host_pages(akv_cache* c, int64_t seq, int32_t* pages, int32_t* n_pages) {
+  if (!c || !n_pages) return AKV_EINVAL;
+  HostSeq* s = find(c, seq);
+  if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
+  *n_pages = (int32_t)s->pages.size();
+  if (pages && !s->pages.empty()) std::memcpy(pages, s->pages.data(), s->pages.size() * sizeof(int32_t));
   return AKV_OK;
 }
 

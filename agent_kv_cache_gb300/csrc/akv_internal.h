@@ -23,6 +23,10 @@ struct Geom {
   int64_t head_stride;   // elements between heads (S * D)
   int32_t layers, phys_layers, hq, hkv, d, s, dtype, max_pages;
   int32_t rope;          // rotary dims R (first R dims rotate, the rest are copied)
+  // low parts of the RoPE table, (cos - RN(cos), sin - RN(sin)) in fp32,
+  // [max_slots][R/2]: the stored-key kernels use them for rotations that
+  // nearly cancel (exact rounding to bf16)
+  const float2* cs_lo;
 };
 
 // Per-sequence device arrays, one fixed-size row per device sequence slot

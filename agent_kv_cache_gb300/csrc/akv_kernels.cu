@@ -11,6 +11,7 @@
 // touching memory out of bounds, sets a bit in the device error word and
 // skips the access.
 #include <algorithm>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -64,45 +65,110 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
   *reinterpret_cast<uint4*>(p) = v;
 }
 
+// Exact rounding of nearly cancelling pairs.  The fp32 rotation below,
+// xo = fma(x, c, -RN(y s)) with c, s the table entries rounded once to fp32,
+// is off the exact value by at most 2^-24 (|x c| + |y s|) (table) +
+// 2^-24 |y s| (product) + 2^-24 |xo| (fma), i.e. about 2^-23 |(x, y)|: an
+// error that scales with the pair, not with the element.  Rounding to bf16
+// then lands within one bf16 ulp of the exactly rotated value rounded to
+// nearest even whenever that error is below half the bf16 spacing at the
+// element, 2^-9 |X|, i.e. whenever |X| >= 2^-14 |(x, y)|.  Elements below
+// 2^-13 (|x| + |y|) (rotations that nearly cancel, about 2 pairs in 10^4) are
+// recomputed in compensated fp32: the products with the fp32 table entries
+// exactly (an fma recovers each rounding error), the table's own rounding
+// error from a second fp32 table of low parts (cos - RN(cos), sin - RN(sin)),
+// so the result is the exact rotation to ~2^-46 |(x, y)| before its final
+// roundings.  Every stored bf16 key is then within one bf16 ulp of Eq. (5)
+// evaluated exactly (page 2, 5.5 keeps fp32 arithmetic, which the common
+// path still is).  fp32 pools need no fix-up (their bound is on the pair).
+//
+// The common path only tests; the recomputation is a separate, never-inlined
+// function entered by the few threads that need it (inlined, the compiler
+// predicates it into every element).
+__device__ __forceinline__ bool cancels(float x, float y, float xo, float yo) {
+  return fminf(fabsf(xo), fabsf(yo)) < (fabsf(x) + fabsf(y)) * 0x1p-13f;
+}
+
+// Recompute the cancelling pairs of one unit (E pairs; table entry of pair
+// e at cs[e * stride], its low part at lo[e * stride]) and overwrite them in
+// dst_lo / dst_hi.
+template <int E>
+__device__ __noinline__ void refine_cancelling(uint4 u_lo, uint4 u_hi, __nv_bfloat16* dst_lo,
+                                               __nv_bfloat16* dst_hi, const float2* cs,
+                                               const float2* lo, int stride) {
+  float x[E], y[E];
+  Vec<__nv_bfloat16>::unpack(u_lo, x);
+  Vec<__nv_bfloat16>::unpack(u_hi, y);
+  for (int e = 0; e < E; ++e) {
+    const float2 t = cs[e * stride];
+    const float xo = fmaf(x[e], t.x, -y[e] * t.y);
+    const float yo = fmaf(x[e], t.y, y[e] * t.x);
+    if (!cancels(x[e], y[e], xo, yo)) continue;
+    const float2 l = lo[e * stride];
+    // x (c + cl) - y (s + sl) and x (s + sl) + y (c + cl); each product with
+    // the fp32 entry split into its rounded value and its exact error
+    const float p1 = x[e] * t.x, e1 = fmaf(x[e], t.x, -p1);
+    const float p2 = y[e] * t.y, e2 = fmaf(y[e], t.y, -p2);
+    const float p3 = x[e] * t.y, e3 = fmaf(x[e], t.y, -p3);
+    const float p4 = y[e] * t.x, e4 = fmaf(y[e], t.x, -p4);
+    const float rx = (p1 - p2) + ((e1 - e2) + fmaf(x[e], l.x, -y[e] * l.y));
+    const float ry = (p3 + p4) + ((e3 + e4) + fmaf(x[e], l.y, y[e] * l.x));
+    dst_lo[e] = __float2bfloat16_rn(rx);
+    dst_hi[e] = __float2bfloat16_rn(ry);
+  }
+}
+
 // One rotation unit: E consecutive pairs (i, i + D/2) starting at i = c*E.
 // (x, y) -> (x cos - y sin, x sin + y cos), fp32, rounded once to T.
+// `lo_row`: the low parts of the row's table entries (same layout).
 template <typename T>
 __device__ __forceinline__ void rotate_unit(const T* src, T* dst, int c, int half,
-                                            const float2* cs_row) {
+                                            const float2* cs_row, const float2* lo_row) {
   constexpr int E = Vec<T>::E;
   const uint4 lo = ld16(src + c * E);
   const uint4 hi = ld16(src + half + c * E);
   float x[E], y[E], xo[E], yo[E];
   Vec<T>::unpack(lo, x);
   Vec<T>::unpack(hi, y);
+  bool any = false;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const float2 t = cs_row[c * E + e];
     xo[e] = fmaf(x[e], t.x, -y[e] * t.y);
     yo[e] = fmaf(x[e], t.y, y[e] * t.x);
+    any |= cancels(x[e], y[e], xo[e], yo[e]);
   }
   st16(dst + c * E, Vec<T>::pack(xo));
   st16(dst + half + c * E, Vec<T>::pack(yo));
+  if constexpr (std::is_same<T, __nv_bfloat16>::value)
+    if (any) refine_cancelling<E>(lo, hi, dst + c * E, dst + half + c * E, cs_row + c * E,
+                                  lo_row + c * E, 1);
 }
 
 // The same rotation on a unit already loaded into registers, with the row's
 // cos/sin stored unit-minor: pair c*E + e at cs_t[e * n_units + c], so the
-// lanes rotating one row read consecutive words (no bank conflicts).
+// lanes rotating one row read consecutive words (no bank conflicts); the low
+// parts in lo_t, same layout.
 template <typename T>
 __device__ __forceinline__ void rotate_regs(uint4 lo, uint4 hi, T* dst, int c, int half,
-                                            const float2* cs_t, int n_units) {
+                                            const float2* cs_t, const float2* lo_t, int n_units) {
   constexpr int E = Vec<T>::E;
   float x[E], y[E], xo[E], yo[E];
   Vec<T>::unpack(lo, x);
   Vec<T>::unpack(hi, y);
+  bool any = false;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const float2 t = cs_t[e * n_units + c];
     xo[e] = fmaf(x[e], t.x, -y[e] * t.y);
     yo[e] = fmaf(x[e], t.y, y[e] * t.x);
+    any |= cancels(x[e], y[e], xo[e], yo[e]);
   }
   st16(dst + c * E, Vec<T>::pack(xo));
   st16(dst + half + c * E, Vec<T>::pack(yo));
+  if constexpr (std::is_same<T, __nv_bfloat16>::value)
+    if (any) refine_cancelling<E>(lo, hi, dst + c * E, dst + half + c * E, cs_t + c, lo_t + c,
+                                  n_units);
 }
 
 template <typename T>
@@ -125,7 +191,7 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
          const int32_t* __restrict__ act, const T* __restrict__ k_raw,
          const T* __restrict__ v_raw, int64_t total_tokens,
          const float2* __restrict__ cs, uint32_t* err, AppendLimits lim) {
-  extern __shared__ float2 s_cs[];   // [kAppendTokens][R/2]
+  extern __shared__ float2 s_cs[];   // [kAppendTokens][R/2] cos/sin, then their low parts
   __shared__ int s_page[kAppendTokens];
   __shared__ int s_off[kAppendTokens];
   const AppendBlock blk = blocks[blockIdx.x];
@@ -178,10 +244,12 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     s_off[t] = slot % S;
   }
   const int R = g.rope, RH = R / 2;
+  float2* s_lo = s_cs + kAppendTokens * RH;
   for (int i = tid; i < nt * RH; i += bs) {
     const int slot = it.slot0 + blk.t0 + i / RH;
-    s_cs[i] = (slot >= 0 && slot < sa.max_slots) ? cs[(int64_t)slot * RH + i % RH]
-                                                  : make_float2(1.f, 0.f);
+    const bool in = slot >= 0 && slot < sa.max_slots;
+    s_cs[i] = in ? cs[(int64_t)slot * RH + i % RH] : make_float2(1.f, 0.f);
+    s_lo[i] = in ? g.cs_lo[(int64_t)slot * RH + i % RH] : make_float2(0.f, 0.f);
   }
   __syncthreads();
 
@@ -207,7 +275,7 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
       const int64_t src_off = ((int64_t)l * total_tokens + tok) * g.hkv * D + (int64_t)h * D;
       const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
       if (r < kr) {
-        rotate_unit<T>(kb + src_off, kp + slab + dst_off, r, RH, s_cs + t * RH);
+        rotate_unit<T>(kb + src_off, kp + slab + dst_off, r, RH, s_cs + t * RH, s_lo + t * RH);
       } else if (r < kr + kc) {
         const int o = R + (r - kr) * E;
         st16(kp + slab + dst_off + o, ld16(kb + src_off + o));
@@ -430,14 +498,16 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, uint32_t li
 // The staged tile pipeline shared by the reposition gather and the prefix
 // fork: for every (layer, KV head) tile of destination page `dpage`, rows
 // t of the stage receive source rows (s_src_page[t], s_src_off[t]) through
-// one bulk copy per run, keys with s_rot[t] are rotated in place with the
-// row's cos/sin (s_cs, unit-minor), and rows [0, n_store) go out with one
+// one bulk copy per run, keys with s_rot[t] set are rotated in place with the
+// row's cos/sin (s_cs, unit-minor; their low parts in s_lo, same layout),
+// and rows [0, n_store) go out with one
 // bulk copy per tensor.  Rows without a source (dead slots of a prefix fork)
 // are written as zeros, so that a stored slot never holds stale bits.  Layers
 // l_begin..l_end-1 map to slab l % phys_layers.
 template <typename T>
 __device__ __forceinline__ void tile_pipeline(
-    const Geom& g, int l_begin, int l_end, unsigned char* stage0, const float2* s_cs, const int* s_src_page,
+    const Geom& g, int l_begin, int l_end, unsigned char* stage0, const float2* s_cs,
+    const float2* s_lo, const int* s_src_page,
     const int* s_src_off, const int* s_rot, const int* s_run_t0, const int* s_run_len, int n_runs,
     uint32_t bytes, int dpage, int n_store, int n_stages, uint64_t* s_full, uint32_t* err,
     uint32_t wait_limit) {
@@ -488,7 +558,7 @@ __device__ __forceinline__ void tile_pipeline(
       T* row = kt + (size_t)t * D;
       const uint4 lo = *reinterpret_cast<const uint4*>(row + c * E);
       const uint4 hi = *reinterpret_cast<const uint4*>(row + RH + c * E);
-      rotate_regs<T>(lo, hi, row, c, RH, s_cs + t * RH, kr);
+      rotate_regs<T>(lo, hi, row, c, RH, s_cs + t * RH, s_lo + t * RH, kr);
     }
     if (n_dead > 0) {
       const int ch = (int)(row_bytes / 16);      // 16-byte chunks of a row
@@ -559,6 +629,7 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
   const uint32_t tile_bytes = S * row_bytes;                 // one (layer, head) tile of one tensor
   unsigned char* stage0 = gsm;                                // [n_stages][K, V][S][D]
   float2* s_cs = reinterpret_cast<float2*>(gsm + (size_t)n_stages * 2 * tile_bytes);   // [S][R/2]
+  float2* s_lo = s_cs + S * RH;                                                         // [S][R/2]
   __shared__ int s_src_page[64], s_src_off[64], s_rot[64];
   __shared__ int s_run_t0[64], s_run_len[64], s_n_runs, s_dst_page;
   __shared__ uint32_t s_bytes;
@@ -592,9 +663,13 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
     for (int i = tid; i < nj * RH; i += kGatherThreads) {
       const int t = i / RH, jj = i % RH;
       const int delta = gather[j0 + t] - (j0 + t);
-      float2 c = make_float2(1.f, 0.f);
-      if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * RH + jj];
+      float2 c = make_float2(1.f, 0.f), l = make_float2(0.f, 0.f);
+      if (delta >= 0 && delta < sa.max_slots) {
+        c = cs[(int64_t)delta * RH + jj];
+        l = g.cs_lo[(int64_t)delta * RH + jj];
+      }
       s_cs[t * RH + (jj % E) * kr + jj / E] = make_float2(c.x, -c.y);
+      s_lo[t * RH + (jj % E) * kr + jj / E] = make_float2(l.x, -l.y);
     }
   }
   if (tid == 0) {
@@ -612,7 +687,7 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
   if (dpage < 0) return;
   const int lper = (g.layers + gridDim.y - 1) / gridDim.y;    // layers of this block
   tile_pipeline<T>(g, blockIdx.y * lper, min(g.layers, (int)(blockIdx.y + 1) * lper), stage0, s_cs,
-                   s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes, dpage, nj,
+                   s_lo, s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes, dpage, nj,
                    n_stages, s_full, err, wait_limit);
 }
 
@@ -637,6 +712,7 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
   const uint32_t tile_bytes = S * row_bytes;
   unsigned char* stage0 = gsm;                                // [n_stages][K, V][S][D]
   float2* s_cs = reinterpret_cast<float2*>(gsm + (size_t)n_stages * 2 * tile_bytes);   // [S][R/2]
+  float2* s_lo = s_cs + S * RH;                                                         // [S][R/2]
   __shared__ int s_src_page[64], s_src_off[64], s_rot[64], s_delta[64];
   __shared__ int s_run_t0[64], s_run_len[64], s_n_runs, s_n_store;
   __shared__ uint32_t s_bytes;
@@ -678,7 +754,9 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
     const int delta = s_delta[t];
     const int a = delta < 0 ? -delta : delta;
     const float2 c = a < max_pos ? cs[(int64_t)a * RH + j] : make_float2(1.f, 0.f);
+    const float2 l = a < max_pos ? g.cs_lo[(int64_t)a * RH + j] : make_float2(0.f, 0.f);
     s_cs[t * RH + (j % E) * kr + j / E] = make_float2(c.x, delta < 0 ? -c.y : c.y);
+    s_lo[t * RH + (j % E) * kr + j / E] = make_float2(l.x, delta < 0 ? -l.y : l.y);
   }
   if (tid == 0) {
     for (int st = 0; st < n_stages; ++st)
@@ -689,7 +767,7 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
   __syncthreads();
   const int lper = (g.phys_layers + gridDim.y - 1) / gridDim.y;   // slabs of this block
   tile_pipeline<T>(g, blockIdx.y * lper, min(g.phys_layers, (int)(blockIdx.y + 1) * lper), stage0,
-                   s_cs, s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes,
+                   s_cs, s_lo, s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes,
                    mb.dst_page, n_store, n_stages, s_full, err, wait_limit);
 }
 
@@ -721,7 +799,7 @@ cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves,
   const size_t elem = g.dtype == AKV_DTYPE_BF16 ? 2 : 4;
   const size_t tile = (size_t)g.s * g.d * elem;
   const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
-  const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
+  const size_t smem = (size_t)n_stages * 2 * tile + 2 * (size_t)g.s * (g.rope / 2) * sizeof(float2);
   const dim3 grid(n_blocks, layer_groups(n_blocks, g.phys_layers));
   if (g.dtype == AKV_DTYPE_BF16) {
     cudaFuncSetAttribute(k_transplant<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -741,7 +819,7 @@ cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* 
                           int64_t total_tokens, const float2* cs, uint32_t* err,
                           AppendLimits lim, cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
-  const size_t smem = (size_t)kAppendTokens * (g.rope / 2) * sizeof(float2);
+  const size_t smem = 2 * (size_t)kAppendTokens * (g.rope / 2) * sizeof(float2);
   const dim3 grid(n_blocks, g.phys_layers == g.layers ? g.layers : 1);
   if (g.dtype == AKV_DTYPE_BF16)
     k_append<__nv_bfloat16><<<grid, 256, smem, st>>>(
@@ -786,7 +864,7 @@ cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* i
   const size_t elem = g.dtype == AKV_DTYPE_BF16 ? 2 : 4;
   const size_t tile = (size_t)g.s * g.d * elem;             // one (layer, head) tile, one tensor
   const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
-  const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
+  const size_t smem = (size_t)n_stages * 2 * tile + 2 * (size_t)g.s * (g.rope / 2) * sizeof(float2);
   const dim3 grid(n_blocks, layer_groups(n_blocks, g.layers));
   if (g.dtype == AKV_DTYPE_BF16) {
     cudaFuncSetAttribute(k_gather<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

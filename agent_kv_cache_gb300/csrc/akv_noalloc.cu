@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(kWarps * 32) k_noalloc_decode(const __grid_con
       s_q[gq][d] = fmaf(x, c, -y * sn) * a.scale_log2;
       s_q[gq][d + H] = fmaf(x, sn, y * c) * a.scale_log2;
     }
+  } else {
+    // no token held (the host rejects active pages then): defined scores
+    for (int i = tid; i < G * D; i += blockDim.x) s_q[i / D][i % D] = 0.f;
   }
   __syncthreads();
 
@@ -234,6 +237,8 @@ extern "C" int akv_decode_attention_noalloc(
   for (int i = 0; i < n_seqs; ++i) {
     if (n_active_pages[i] < 0 || n_active_pages[i] > row_stride) return AKV_EINVAL;
     if (n_held[i] < 0 || (int64_t)n_held[i] > (int64_t)keep_stride * 32) return AKV_EINVAL;
+    // an active page needs a held token, whose position the query takes
+    if (n_active_pages[i] > 0 && n_held[i] < 1) return AKV_EINVAL;
     total += n_active_pages[i];
     longest = n_active_pages[i] > longest ? n_active_pages[i] : longest;
   }

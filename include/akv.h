@@ -254,7 +254,8 @@ int akv_restore_attention(akv_cache* cache, const akv_op* ops, int32_t n_ops, in
  * It covers the plain method: full-width RoPE and full attention (no
  * rope_dim, no window).
  * Errors: AKV_ECAPACITY when n_seqs > AKV_NOALLOC_MAX_SEQS; AKV_EINVAL for
- * a bad shape or pointer; AKV_ECUDA when a launch fails. */
+ * a bad shape or pointer, or a sequence with active pages but no held token;
+ * AKV_ECUDA when a launch fails. */
 #define AKV_NOALLOC_SCRATCH_BYTES (8 << 20)
 #define AKV_NOALLOC_MAX_SEQS 256
 int akv_decode_attention_noalloc(
@@ -284,6 +285,12 @@ int akv_seq_gather_map(akv_cache* cache, int64_t seq, int32_t* map, int64_t* n);
  * NULL output is skipped; counts are always set. */
 int akv_seq_page_table(akv_cache* cache, int64_t seq, int32_t* pages,
                        int32_t* n_pages, int32_t* active, int32_t* n_active);
+
+/* The planner's page table of a sequence: pool page per slot page, -1 once
+ * released (host output of n_pages entries; *n_pages is always set).  It is
+ * host state and needs no wait: the device table holds the same once the
+ * cache's stream reaches the calls made so far. */
+int akv_seq_host_pages(akv_cache* cache, int64_t seq, int32_t* pages, int32_t* n_pages);
 
 /* 128-bit key of the sequence's operation history (Eq. 6): equal histories
  * give equal keys; different ones differ (with overwhelming probability).

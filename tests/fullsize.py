@@ -14,7 +14,7 @@ import torch
 
 from agent_kv_cache_gb300 import Cache
 from oracle.akv_oracle import OracleCache
-from twin import ATTN_TOL, key_tolerance, key_ulp_fraction
+from twin import ATTN_TOL, check_key_step, key_tolerance, key_ulp_fraction
 from workloads import device, synth
 
 
@@ -96,6 +96,7 @@ class FullSize:
             del keep
         layers = [self.writer_layer(p) for p in self.sample_layers]
         for s in seqs:
+            h0 = self.meta.seqs[self.om[s]].alive.size
             self.meta.append(self.om[s], np.zeros((0, n, H, D)), np.zeros((0, n, H, D)))
             if s in self.ok:
                 kk = synth.kv_tokens(self.seed, self.tags[s], synth.KIND_K, layers, starts[s], n,
@@ -103,6 +104,12 @@ class FullSize:
                 vv = synth.kv_tokens(self.seed, self.tags[s], synth.KIND_V, layers, starts[s], n,
                                      H, D, self.width)
                 self.kv.append(self.ok[s], kk, vv)
+                # step-wise: the new keys are R(pos) of their raw bits, rounded once
+                pos = self.meta.seqs[self.om[s]].pos[h0:h0 + n]
+                got = np.stack([self.gpu.read_kv(s, slab, h0, h0 + n)[0]
+                                for slab in self.sample_layers], axis=1)
+                check_key_step(got, kk.transpose(1, 0, 2, 3), np.zeros_like(pos), pos,
+                               self.kv.freq, sh.dtype, "append")
 
     def drop(self, s, ranges):
         self.gpu.drop(s, ranges)
@@ -111,6 +118,19 @@ class FullSize:
             self.kv.drop(self.ok[s], ranges)
 
     def reposition(self, seqs):
+        # the key bits the kernel will read, for the sampled sequences, first
+        # against the oracle's own state (chained bound)
+        before = {}
+        for s in seqs:
+            if s not in self.ok:
+                continue
+            st = self.kv.seqs[self.ok[s]]
+            src = np.flatnonzero(st.alive)
+            k_old = np.stack([self.gpu.read_kv(s, slab)[0] for slab in self.sample_layers])
+            ref = st.K[:, src]
+            err = np.abs(k_old[:, src] - ref)
+            assert not (err > key_tolerance(ref, self.shape.dtype, self.rot[s])).any()
+            before[s] = (k_old[:, src], st.pos[src].copy())
         self.gpu.reposition(seqs)
         for s in seqs:
             st = self.meta.seqs[self.om[s]]
@@ -119,6 +139,14 @@ class FullSize:
             self.meta.reposition(self.om[s])
             if s in self.ok:
                 self.kv.reposition(self.ok[s])
+        # step-wise: survivor j is the key read from its old slot, rotated
+        # from its old position to j
+        torch.cuda.synchronize()
+        for s, (k_src, p_old) in before.items():
+            r = p_old.size
+            got = np.stack([self.gpu.read_kv(s, slab, 0, r)[0] for slab in self.sample_layers])
+            check_key_step(got.transpose(1, 0, 2, 3), k_src.transpose(1, 0, 2, 3), p_old,
+                           np.arange(r), self.kv.freq, self.shape.dtype, "reposition")
 
     # -- checks -------------------------------------------------------------
     def check_metadata(self):

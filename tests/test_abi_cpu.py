@@ -65,3 +65,15 @@ def test_null_handles_are_rejected(lib):
     cfg = abi.make_config(1, 8, 2, 64, 16, "fp32", 40, 1, 600, 1e4)
     # null pools are rejected before any CUDA call
     assert lib.akv_cache_create(ctypes.byref(cfg), None, None, 0, None, ctypes.byref(out)) == abi.AKV_EINVAL
+
+
+def test_binding_constants_match_the_header():
+    text = open(HEADER).read()
+    for name in ("AKV_NOALLOC_SCRATCH_BYTES", "AKV_NOALLOC_MAX_SEQS", "AKV_OK", "AKV_EINVAL",
+                 "AKV_ECAPACITY"):
+        m = re.search(r"#define\s+%s\s+(.+)" % name, text)
+        if m is None:
+            m = re.search(r"\b%s\s*=\s*([^,\n]+)" % name, text)
+        assert m is not None, name
+        value = re.sub(r"/\*.*", "", m.group(1)).strip().rstrip(",")
+        assert eval(value) == getattr(abi, name), name

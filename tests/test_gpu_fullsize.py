@@ -207,7 +207,7 @@ def test_prefix_fork_llama8b_fullsize():
     tokens."""
     import oracle.akv_prefix as P
     from agent_kv_cache_gb300 import PrefixIndex
-    from twin import key_tolerance
+    from twin import check_key_step, key_tolerance
     sh = traces.LLAMA8B
     seed = traces.seed_for(5)
     turns = traces.turn_programs(seed)
@@ -282,7 +282,29 @@ def test_prefix_fork_llama8b_fullsize():
                 oc.reposition(osid)
         os_ = oc.seqs[osid]
         assert np.array_equal(os_.logical, held)
+        # step-wise, every needed token: the child's key is the entry's stored
+        # key rotated from its stored position to the request's; the entry's
+        # keys are first checked against the oracle replay of its own program
+        eo = OracleCache(sh.hq, H, D, sh.rope_theta, sh.dtype, layers=(0,), page_size=S)
+        esid = eo.create()
+        tt = 0
+        for op in hist:
+            if op[0] == "append":
+                eo.append(esid, synth.kv_tokens(seed, 1, synth.KIND_K, [0], tt, op[1], H, D, w),
+                          synth.kv_tokens(seed, 1, synth.KIND_V, [0], tt, op[1], H, D, w))
+                tt += op[1]
+            elif op[0] == "drop":
+                eo.drop(esid, op[1])
+            else:
+                eo.reposition(esid)
+        src = np.array([stored[x] for x in need], dtype=np.int64)
+        dst = np.array([st.pos[x] for x in need], dtype=np.int64)
+        ke, _ = gpu.read_kv(last, 0)
         kg, vg = gpu.read_kv(child, 0)
+        eref = eo.seqs[esid].K[0][src]
+        n_rot_e = 1 + sum(1 for r in er if r[0] == "R")
+        assert not (np.abs(ke[src] - eref) > key_tolerance(eref, sh.dtype, n_rot_e)).any()
+        check_key_step(kg[dst], ke[src], src, dst, oc.freq, sh.dtype, kind)
         rng = np.random.default_rng(3)
         live_slots = np.flatnonzero(os_.alive)
         pick = rng.choice(live_slots, size=min(512, live_slots.size), replace=False)

@@ -19,7 +19,7 @@ import torch
 from agent_kv_cache_gb300 import Cache, PrefixIndex, abi, build
 import oracle.akv_prefix as P
 from oracle.akv_oracle import OracleCache
-from twin import ATTN_TOL, key_tolerance
+from twin import ATTN_TOL, check_key_step, key_tolerance
 from workloads import synth
 
 pytestmark = pytest.mark.gpu
@@ -182,6 +182,22 @@ def _check_child(f, child, req, m, entry_recs):
         tol = key_tolerance(ref, f.dtype, n_rot)
         assert not (err > tol).any(), (l, err.max())
         np.testing.assert_array_equal(v[live], os_.V[l][live])
+    # step-wise: each needed key is the entry's stored key, read from its slot
+    # (its stored position) and rotated to the request's position; the
+    # entry's stored keys are first checked against a cache built from the
+    # entry's own records (chained bound)
+    eo, esid = f.oracle(entry_recs)
+    es = eo.seqs[esid]
+    n_rot_e = sum(1 for r in entry_recs if r[0] == "R") + 1
+    mv = sorted(plan["moves"].values())
+    dst = np.array([x[0] for x in mv], dtype=np.int64)
+    src = np.array([x[1] for x in mv], dtype=np.int64)
+    for l in range(f.L):
+        ke, _ = f.gpu.read_kv(m["entry"], l)
+        k, _ = f.gpu.read_kv(child, l)
+        ref = es.K[l][src]
+        assert not (np.abs(ke[src] - ref) > key_tolerance(ref, f.dtype, n_rot_e)).any()
+        check_key_step(k[dst], ke[src], src, dst, oc.freq, f.dtype, "prefix fork")
 
 
 @pytest.mark.parametrize("dtype,D,G,S", [("bf16", 64, 4, 16), ("bf16", 128, 8, 16),

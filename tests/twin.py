@@ -1,25 +1,41 @@
 """Drive the CUDA library and the CPU oracle with the same seeded inputs.
 
-Inputs come from ``workloads.synth`` only (values exact in the pool dtype);
-the oracle never sees anything produced by the CUDA path.
+Inputs come from ``workloads.synth`` only (values exact in the pool dtype).
+The oracle's state is built from those inputs alone and every comparison of
+the chained kind below is against that state.  The step-wise key check is
+the one place where the oracle's rotation function is applied to key bits
+read from the pool: the bits one step starts from, which are first checked
+against the oracle's own state (chained bound); almost all of them are
+bit-identical to it.
 
 Tolerances (derived from the arithmetic):
 
 * indices, keep masks, positions, gather maps, active page lists: bit-exact;
 * V: bit-exact (it is only copied);
-* K: every stored key went through r roundings to the pool dtype (the
-  append plus each reposition that moved it).  One rotation of a pair
-  (x, y) in fp32 with table cos/sin rounded once from fp64 is off the exact
-  value by at most about 4 * 2^-24 * |(x, y)| before the final rounding, so
-  a single step lands within 1 ulp of the oracle's RNE(exact) (the bound the
-  method states).  Over a chain, the two sides start each later rotation
-  from inputs that may differ by 1 ulp per component; a rotation preserves
-  the norm of that difference and spreads it over both components, so the
-  bound per element is
+* K, step-wise (the bound the method states for Eq. (5)): every key write --
+  the rotation of an append, of a reposition, of a prefix fork -- is checked
+  against the oracle applied to the exact bits the kernel read
+  (``oracle.reposition_key`` from the old position p to the new position q,
+  in fp64, rounded to the pool dtype, RNE).  bf16 pools: every element within
+  1 bf16 ulp of that value.  fp32 pools: within 4 * 2^-24 * |(x, y)| (one
+  rotation in fp32 from a table rounded once from fp64 -- table, product and
+  fma roundings, 3 * 2^-24 |(x, y)| -- plus the oracle's own rounding of the
+  result).  Both allow, on top, 2^-50 (|p| + |q| + 4) |(x, y)|: a bound on
+  the fp64 evaluation error of the rotation angles p f_i and q f_i (f_i <= 1),
+  which is what separates the oracle's value from the exact one (about 10^-6
+  of a bf16 ulp at typical magnitudes).  A key whose position does not change
+  must be bit-identical to what was read; dims past the rotary part too.
+* K, chained (the whole history against the oracle's own chain): every
+  stored key went through r roundings to the pool dtype (the append plus
+  each reposition that moved it), and the two sides start each later
+  rotation from inputs that may already differ by 1 ulp per component; a
+  rotation preserves the norm of that difference and spreads it over both
+  components, so the bound per element is
       ulp(ref) + (r - 1) * sqrt(2) * 2^(1-p) * |(x, y)| + r * 8 * 2^-24 * |(x, y)|
   (p = 8 significant bits for bf16, 24 for fp32; ulp(v) <= 2^(1-p) |v|).
   Every element must meet it, and at least 99% of the elements must lie
-  within r ulp of the oracle (the per-step bound applied r times).
+  within r ulp of the oracle.  This compounding is not a kernel error: the
+  step-wise check pins each step to 1 ulp.
 * attention output (fp32): max abs error <= 1e-2 and mean abs error <= 1e-3
   for bf16 pools; 1e-4 / 1e-5 for fp32 pools.
 """
@@ -27,7 +43,7 @@ import numpy as np
 import torch
 
 from agent_kv_cache_gb300 import Cache
-from oracle.akv_oracle import OracleCache
+from oracle.akv_oracle import OracleCache, reposition_key, to_pool
 from workloads import synth
 
 ATTN_TOL = {"bf16": (1e-2, 1e-3), "fp32": (1e-4, 1e-5)}
@@ -58,6 +74,39 @@ def key_tolerance(ref, dtype, n_rot, rope_dim=0):
             + r * 8 * 2.0 ** -24 * norm)
 
 
+def check_key_step(got, src, p, q, freq, dtype, what=""):
+    """Step-wise check of key writes: ``src`` [n, ..., D] are the stored key
+    bits a kernel read (fp64 copies of pool values; the raw input for an
+    append, with p = 0), ``got`` what it stored, each row rotated from
+    position p[n] to q[n] (Eq. 5; Eq. 3 for an append).  ``freq`` holds the
+    rotary frequencies (its length is half the rotary width).  Returns the
+    largest error in units of the bf16/fp32 bound (<= 1 passes)."""
+    got = np.asarray(got, dtype=np.float64)
+    src = np.asarray(src, dtype=np.float64)
+    p = np.asarray(p, dtype=np.int64)
+    q = np.asarray(q, dtype=np.int64)
+    if got.shape[0] == 0:
+        return 0.0
+    shp = (-1,) + (1,) * (src.ndim - 2)
+    rw = 2 * len(freq)
+    same = p == q
+    # unmoved keys and the dims past the rotary part: bit copies
+    np.testing.assert_array_equal(got[same], src[same], err_msg=what)
+    np.testing.assert_array_equal(got[..., rw:], src[..., rw:], err_msg=what)
+    want = to_pool(reposition_key(src, p.reshape(shp), q.reshape(shp), freq), dtype)
+    norm = _pair_norm(src, rw)[..., :rw]
+    slack = 2.0 ** -50 * (np.abs(p) + np.abs(q) + 4).astype(np.float64).reshape(shp + (1,)) * norm
+    if dtype == "bf16":
+        tol = ulp(want[..., :rw], dtype) + slack
+    else:
+        tol = 4 * 2.0 ** -24 * norm + slack
+    err = np.abs(got[..., :rw] - want[..., :rw])
+    bad = err > tol
+    assert not bad.any(), (what, int(bad.sum()), err[bad][:4], want[..., :rw][bad][:4],
+                           tol[bad][:4])
+    return float((err / np.maximum(tol, 1e-300)).max())
+
+
 def key_ulp_fraction(err, ref, dtype, n_rot, rope_dim=0):
     """Fraction of elements within n_rot ulp of the oracle."""
     r = max(n_rot, 1)
@@ -82,6 +131,8 @@ class Twin:
         self.o = {}        # gpu seq id -> oracle seq id
         self.tag = {}      # gpu seq id -> input stream tag
         self.rot = {}      # gpu seq id -> rotations a key may have gone through
+        self.same_bits = 0  # reposition inputs bit-identical to the oracle's state
+        self.all_bits = 0
         self.next_tag = 1
         self.tdtype = torch.bfloat16 if dtype == "bf16" else torch.float32
 
@@ -125,22 +176,63 @@ class Twin:
             ids = None if token_ids is None else token_ids[tok:tok + n]
             self.orc.append(self.o[g], k, v, ids)
             tok += n
+        starts = {g: self.gpu.info(g)["n_held"] for g in seqs}
         kt = torch.from_numpy(np.concatenate(ks, axis=1)).to(self.tdtype).cuda().contiguous()
         vt = torch.from_numpy(np.concatenate(vs, axis=1)).to(self.tdtype).cuda().contiguous()
         self.gpu.append(list(seqs), list(ns), kt, vt, token_ids)
         torch.cuda.synchronize()
+        # step-wise: each new key is R(pos) of its raw bits, rounded once
+        for g, n, k in zip(seqs, ns, ks):
+            if n == 0:
+                continue
+            h0 = starts[g]
+            pos = self.orc.seqs[self.o[g]].pos[h0:h0 + n]
+            got = self._keys(g)[:, h0:h0 + n]                   # [L][n][hkv][D]
+            src = np.asarray(k, dtype=np.float64)
+            check_key_step(got.transpose(1, 0, 2, 3), src.transpose(1, 0, 2, 3),
+                           np.zeros_like(pos), pos, self.orc.freq, self.dtype, "append")
 
     def drop(self, g, ranges):
         self.gpu.drop(g, ranges)
         self.orc.drop(self.o[g], ranges)
 
+    def _keys(self, g):
+        """Stored keys of every layer, [L][n_held][hkv][D] (fp64 copy)."""
+        if self.gpu.info(g)["n_held"] == 0:
+            return np.zeros((self.L, 0, self.hkv, self.d))
+        return np.stack([self.gpu.read_kv(g, l)[0] for l in range(self.L)])
+
     def reposition(self, seqs):
+        before = {}
+        for g in seqs:
+            st = self.orc.seqs[self.o[g]]
+            k_old = self._keys(g)
+            src = np.flatnonzero(st.alive)
+            # the bits the kernel will read, against the oracle's own state
+            ref = st.K[:, src]
+            err = np.abs(k_old[:, src] - ref)
+            assert not (err > key_tolerance(ref, self.dtype, self.rot[g],
+                                            self.orc.rope_dim)).any()
+            self.same_bits += int((err == 0).sum())
+            self.all_bits += err.size
+            before[g] = (k_old, st.pos.copy(), src)
         self.gpu.reposition(list(seqs))
         for g in seqs:
             st = self.orc.seqs[self.o[g]]
             if not (st.alive.all() and np.array_equal(st.pos, np.arange(st.alive.size))):
                 self.rot[g] += 1
             self.orc.reposition(self.o[g])
+        # step-wise: survivor j is the key read from its old slot, rotated
+        # from its old position to j
+        torch.cuda.synchronize()
+        for g in seqs:
+            k_old, pos_old, src = before[g]
+            if src.size == 0:
+                continue
+            got = self._keys(g)[:, :src.size]
+            check_key_step(got.transpose(1, 0, 2, 3), k_old[:, src].transpose(1, 0, 2, 3),
+                           pos_old[src], np.arange(src.size), self.orc.freq, self.dtype,
+                           "reposition")
 
     def set_window(self, layer, window):
         self.gpu.set_layer_window(layer, window)
