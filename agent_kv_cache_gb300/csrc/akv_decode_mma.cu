@@ -112,6 +112,39 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
+// Which split of the call the blocks use (DecodeArgs::items_w): decided by
+// the first block of the call to get here, from whether every block of the
+// previous decode call had finished its work by then; the others read that
+// decision.  Only this call's blocks write its word (the word of call c is
+// reused by call c + 8, which cannot start before every block of call c has
+// passed this point and signalled its dependents).  1: the whole-wave split.
+__device__ __forceinline__ uint32_t choose_split(const DecodeArgs& a) {
+  const uint32_t id = a.call_id & 0x1fffffffu;
+  uint32_t* word = a.mode_words + (a.call_id % kDecodeModeWords);
+  uint32_t v = *reinterpret_cast<volatile uint32_t*>(word);
+  if ((v >> 3) != id) {
+    const uint32_t done = *reinterpret_cast<volatile uint32_t*>(a.done_word);
+    const uint32_t want = (id << 3) | (done + 1 == a.call_id ? 1u : 0u);
+    const uint32_t prev = atomicCAS(word, v, want);
+    v = prev == v ? want : prev;                // else another block of this call chose
+  }
+  return v & 7u;
+}
+
+// A block of the call has done its work: count it (one atomic add; a loop
+// of compare-and-swap on one word serialises the call's blocks); the last
+// one resets the count for the call that reuses the word and publishes the
+// call as finished.  Read by the next call's choice only, so a count that
+// goes astray (a block that stopped on an error) costs a plan choice,
+// never a result.
+__device__ __forceinline__ void count_exit(const DecodeArgs& a) {
+  uint32_t* cnt = a.exit_words + (a.call_id % kDecodeExitWords);
+  if (atomicAdd(cnt, 1u) + 1u == gridDim.x * gridDim.y) {
+    atomicExch(cnt, 0u);
+    atomicMax(a.done_word, a.call_id);
+  }
+}
+
 // A member (query row) must name memory this call owns.
 __device__ __forceinline__ bool member_ok(const DecodeMember& m, const DecodeArgs& a) {
   return m.row >= 0 && m.row < a.n_rows && m.row < a.counter_rows && m.n_splits >= 1 &&
@@ -143,10 +176,27 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   __shared__ DecodeMember s_mem[SHARE ? kDecodeMaxMembers : 1];
   __shared__ int s_lastm[SHARE ? kDecodeMaxMembers : 1];
 
+  // the split this call uses (one of two when the planner made a whole-wave
+  // split too), chosen before the next call may start
+  const DecodeItem* items = a.items;
+  int n_items = a.n_items;
+  if (a.n_items_w > 0 && a.call_id > 0) {
+    __shared__ uint32_t s_split;
+    if (threadIdx.x == 0) s_split = choose_split(a);
+    __syncthreads();
+    if (s_split == 1) {
+      items = a.items_w;
+      n_items = a.n_items_w;
+    }
+  }
   // the next decode call may be scheduled now: its blocks start as this
   // grid's blocks retire and wait (griddepcontrol.wait) before writing
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const DecodeItem it = a.items[blockIdx.x];
+  if ((int)blockIdx.x >= n_items) {             // the grid is sized for the larger split
+    if (threadIdx.x == 0 && a.call_id > 0) count_exit(a);
+    return;
+  }
+  const DecodeItem it = items[blockIdx.x];
   const int kvh = blockIdx.y;
   const Geom& g = a.g;
   const int G = g.hq / g.hkv;
@@ -473,6 +523,7 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
       if (d == 0) a.part_ml[pi] = make_float2(M, L);
     }
   }
+  if (tid == 0 && a.call_id > 0) count_exit(a);
   if (!multi) return;
 
   // for each member, the last split of (row, kv head) to finish merges all
@@ -654,7 +705,7 @@ bool make_pool_tensor_maps(const Geom& g, CUtensorMap* tk, CUtensorMap* tv) {
 // copy, the caller's kernels) never signals early, so for it the ordering is
 // the plain stream order.
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
-  const dim3 grid(a.n_items, a.g.hkv);
+  const dim3 grid(a.n_items_w > a.n_items ? a.n_items_w : a.n_items, a.g.hkv);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);

@@ -41,8 +41,8 @@ constexpr int kMaxMembers = 16384;         // members of shared decode items per
 constexpr int kMinSharedPages = 4;         // shorter runs of common pages are read per row
 constexpr int kShareRows = 128;            // query rows of a shared-prefix (tensor-core) item
 constexpr int kShareMaxMembers = 128;
-constexpr int kSharePagesMin = 32;         // pages per shared-prefix item (the kernel takes <= 64)
-constexpr int kSharePagesMax = 64;
+constexpr int kSharePagesMin = 32;         // pages per shared-prefix item (the kernel takes <= 128)
+constexpr int kSharePagesMax = 128;
 
 // 128-bit key of an operation history: two independent 64-bit chains, each
 // step finished with the MurmurHash3 64-bit finaliser (Appleby).
@@ -196,6 +196,8 @@ struct akv_cache {
     int members = 0;
     int sitems = 0;           // tensor-core shared-prefix items
     size_t o_sitems = 0;
+    int items_w = 0;          // the same call split for a whole wave (0: none)
+    size_t o_items_w = 0;
     size_t o_members = 0;
     uint64_t used = 0;
   };
@@ -233,6 +235,11 @@ struct akv_cache {
     std::vector<Segment> shared;
   } share_cache;
   int32_t* d_counters = nullptr;   // fused split merge: finished splits per (row, kv head)
+  // device plan choice of the one-row decode kernel: per-call words
+  uint32_t* d_mode = nullptr;          // [kDecodeModeWords]
+  uint32_t* d_exits = nullptr;         // [kDecodeExitWords]
+  uint32_t* d_done = nullptr;
+  uint32_t decode_call = 0;            // id of the last one-row decode call
   void* d_restore = nullptr;       // temporary key/value versions of restore attention
   size_t restore_cap = 0;
   void* d_fork = nullptr;          // descriptor of a prefix fork
@@ -350,6 +357,9 @@ void destroy(akv_cache* c) {
   cudaFree(c->d_err);
   for (auto& pl : c->plans) cudaFree(pl.d);
   cudaFree(c->d_counters);
+  cudaFree(c->d_mode);
+  cudaFree(c->d_exits);
+  cudaFree(c->d_done);
   cudaFree(c->d_restore);
   cudaFree(c->d_fork);
   for (Stage& s : c->stages) {
@@ -455,7 +465,7 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   CKC(cudaMalloc(&c->d_part_ml, (size_t)kMaxItems * f.hq * sizeof(float2)));
   CKC(cudaMalloc(&c->d_err, sizeof(uint32_t)));
   CKC(cudaMemset(c->d_err, 0, sizeof(uint32_t)));
-  c->plan_cap = kMaxItems * sizeof(DecodeItem) + 2 * ns * sizeof(int32_t) +
+  c->plan_cap = 2 * kMaxItems * sizeof(DecodeItem) + 2 * ns * sizeof(int32_t) +
                 kMaxMembers * sizeof(DecodeMember) + kMaxItems * sizeof(ShareItem) + 96;
   for (auto& pl : c->plans) CKC(cudaMalloc(&pl.d, c->plan_cap));
   c->stage_bytes = std::max<size_t>(1 << 20, 8 * (size_t)f.max_pages + 96 * ns +
@@ -468,6 +478,12 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   }
   CKC(cudaMalloc(&c->d_counters, (size_t)kMaxItems * f.hkv * sizeof(int32_t)));
   CKC(cudaMemset(c->d_counters, 0, (size_t)kMaxItems * f.hkv * sizeof(int32_t)));
+  CKC(cudaMalloc(&c->d_mode, kDecodeModeWords * sizeof(uint32_t)));
+  CKC(cudaMemset(c->d_mode, 0, kDecodeModeWords * sizeof(uint32_t)));
+  CKC(cudaMalloc(&c->d_exits, kDecodeExitWords * sizeof(uint32_t)));
+  CKC(cudaMemset(c->d_exits, 0, kDecodeExitWords * sizeof(uint32_t)));
+  CKC(cudaMalloc(&c->d_done, sizeof(uint32_t)));
+  CKC(cudaMemset(c->d_done, 0, sizeof(uint32_t)));
   c->use_mma = make_pool_tensor_maps(g, &c->tm_k, &c->tm_v) &&
                make_pool_tensor_maps4(g, &c->tm_k4, &c->tm_v4);
   if (c->use_mma) {
@@ -1086,7 +1102,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       }
       total += hs[i]->n_active_pages - first[i];
     }
-    std::vector<DecodeItem> items;
+    std::vector<DecodeItem> items, items_w;
     std::vector<DecodeMember> members;
     std::vector<ShareItem> sitems;
     std::vector<int32_t> item0(n_seqs), splits(n_seqs);
@@ -1128,7 +1144,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       std::vector<Segment> segs, tsegs;   // one-row kernel / tensor-core shared-prefix kernel
       // share: 0 none, 1 tensor-core shared-prefix items, 2 shared items of
       // the one-row kernel (at most `mcap` rows each)
-      auto plan_mma = [&](int share, int mcap) -> int {
+      auto plan_mma = [&](int share, int mcap, int64_t min_waves) -> int {
         segs.clear();
         tsegs.clear();
         sitems.clear();
@@ -1189,7 +1205,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
         const int64_t resident = (int64_t)c->sm_count * c->mma_blocks_per_sm;
         const int64_t quarter = std::max<int64_t>(1, resident / 4);
         const int64_t pairs = (int64_t)segs.size() * c->cfg.hkv;
-        const int64_t waves = std::max<int64_t>(c->decode_waves, (pairs + quarter - 1) / quarter);
+        const int64_t waves = std::max<int64_t>(min_waves, (pairs + quarter - 1) / quarter);
         int64_t target = std::max<int64_t>((int64_t)segs.size(), waves * quarter / c->cfg.hkv);
         // A consumer warp of an item with nb column blocks reads nb/4 of the
         // tiles (one row: a quarter), so the work of a split, the cap of
@@ -1231,6 +1247,14 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
         // the longest of them off the critical path
         if (!tsegs.empty()) target = std::max<int64_t>(target, resident / c->cfg.hkv);
         target = std::min<int64_t>(std::max(target, sum), kMaxItems);
+        // a call with nothing to overlap its end with (a whole-wave split, or
+        // one-row items next to shared-prefix items) runs whole waves of
+        // blocks: a partial last wave would leave the rest of the GPU idle
+        if (min_waves >= 4 || !tsegs.empty()) {
+          const int64_t per_wave = std::max<int64_t>(1, resident / c->cfg.hkv);
+          if (target > per_wave)
+            target = std::min<int64_t>(kMaxItems, (target + per_wave - 1) / per_wave * per_wave);
+        }
         while (sum < target && !pq.empty()) {
           Entry e = pq.top();
           pq.pop();
@@ -1349,13 +1373,29 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       }
       const int mode = !share ? 0 : (c->decode_share == 1 && decode_share_supported(c->g)) ? 1 : 2;
       const int mcap = c->decode_share > 1 ? c->decode_share : std::max(1, 16 / G);
-      int rc = plan_mma(mode, std::min(mcap, 32 / G));
+      int rc = plan_mma(mode, std::min(mcap, 32 / G), c->decode_waves);
+      bool plain = mode == 0;
       if (rc && mode) {
         std::fill(splits.begin(), splits.end(), 0);
-        rc = plan_mma(0, 1);
+        rc = plan_mma(0, 1, c->decode_waves);
+        plain = true;
       }
       if (rc) return fail(c, AKV_ECAPACITY, "decode needs more than %d work items", kMaxItems);
       combine = false;                                 // merged inside the kernel
+      // Calls without shared items get a second split for a whole wave of
+      // blocks; the kernel takes it when the call runs on its own (see
+      // DecodeArgs::items_w).  The quarter-wave split above is best when
+      // calls come back to back, and a call on its own would leave three
+      // quarters of the GPU idle with it.
+      if (plain && c->decode_waves < 4) {
+        std::vector<DecodeItem> q_items = std::move(items);
+        std::vector<int32_t> q_item0 = item0, q_splits = splits;
+        std::fill(splits.begin(), splits.end(), 0);
+        if (plan_mma(0, 1, 4) == AKV_OK && items.size() > q_items.size()) items_w = std::move(items);
+        items = std::move(q_items);
+        item0 = std::move(q_item0);
+        splits = std::move(q_splits);
+      }
     } else {
       // split so that the (item, kv head) blocks fill the GPU a few times over
       const int64_t tgt = (int64_t)c->sm_count * 8;
@@ -1377,6 +1417,7 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
     blob.put(splits.data(), splits.size());
     const size_t o_members = blob.put(members.data(), members.size());
     const size_t o_sitems = blob.put(sitems.data(), sitems.size());
+    const size_t o_items_w = blob.put(items_w.data(), items_w.size());
     if (blob.b.size() > c->plan_cap) return fail(c, AKV_ECAPACITY, "decode plan too large");
     plan = &c->plans[0];
     for (auto& pl : c->plans)
@@ -1398,6 +1439,8 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
     plan->o_members = o_members;
     plan->sitems = (int)sitems.size();
     plan->o_sitems = o_sitems;
+    plan->items_w = (int)items_w.size();
+    plan->o_items_w = o_items_w;
   }
   plan->used = ++c->plan_clock;
   c->last_items = plan->items + plan->sitems;
@@ -1435,6 +1478,15 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
   a.shared = plan->shared;
   a.share_items = reinterpret_cast<const ShareItem*>(plan->d + plan->o_sitems);
   a.n_share_items = plan->sitems;
+  a.items_w = reinterpret_cast<const DecodeItem*>(plan->d + plan->o_items_w);
+  a.n_items_w = plan->items_w;
+  a.mode_words = c->d_mode;
+  a.exit_words = c->d_exits;
+  a.done_word = c->d_done;
+  if (c->use_mma && plan->items > 0) {
+    if (++c->decode_call >= (1u << 29)) c->decode_call = 1;   // the words keep 29 bits of it
+    a.call_id = c->decode_call;
+  }
   if (plan->sitems > 0) {
     CK(launch_decode_share(a, c->stream));
     ++c->launches;

@@ -145,7 +145,20 @@ struct DecodeArgs {
   int32_t shared;       // the plan has shared items
   const ShareItem* share_items;   // tensor-core shared-prefix items (before the others)
   int32_t n_share_items;
+  // Plan choice made on the device (tensor-core one-row kernel): items_w is
+  // the same call split for a whole wave of blocks (0: no second plan).  The
+  // call's first block takes it iff the previous decode call had finished
+  // (nothing of it left to overlap with: a call on its own), else the
+  // call keeps `items` (a quarter wave: room for its neighbours' blocks).
+  const DecodeItem* items_w;
+  int32_t n_items_w;
+  uint32_t call_id;             // > 0, one per call of this cache
+  uint32_t* mode_words;         // [8] (call_id << 3 | plan) once a call has chosen
+  uint32_t* exit_words;         // [1024] blocks of call c exited, at c % 1024
+  uint32_t* done_word;          // last call whose blocks have all exited
 };
+constexpr int kDecodeModeWords = 8;
+constexpr int kDecodeExitWords = 1024;
 constexpr int kDecodeMaxTiles = 512;   // 16-token tiles in one split of the tensor-core path
 // bound of the waits that let a kernel's own copies / MMAs land before it
 // exits after a failed wait (independent of the user's wait limit)

@@ -213,10 +213,10 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
   const int tid = threadIdx.x, bs = blockDim.x;
   const int64_t row_base = (int64_t)it.dslot;
 
-  // blockIdx.y picks the layer when every logical layer has its own slab;
-  // with aliased slabs one block walks all layers in order (last one wins)
-  const int l_begin = gridDim.y > 1 ? (int)blockIdx.y : 0;
-  const int l_end = gridDim.y > 1 ? (int)blockIdx.y + 1 : g.layers;
+  // blockIdx.y picks the physical slab; the block writes the logical layers
+  // stored there in order (y, y + phys_layers, ...; with one slab per layer
+  // that is one layer), so the last of them is what the slab keeps
+  const int l_begin = blockIdx.y, l_step = g.phys_layers;
   const bool meta = blockIdx.y == 0;
 
   if (blk.t0 == 0 && meta) {
@@ -271,7 +271,7 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     const int64_t tok = it.tok0 + blk.t0 + t;
     const int64_t dst_off = (int64_t)pid * g.page_stride + (int64_t)h * g.head_stride +
                             (int64_t)s_off[t] * D;
-    for (int l = l_begin; l < l_end; ++l) {
+    for (int l = l_begin; l < g.layers; l += l_step) {
       const int64_t src_off = ((int64_t)l * total_tokens + tok) * g.hkv * D + (int64_t)h * D;
       const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
       if (r < kr) {
@@ -820,7 +820,7 @@ cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* 
                           AppendLimits lim, cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
   const size_t smem = 2 * (size_t)kAppendTokens * (g.rope / 2) * sizeof(float2);
-  const dim3 grid(n_blocks, g.phys_layers == g.layers ? g.layers : 1);
+  const dim3 grid(n_blocks, g.phys_layers);
   if (g.dtype == AKV_DTYPE_BF16)
     k_append<__nv_bfloat16><<<grid, 256, smem, st>>>(
         g, sa, items, blocks, ids, act, static_cast<const __nv_bfloat16*>(k_raw),

@@ -69,6 +69,10 @@ TRACE120B = dict(name="gptoss120b", shape=traces.GPTOSS120B, batch=4, n_tokens=1
                  decode=256, seed=traces.seed_for(2))
 BRANCH = dict(shape=traces.LLAMA8B, prefix=16384, branches=64, decode=128,
               seed=traces.seed_for(3))
+# profiler case of the 70B shape (not a block): 8 sequences of 40960 tokens
+# with ~60% dropped, about the steady state's ~16K active tokens per sequence
+TRACE70B = dict(name="llama70b", shape=traces.LLAMA70B, batch=8, n_tokens=40960, decode=4,
+                seed=traces.seed_for(4))
 
 
 def load_peaks():
@@ -570,12 +574,15 @@ class Steady:
         if host is not None:
             if not hasattr(self, "_h2d"):
                 self._h2d = torch.cuda.Stream()
+                self._d2h = torch.cuda.Stream()
                 self._tool_ready = [torch.cuda.Event() for _ in self.groups]
                 self._ready = [torch.cuda.Event() for _ in range(STEADY_DECODE)]
+                self._done = [torch.cuda.Event() for _ in range(STEADY_DECODE)]
                 self._prefetched = None
             if self._prefetched != k:          # nothing prefetched: copy now
                 self._h2d.wait_stream(st)
                 self._tool_copy(k, host)
+            st.wait_stream(self._d2h)          # the previous turn's outputs have been read
         if ev is not None:
             ev["append"][0].record(st)
         for gi, g in enumerate(self.groups):
@@ -611,11 +618,18 @@ class Steady:
             if ev is not None:
                 ev["dec"][t][0].record(st)
             for l in range(L):
-                c.decode_attention(l, self.q[t, l], self.seqs, self.out[l])
+                # the last layer's output of every step has its own device
+                # slot, read back on a stream of its own (a read-back on the
+                # compute stream would wait behind the input copies)
+                dst = host["out_dev"][t] if host is not None and l == L - 1 else self.out[l]
+                c.decode_attention(l, self.q[t, l], self.seqs, dst)
             if ev is not None:
                 ev["dec"][t][1].record(st)
             if host is not None:
-                host["out"][t].copy_(self.out[L - 1], non_blocking=True)
+                self._done[t].record(st)
+                self._d2h.wait_event(self._done[t])
+                with torch.cuda.stream(self._d2h):
+                    host["out"][t].copy_(host["out_dev"][t], non_blocking=True)
         self._drop_repos(k, ev)
 
     def _tool_copy(self, k, host):
@@ -642,6 +656,7 @@ class Steady:
              "kn": pin(self.knew), "vn": pin(self.vnew),
              "out": torch.empty((STEADY_DECODE, STEADY_SEQS, self.sh.hq, self.sh.head_dim),
                                 dtype=torch.float32, pin_memory=True)}
+        h["out_dev"] = torch.empty(h["out"].shape, dtype=torch.float32, device="cuda")
         h["slots"] = [(self.kraw, self.vraw)] + [
             (torch.empty(n, dtype=torch.bfloat16, device="cuda"),
              torch.empty(n, dtype=torch.bfloat16, device="cuda"))
@@ -684,7 +699,7 @@ class TraceBench:
         self.sh, self.name = sh, spec["name"]
         self.B = batch or spec["batch"]
         self.N, self.DEC, self.seed = spec["n_tokens"], decode or spec["decode"], spec["seed"]
-        mk = traces.llama8b_batch if spec["name"] == "llama8b" else traces.gptoss_batch
+        mk = traces.gptoss_batch if spec["name"] == "gptoss120b" else traces.llama8b_batch
         self.trajs = mk(self.seed, batch=max(self.B, spec["batch"]), n_total=self.N)[:self.B]
         S, L, H, D, Hq = sh.page_size, sh.layers, sh.hkv, sh.head_dim, sh.hq
         kvt = kvt_of(sh)
@@ -839,7 +854,7 @@ class TraceBench:
 
     def workload(self):
         sh = self.sh
-        pct = {"llama8b": "~60%", "gptoss120b": "~80%"}[self.name]
+        pct = {"llama8b": "~60%", "gptoss120b": "~80%", "llama70b": "~60%"}[self.name]
         return (f"{sh.name}-shaped agent trace: {sh.layers} layers, {sh.hq}/{sh.hkv} heads, "
                 f"head_dim {sh.head_dim}, {sh.dtype}, rope theta {sh.rope_theta:g}, page "
                 f"{sh.page_size}; batch {self.B} x {self.N} logical tokens, tool spans dropped "
@@ -864,14 +879,18 @@ class BranchBench:
     is), 128 decode steps x (append + decode attention on all 32 layers)
     over all 64 branches, free the branches."""
 
-    def __init__(self, rank):
+    def __init__(self, rank, layers=None):
+        import dataclasses
         import torch
         from agent_kv_cache_gb300 import Cache, build
         from workloads import device as dev
         self.torch, self.dev = torch, dev
         build()
         dev.build()
-        sh = self.sh = BRANCH["shape"]
+        sh = BRANCH["shape"]
+        if layers:
+            sh = dataclasses.replace(sh, layers=layers)
+        self.sh = sh
         P, NB, DEC, seed = BRANCH["prefix"], BRANCH["branches"], BRANCH["decode"], BRANCH["seed"]
         self.P, self.NB, self.DEC, self.seed = P, NB, DEC, seed
         _, self.branches = traces.branching(seed, n_branches=NB, prefix_len=P)
@@ -1622,7 +1641,11 @@ def gpu_arm(args):
     with Clocks(gpu_id(local)) as clk:
         start.record(b.stream)
         for i in range(K):
+            if args.nvtx:
+                torch.cuda.nvtx.range_push("turn")
             b.turn(STEADY_FIRST + i, ev=evs[i])
+            if args.nvtx:
+                torch.cuda.nvtx.range_pop()
         stop.record(b.stream)
         torch.cuda.synchronize()
     barrier()
@@ -1662,27 +1685,33 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         barrier()
         s2, e2 = events(torch, 1)[0]
+        evs2 = [b.events() for _ in range(K)]
         s2.record(b.stream)
         for i in range(K):
-            b.turn(k0 + 1 + i, host=host)
+            b.turn(k0 + 1 + i, ev=evs2[i], host=host)
         e2.record(b.stream)
         torch.cuda.synchronize()
         barrier()
         assert b.cache.sync_errors() == 0
         ms2 = reduce_max(s2.elapsed_time(e2) / K, dist, "cuda")
         tot2 = sum(b.acct[k0 + 1 + i]["total"] for i in range(K))
+        dec2 = np.array([[s_.elapsed_time(e_) / L for s_, e_ in ev["dec"]] for ev in evs2])
+        app2 = [ev["append"][0].elapsed_time(ev["append"][1]) for ev in evs2]
         e2e = {"value": round(world * tot2 / (ms2 * K * 1e-3) / 1e9, 1), "unit": "GB/s",
                "h2d_bytes_per_step": int(np.mean([b.h2d_bytes(k0 + 1 + i) for i in range(K)])),
                "d2h_bytes_per_step": int(host["out"].numel() * 4),
                "ms_per_step": round(ms2, 3),
                "turns": f"{k0 + 2}..{k0 + 1 + K}",
+               "decode_avg_call_us": round(float(np.mean(dec2)) * 1e3, 2),
+               "decode_ms_per_turn": round(float(np.sum(dec2)) * L / K, 1),
+               "append_ms_per_turn": round(float(np.mean(app2)), 3),
                "what": "public C-ABI calls (append / decode / drop / reposition) with every "
                        "turn's inputs copied from pinned host memory on a copy stream: its "
                        "tool responses' raw K/V during the previous turn's decode (one device "
                        "slot per group of 16 sequences; each group's append waits for its "
                        "copy), its decode steps' queries and new-token K/V while its decode "
                        "runs (each step waits for its own); every decode step's last-layer "
-                       "attention output copied back"}
+                       "attention output copied back on a third stream"}
         del host
     b.close()
 
@@ -1766,10 +1795,10 @@ def only_arm(args):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     name = args.only
     if name == "branching":
-        b = BranchBench(0)
+        b = BranchBench(0, layers=args.layers)
     else:
-        b = TraceBench(TRACE8B if name == "llama8b" else TRACE120B, 0, batch=args.batch,
-                       layers=args.layers, decode=args.decode_steps)
+        spec = {"llama8b": TRACE8B, "gptoss120b": TRACE120B, "llama70b": TRACE70B}[name]
+        b = TraceBench(spec, 0, batch=args.batch, layers=args.layers, decode=args.decode_steps)
     res = b.run(args.warmup, args.steps)
     line = {"metric": METRIC, "value": res["gbs"], "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
@@ -1819,8 +1848,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-blocks", action="store_true",
                     help="headline only (no 8B / 120B / branching blocks)")
-    ap.add_argument("--only", choices=["llama8b", "gptoss120b", "branching"], default=None,
-                    help="one block's workload as its own line")
+    ap.add_argument("--only", choices=["llama8b", "gptoss120b", "branching", "llama70b"],
+                    default=None, help="one block's workload (or the 70B-shaped profiler "
+                                       "case) as its own line")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="wrap each timed turn in an NVTX range 'turn' (profiler launch lists)")
     ap.add_argument("--restore", action="store_true",
                     help="time segment-batch restore attention instead (its own line)")
     ap.add_argument("--restore-cuda-cores", action="store_true")

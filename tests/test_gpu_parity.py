@@ -12,8 +12,8 @@ import pytest
 import torch
 
 from agent_kv_cache_gb300 import abi, build
-from workloads import traces
-from twin import Twin
+from workloads import synth, traces
+from twin import ATTN_TOL, Twin
 
 pytestmark = pytest.mark.gpu
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
@@ -614,3 +614,48 @@ def test_bounded_waits_time_out_and_recover():
     t.restore(prog)
     for g in seqs:
         t.check(g)
+
+
+def test_decode_back_to_back_and_one_at_a_time():
+    """The one-row decode kernel splits a call for a quarter of the GPU's
+    block slots when decode calls come back to back (the next call's blocks
+    start in the rest) and for a whole wave when a call runs on its own; the
+    choice is made on the device, per call.  Calls enqueued back to back
+    (three rounds over every layer, no wait in between) and the same calls
+    one at a time (a synchronisation before each) must all match the oracle,
+    and both sets must agree within the attention tolerance."""
+    build()
+    t = Twin(layers=4, hq=32, hkv=8, head_dim=128, page_size=16, dtype="bf16", rope_theta=5e5,
+             max_pages=2048, max_seqs=8, max_slots=4096, seed=21)
+    seqs = [t.create() for _ in range(4)]
+    t.append(seqs, [3000, 1000, 2500, 400])
+    t.drop(seqs[0], [(100, 900)])
+    t.drop(seqs[2], [(2000, 2400)])
+    t.reposition([seqs[0], seqs[2]])
+    t.append(seqs, [1, 1, 1, 1])
+    L = t.L
+    q = [np.stack([synth.query(t.seed, t.tag[s], l, 0, t.hq, t.d, t.width) for s in seqs])
+         for l in range(L)]
+    qd = [torch.from_numpy(x).to(torch.bfloat16).cuda() for x in q]
+    want = [t.orc.attention(l, q[l], [t.o[s] for s in seqs]) for l in range(L)]
+    outs = [torch.empty((len(seqs), t.hq, t.d), dtype=torch.float32, device="cuda")
+            for _ in range(3 * L)]
+    torch.cuda.synchronize()
+    for r in range(3):
+        for l in range(L):
+            t.gpu.decode_attention(l, qd[l], seqs, out=outs[r * L + l])
+    torch.cuda.synchronize()
+    alone = []
+    for l in range(L):
+        torch.cuda.synchronize()
+        alone.append(t.gpu.decode_attention(l, qd[l], seqs).clone())
+        torch.cuda.synchronize()
+    tmax, tmean = ATTN_TOL["bf16"]
+    for i, o in enumerate(outs + alone):
+        l = i % L
+        err = np.abs(o.double().cpu().numpy() - want[l])
+        assert err.max() <= tmax and err.mean() <= tmean, (i, err.max(), err.mean())
+    for l in range(L):
+        d = (outs[l] - alone[l]).abs()
+        assert d.max().item() <= tmax and d.mean().item() <= tmean
+    assert t.gpu.sync_errors() == 0
