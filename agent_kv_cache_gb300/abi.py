@@ -368,7 +368,9 @@ def akv_set_decode_waves(cache, waves):
 
 
 def akv_set_restore_tensor_cores(cache, enable):
-    _check(lib().akv_set_restore_tensor_cores(cache, 1 if enable else 0), cache)
+    """0/False: CUDA cores; 1/True: tensor cores, two query tiles per CTA
+    (default); 2: tensor cores, one query tile per CTA."""
+    _check(lib().akv_set_restore_tensor_cores(cache, int(enable)), cache)
 
 
 def akv_set_decode_sharing(cache, mode):

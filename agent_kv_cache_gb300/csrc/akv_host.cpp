@@ -245,6 +245,7 @@ struct akv_cache {
   void* d_fork = nullptr;          // descriptor of a prefix fork
   size_t fork_cap = 0;
   bool restore_generic = false;    // CUDA-core restore kernel for every shape
+  bool restore_pairs = true;       // tensor-core restore: two query tiles per CTA
 };
 
 namespace {
@@ -1578,10 +1579,25 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
       t = e;
     }
   }
+  // two-tile form: consecutive tiles of one era share a CTA (the later one's
+  // key range extends the earlier one's by its own tokens)
+  std::vector<int2> pairs;
+  if (mma && c->restore_pairs) {
+    for (size_t i = 0; i < tiles.size();) {
+      if (i + 1 < tiles.size() && tiles[i + 1].era_off == tiles[i].era_off) {
+        pairs.push_back(make_int2((int)i, (int)i + 1));
+        i += 2;
+      } else {
+        pairs.push_back(make_int2((int)i, -1));
+        i += 1;
+      }
+    }
+  }
   Blob blob;
   const size_t o_keys = blob.put(keys.data(), keys.size());
   const size_t o_q = blob.put(queries.data(), queries.size());
   const size_t o_t = blob.put(tiles.data(), tiles.size());
+  const size_t o_p = blob.put(pairs.data(), pairs.size());
   // scratch: [K versions | V versions | descriptor]
   const size_t elem = c->cfg.dtype == AKV_DTYPE_BF16 ? 2 : 4;
   const size_t half = (keys.size() * (size_t)c->cfg.hkv * c->cfg.head_dim * elem + 255) & ~size_t(255);
@@ -1600,6 +1616,8 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
   RestoreArgs a{};
   a.tiles = reinterpret_cast<const RestoreTile*>(d + o_t);
   a.n_tiles = (int32_t)tiles.size();
+  a.pairs = reinterpret_cast<const int2*>(d + o_p);
+  a.n_pairs = (int32_t)pairs.size();
   a.use_mma = mma;
   a.wait_limit = c->wait_limit;
   if (mma && !make_restore_tensor_maps(c->g, c->d_restore, static_cast<char*>(c->d_restore) + half,
@@ -2034,8 +2052,9 @@ int akv_decode_plan_stats(akv_cache* c, int32_t* items, int32_t* shared_items, i
 }
 
 int akv_set_restore_tensor_cores(akv_cache* c, int32_t enable) {
-  if (!c || (enable != 0 && enable != 1)) return AKV_EINVAL;
+  if (!c || enable < 0 || enable > 2) return AKV_EINVAL;
   c->restore_generic = enable == 0;
+  c->restore_pairs = enable == 1;
   return AKV_OK;
 }
 

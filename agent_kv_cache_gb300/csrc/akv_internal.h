@@ -190,6 +190,10 @@ struct RestoreArgs {
   uint32_t* err;
   const RestoreTile* tiles;   // tensor-core path only
   int32_t n_tiles;
+  // two-tile tensor-core kernel: (tile A, tile B or -1) per CTA, consecutive
+  // tiles of one era; 0 pairs: one tile per CTA
+  const int2* pairs;
+  int32_t n_pairs;
   int32_t use_mma;
   uint32_t wait_limit;        // bounded waits of the tensor-core path
 };

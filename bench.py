@@ -1142,7 +1142,8 @@ def restore_arm(args):
         for l in range(sh.layers):
             cache.restore_attention(prog, l, q, k, v, out=out)
     torch.cuda.synchronize()
-    assert cache.sync_errors() == 0
+    w = cache.sync_errors()
+    assert w == 0, f"device error word 0x{w:x} after the warm-up"
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps * sh.layers)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -334,8 +334,9 @@ int akv_decode_plan_stats(akv_cache* cache, int32_t* items, int32_t* shared_item
                           int32_t* members);
 
 /* Kernel choice for akv_restore_attention: 1 (default) = tensor-core
- * kernel where it applies (bf16 pool, D 64 or 128), 0 = the CUDA-core
- * kernel for every shape.  Both compute the same attention. */
+ * kernel where it applies (bf16 pool, D 64 or 128) with two query tiles
+ * per CTA, 2 = the tensor-core kernel with one query tile per CTA, 0 = the
+ * CUDA-core kernel for every shape.  All compute the same attention. */
 int akv_set_restore_tensor_cores(akv_cache* cache, int32_t enable);
 
 /* Number of kernels this cache has launched since creation. */

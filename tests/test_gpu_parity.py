@@ -260,20 +260,25 @@ def _random_program(rng, n_tokens, n_ops):
 
 
 RESTORE = [
-    # dtype, page, G, D, rope_dim, window, tensor cores
-    ("bf16", 16, 4, 128, 0, 0, True),
-    ("bf16", 16, 4, 128, 0, 0, False),
-    ("bf16", 16, 8, 64, 0, 0, True),
-    ("bf16", 16, 8, 64, 0, 0, False),
-    ("bf16", 16, 1, 128, 0, 0, True),
-    ("bf16", 16, 2, 64, 0, 0, True),
-    ("bf16", 8, 16, 64, 32, 0, True),
-    ("fp32", 16, 2, 64, 0, 0, True),
-    ("bf16", 16, 4, 128, 64, 0, True),
-    ("bf16", 16, 4, 128, 64, 0, False),
-    ("bf16", 16, 4, 128, 0, 24, True),
-    ("bf16", 16, 2, 128, 0, 100, True),
-    ("fp32", 4, 16, 128, 32, 7, True),
+    # dtype, page, G, D, rope_dim, window, kernel (1: tensor cores, two query
+    # tiles per CTA; 2: tensor cores, one tile per CTA; 0: CUDA cores)
+    ("bf16", 16, 4, 128, 0, 0, 1),
+    ("bf16", 16, 4, 128, 0, 0, 2),
+    ("bf16", 16, 4, 128, 0, 0, 0),
+    ("bf16", 16, 8, 64, 0, 0, 1),
+    ("bf16", 16, 8, 64, 0, 0, 2),
+    ("bf16", 16, 8, 64, 0, 0, 0),
+    ("bf16", 16, 1, 128, 0, 0, 1),
+    ("bf16", 16, 2, 64, 0, 0, 1),
+    ("bf16", 8, 16, 64, 32, 0, 1),
+    ("bf16", 8, 16, 64, 32, 0, 2),
+    ("fp32", 16, 2, 64, 0, 0, 1),
+    ("bf16", 16, 4, 128, 64, 0, 1),
+    ("bf16", 16, 4, 128, 64, 0, 0),
+    ("bf16", 16, 4, 128, 0, 24, 1),
+    ("bf16", 16, 4, 128, 0, 24, 2),
+    ("bf16", 16, 2, 128, 0, 100, 1),
+    ("fp32", 4, 16, 128, 32, 7, 1),
 ]
 
 
@@ -282,7 +287,7 @@ RESTORE = [
 def test_restore_attention_random_programs(dtype, page, G, D, R, W, tc, seed):
     """Every appended token's restore attention equals its attention at the
     time it was appended (oracle replay), keys dropped later included.
-    bf16 runs both the tensor-core and the CUDA-core kernel."""
+    bf16 runs the tensor-core kernel in both forms and the CUDA-core one."""
     rng = np.random.default_rng(seed * 100 + D + G + R + W)
     t = Twin(layers=2, hq=2 * G, hkv=2, head_dim=D, page_size=page, dtype=dtype,
              rope_theta=1e4, max_pages=512, max_seqs=4, max_slots=2048, seed=seed, rope_dim=R)
@@ -304,7 +309,7 @@ def test_restore_attention_random_programs(dtype, page, G, D, R, W, tc, seed):
     t.check(s)
 
 
-@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("tc", [1, 2, 0])
 def test_restore_attention_long_program(tc):
     """A 2000-token program with few repositions: eras of thousands of keys
     (many 64-key tiles per query tile), drops that empty whole tiles, and a
