@@ -696,14 +696,14 @@ bool make_pool_tensor_maps(const Geom& g, CUtensorMap* tk, CUtensorMap* tv) {
   return true;
 }
 
-// Launched with programmatic stream serialisation: when the previous work on
-// the stream is a decode call (which signals launch_dependents at its start),
-// this grid's blocks may start while that grid's last blocks still run, so
-// its start-up (work item, tile list, query) hides behind the other's tail.
-// A decode call reads nothing a decode call writes before its
-// griddepcontrol.wait; any other predecessor (append, drop, reposition, a
-// copy, the caller's kernels) never signals early, so for it the ordering is
-// the plain stream order.
+// Launched with programmatic stream serialisation when the previous work on
+// the stream is a decode call (a.pdl; such a call signals launch_dependents
+// at its start): this grid's blocks may start while that grid's last blocks
+// still run, so its start-up (work item, tile list, query) hides behind the
+// other's tail.  A decode call reads nothing a decode call writes before its
+// griddepcontrol.wait.  After anything else (append, drop, reposition, the
+// kernel that copies this call's new plan in) the launch is plain stream
+// order.
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
   const dim3 grid(a.n_items_w > a.n_items ? a.n_items_w : a.n_items, a.g.hkv);
   cudaLaunchConfig_t cfg = {};
@@ -714,7 +714,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 1 : 0;
   if (a.g.d == 64) {
     set_smem_attr<64>();
     cfg.dynamicSmemBytes = mma_smem<64>();

@@ -593,9 +593,9 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t st) {
     cudaFuncSetAttribute(k_decode_share_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     attr = true;
   }
-  // programmatic stream serialisation: after a decode call (which signals
-  // its dependents at its start) this grid's blocks start early and wait
-  // (griddepcontrol.wait) before their first write
+  // programmatic stream serialisation (a.pdl: the stream's previous work is
+  // a decode call, which signals its dependents at its start): this grid's
+  // blocks start early and wait (griddepcontrol.wait) before their first write
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_share_items, a.g.hkv);
   cfg.blockDim = dim3(kThreads);
@@ -605,7 +605,7 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t st) {
   attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, k_decode_share_tc<D>, a);
 }
 

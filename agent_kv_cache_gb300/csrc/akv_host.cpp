@@ -91,7 +91,14 @@ struct Segment {
   int32_t ns = 1;
 };
 
-struct Stage { char* h = nullptr; char* d = nullptr; cudaEvent_t ev = nullptr; bool used = false; };
+// A staging block: pinned host memory (hd: its device view) and a device copy.
+struct Stage {
+  char* h = nullptr;
+  char* hd = nullptr;
+  char* d = nullptr;
+  cudaEvent_t ev = nullptr;
+  bool used = false;
+};
 
 struct Blob {
   std::vector<char> b;
@@ -216,6 +223,7 @@ struct akv_cache {
   uint32_t wait_limit = 1u << 22;
   int sm_count = 148;
   uint64_t launches = 0;
+  uint64_t decode_tail = ~0ULL;     // launches right after the last decode call
   CUtensorMap tm_k{}, tm_v{}, tm_k4{}, tm_v4{};
   bool use_mma = false;
   int mma_blocks_per_sm = 0;
@@ -310,6 +318,14 @@ void take_pages(akv_cache* c, size_t n) {
   }
 }
 
+// Device-to-device bytes on the cache's stream, by a kernel (no copy-engine
+// work on the caller's stream); n may be 0.
+cudaError_t copy_rows(akv_cache* c, void* dst, const void* src, size_t n) {
+  if (n == 0) return cudaSuccess;
+  ++c->launches;
+  return launch_copy_bytes(dst, src, n, c->stream);
+}
+
 int upload(akv_cache* c, const Blob& blob, char* dst, char** dptr) {
   if (blob.b.size() > c->stage_bytes)
     return fail(c, AKV_ECAPACITY, "descriptor of %zu bytes exceeds the staging block (%zu)",
@@ -319,7 +335,8 @@ int upload(akv_cache* c, const Blob& blob, char* dst, char** dptr) {
   if (s.used) CK(cudaEventSynchronize(s.ev));
   if (!blob.b.empty()) {
     std::memcpy(s.h, blob.b.data(), blob.b.size());
-    CK(cudaMemcpyAsync(dst ? dst : s.d, s.h, blob.b.size(), cudaMemcpyHostToDevice, c->stream));
+    CK(launch_copy_bytes(dst ? dst : s.d, s.hd, blob.b.size(), c->stream));
+    ++c->launches;
   }
   CK(cudaEventRecord(s.ev, c->stream));
   s.used = true;
@@ -336,7 +353,8 @@ int upload_large(akv_cache* c, const Blob& blob, char* dst) {
     c->stage_next = (c->stage_next + 1) % kStages;
     if (s.used) CK(cudaEventSynchronize(s.ev));
     std::memcpy(s.h, blob.b.data() + off, m);
-    CK(cudaMemcpyAsync(dst + off, s.h, m, cudaMemcpyHostToDevice, c->stream));
+    CK(launch_copy_bytes(dst + off, s.hd, m, c->stream));
+    ++c->launches;
     CK(cudaEventRecord(s.ev, c->stream));
     s.used = true;
   }
@@ -474,6 +492,7 @@ int akv_cache_create(const akv_config* cfg, void* k_pool, void* v_pool, size_t p
   c->stage_bytes = (c->stage_bytes + 4095) & ~size_t(4095);
   for (Stage& s : c->stages) {
     CKC(cudaMallocHost(&s.h, c->stage_bytes));
+    CKC(cudaHostGetDevicePointer(reinterpret_cast<void**>(&s.hd), s.h, 0));
     CKC(cudaMalloc(&s.d, c->stage_bytes));
     CKC(cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming));
   }
@@ -542,15 +561,15 @@ int akv_seq_fork(akv_cache* c, int64_t parent, int64_t* child) {
   const int64_t ps = p->dslot, cs = s.dslot;
   const size_t nw = (size_t)((p->n_slots + 31) / 32);
   const size_t np = p->pages.size();
-  CK(cudaMemcpyAsync(sa.keep + cs * sa.keep_words, sa.keep + ps * sa.keep_words,
-                     nw * sizeof(uint32_t), cudaMemcpyDeviceToDevice, c->stream));
-  CK(cudaMemcpyAsync(sa.pages + cs * sa.seq_pages, sa.pages + ps * sa.seq_pages,
-                     np * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
-  CK(cudaMemcpyAsync(sa.active + cs * sa.seq_pages, sa.active + ps * sa.seq_pages,
-                     (size_t)p->n_active_pages * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
+  CK(copy_rows(c, sa.keep + cs * sa.keep_words, sa.keep + ps * sa.keep_words,
+               nw * sizeof(uint32_t)));
+  CK(copy_rows(c, sa.pages + cs * sa.seq_pages, sa.pages + ps * sa.seq_pages,
+               np * sizeof(int32_t)));
+  CK(copy_rows(c, sa.active + cs * sa.seq_pages, sa.active + ps * sa.seq_pages,
+               (size_t)p->n_active_pages * sizeof(int32_t)));
   if (!p->gather_identity && p->gather_n)
-    CK(cudaMemcpyAsync(sa.gather + cs * sa.max_slots, sa.gather + ps * sa.max_slots,
-                       (size_t)p->gather_n * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
+    CK(copy_rows(c, sa.gather + cs * sa.max_slots, sa.gather + ps * sa.max_slots,
+                 (size_t)p->gather_n * sizeof(int32_t)));
   c->free_dslots.pop_back();
   for (int32_t pg : s.pages)
     if (pg >= 0) ++c->refcnt[pg];
@@ -567,8 +586,9 @@ int akv_seq_free(akv_cache* c, int64_t seq) {
   HostSeq* s = find(c, seq);
   if (!s) return fail(c, AKV_ENOSEQ, "unknown sequence %lld", (long long)seq);
   // a free device row keeps all keep bits clear (append only sets bits)
-  CK(cudaMemsetAsync(c->sa.keep + (int64_t)s->dslot * c->sa.keep_words, 0,
-                     (size_t)c->sa.keep_words * sizeof(uint32_t), c->stream));
+  CK(launch_fill_u32(c->sa.keep + (int64_t)s->dslot * c->sa.keep_words, 0,
+                     (size_t)c->sa.keep_words, c->stream));
+  ++c->launches;
   for (int32_t pg : s->pages) decref(c, pg);
   c->free_dslots.push_back(s->dslot);
   c->seqs.erase(seq);
@@ -1388,7 +1408,14 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       // DecodeArgs::items_w).  The quarter-wave split above is best when
       // calls come back to back, and a call on its own would leave three
       // quarters of the GPU idle with it.
-      if (plain && c->decode_waves < 4) {
+      // Only where the quarter-wave split keeps too few tile copies in flight
+      // to fill HBM on its own (its blocks x the ring's 8 stages of K and V
+      // tiles): the 120B-shaped call (184 blocks, D 64: ~6 MB) gains from a
+      // whole wave alone, the 8B-shaped one (228 blocks, D 128: ~15 MB)
+      // loses to the extra splits' merges.
+      const int64_t q_blocks = (int64_t)items.size() * c->cfg.hkv;
+      const int64_t in_flight = q_blocks * 8 * 2 * 16 * (int64_t)c->cfg.head_dim * 2;
+      if (plain && c->decode_waves < 4 && in_flight < ((int64_t)12 << 20)) {
         std::vector<DecodeItem> q_items = std::move(items);
         std::vector<int32_t> q_item0 = item0, q_splits = splits;
         std::fill(splits.begin(), splits.end(), 0);
@@ -1488,13 +1515,19 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
     if (++c->decode_call >= (1u << 29)) c->decode_call = 1;   // the words keep 29 bits of it
     a.call_id = c->decode_call;
   }
+  // early launch only right behind a decode call of this cache (not behind
+  // the copy of a new plan, an append or any other kernel of this cache)
+  a.pdl = c->launches == c->decode_tail;
+  const uint64_t before = c->launches;
   if (plan->sitems > 0) {
     CK(launch_decode_share(a, c->stream));
     ++c->launches;
+    a.pdl = true;                 // behind the shared-prefix kernel, a decode kernel
   }
   CK(launch_decode(a, plan->combine, n_seqs, reinterpret_cast<const int32_t*>(plan->d + o_item0),
                    reinterpret_cast<const int32_t*>(plan->d + o_splits), c->stream));
   if (plan->items > 0) c->launches += plan->combine ? 2 : 1;
+  if (c->launches != before) c->decode_tail = c->launches;
   return AKV_OK;
 }
 
@@ -1851,15 +1884,12 @@ int akv_prefix_fork(akv_cache* c, akv_prefix_index* x, const akv_op* ops, int32_
   c->free_dslots.pop_back();
   const SeqArrays& sa = c->sa;
   char* d = static_cast<char*>(c->d_fork);
-  if (!keep.empty())
-    CK(cudaMemcpyAsync(sa.keep + (int64_t)s.dslot * sa.keep_words, d + o_keep,
-                       keep.size() * sizeof(uint32_t), cudaMemcpyDeviceToDevice, c->stream));
-  if (!s.pages.empty())
-    CK(cudaMemcpyAsync(sa.pages + (int64_t)s.dslot * sa.seq_pages, d + o_pages,
-                       s.pages.size() * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
-  if (!act.empty())
-    CK(cudaMemcpyAsync(sa.active + (int64_t)s.dslot * sa.seq_pages, d + o_act,
-                       act.size() * sizeof(int32_t), cudaMemcpyDeviceToDevice, c->stream));
+  CK(copy_rows(c, sa.keep + (int64_t)s.dslot * sa.keep_words, d + o_keep,
+               keep.size() * sizeof(uint32_t)));
+  CK(copy_rows(c, sa.pages + (int64_t)s.dslot * sa.seq_pages, d + o_pages,
+               s.pages.size() * sizeof(int32_t)));
+  CK(copy_rows(c, sa.active + (int64_t)s.dslot * sa.seq_pages, d + o_act,
+               act.size() * sizeof(int32_t)));
   const int64_t id = c->next_id++;
   c->seqs.emplace(id, std::move(s));
   ++c->epoch;

@@ -156,6 +156,7 @@ struct DecodeArgs {
   uint32_t* mode_words;         // [8] (call_id << 3 | plan) once a call has chosen
   uint32_t* exit_words;         // [1024] blocks of call c exited, at c % 1024
   uint32_t* done_word;          // last call whose blocks have all exited
+  bool pdl;                     // host only: launch with programmatic stream serialisation
 };
 constexpr int kDecodeModeWords = 8;
 constexpr int kDecodeExitWords = 1024;
@@ -220,6 +221,11 @@ cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* 
                           AppendLimits lim, cudaStream_t st);
 cudaError_t launch_copy_pages(const Geom& g, const PagePair* pairs, int n_pairs,
                               uint32_t* err, cudaStream_t st);
+// n bytes from src to dst by a kernel (src may be pinned host memory, read
+// over the host link); any alignment, n may be 0.
+cudaError_t launch_copy_bytes(void* dst, const void* src, size_t n, cudaStream_t st);
+// dst[0..n) = v by a kernel.
+cudaError_t launch_fill_u32(uint32_t* dst, uint32_t v, size_t n, cudaStream_t st);
 cudaError_t launch_drop(const Geom& g, const SeqArrays& sa, const DropItem* items,
                         int n_items, const int32_t* ranges, uint32_t* err, cudaStream_t st);
 cudaError_t launch_compact(const Geom& g, const SeqArrays& sa, const ReposItem* items,

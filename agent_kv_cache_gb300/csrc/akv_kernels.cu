@@ -843,6 +843,47 @@ cudaError_t launch_copy_pages(const Geom& g, const PagePair* pairs, int n_pairs,
   return cudaGetLastError();
 }
 
+// Byte copy by the SMs: descriptors staged in pinned host memory (read over
+// the host link) and metadata rows moved inside device memory.  The copy
+// engines stay out of the caller's stream: a small engine copy queued there
+// behind the caller's own bulk host-to-device traffic on another stream can
+// wait for milliseconds, and the decode step behind it with it.
+__global__ void k_copy_bytes(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                             int64_t n) {
+  const int64_t n16 = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15)
+                          ? 0 : n / 16;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t i = t0; i < n16; i += stride)
+    reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+  for (int64_t i = n16 * 16 + t0; i < n; i += stride) dst[i] = src[i];
+}
+
+__global__ void k_fill_u32(uint32_t* __restrict__ dst, uint32_t v, int64_t n) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = v;
+}
+
+namespace {
+int copy_grid(int64_t units) {
+  const int64_t b = (units + 255) / 256;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(b, 1024));
+}
+}  // namespace
+
+cudaError_t launch_copy_bytes(void* dst, const void* src, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  k_copy_bytes<<<copy_grid((int64_t)(n + 15) / 16), 256, 0, st>>>(
+      static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), (int64_t)n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_u32(uint32_t* dst, uint32_t v, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  k_fill_u32<<<copy_grid((int64_t)n), 256, 0, st>>>(dst, v, (int64_t)n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_drop(const Geom& g, const SeqArrays& sa, const DropItem* items,
                         int n_items, const int32_t* ranges, uint32_t* err, cudaStream_t st) {
   if (n_items <= 0) return cudaSuccess;

@@ -573,14 +573,16 @@ class Steady:
         L = self.sh.layers
         if host is not None:
             if not hasattr(self, "_h2d"):
-                self._h2d = torch.cuda.Stream()
+                self._h2d = torch.cuda.Stream()            # this turn's queries / new K/V
+                self._h2d_tool = torch.cuda.Stream()       # the next turn's tool responses
                 self._d2h = torch.cuda.Stream()
                 self._tool_ready = [torch.cuda.Event() for _ in self.groups]
                 self._ready = [torch.cuda.Event() for _ in range(STEADY_DECODE)]
                 self._done = [torch.cuda.Event() for _ in range(STEADY_DECODE)]
                 self._prefetched = None
+                self._tool_ev, self._tool_host_s = {}, {}
             if self._prefetched != k:          # nothing prefetched: copy now
-                self._h2d.wait_stream(st)
+                self._h2d_tool.wait_stream(st)
                 self._tool_copy(k, host)
             st.wait_stream(self._d2h)          # the previous turn's outputs have been read
         if ev is not None:
@@ -598,7 +600,9 @@ class Steady:
             ev["append"][1].record(st)
         if host is not None:
             # the previous turn's decode has read q / new K/V, and this turn's
-            # appends have read the tool slots (both enqueued on the stream)
+            # appends have read the tool slots (both enqueued on the stream);
+            # the two kinds of copies go on streams of their own, so that the
+            # queries never queue behind the next turn's tool responses
             self._h2d.wait_stream(st)
             with torch.cuda.stream(self._h2d):
                 for t in range(STEADY_DECODE):
@@ -606,10 +610,16 @@ class Steady:
                     self.knew[t].copy_(host["kn"][t], non_blocking=True)
                     self.vnew[t].copy_(host["vn"][t], non_blocking=True)
                     self._ready[t].record(self._h2d)
-            if k + 1 < self.n_turns:
-                self._tool_copy(k + 1, host)
-                self._prefetched = k + 1
         for t in range(STEADY_DECODE):
+            if host is not None and t == 8 and k + 1 < self.n_turns:
+                # the next turn's tool responses go up once this turn's
+                # queries have (started at the turn start, the 27 GB copy
+                # held the first decode step's 0.1 GB of queries back)
+                self._h2d_tool.wait_stream(st)
+                h0 = time.perf_counter()
+                self._tool_copy(k + 1, host, timed=True)
+                self._tool_host_s[k + 1] = time.perf_counter() - h0
+                self._prefetched = k + 1
             if host is not None:
                 st.wait_event(self._ready[t])
             c.append(self.seqs, [1] * STEADY_SEQS, self.knew[t], self.vnew[t])
@@ -632,18 +642,24 @@ class Steady:
                     host["out"][t].copy_(host["out_dev"][t], non_blocking=True)
         self._drop_repos(k, ev)
 
-    def _tool_copy(self, k, host):
+    def _tool_copy(self, k, host, timed=False):
         """Turn k's tool-response K/V from pinned host memory into the group
-        slots, on the copy stream."""
+        slots, on the copy stream (``timed``: an event pair around it)."""
         torch = self.torch
-        with torch.cuda.stream(self._h2d):
+        if timed:
+            self._tool_ev[k] = events(torch, 1)[0]
+        with torch.cuda.stream(self._h2d_tool):
+            if timed:
+                self._tool_ev[k][0].record(self._h2d_tool)
             for gi, g in enumerate(self.groups):
                 n = sum(self.turns[i][k].tool_len for i in g)
                 kk, vv = self.raw(n, host["slots"][gi])
                 hk, hv = self.raw(n, (host["k"], host["v"]))
                 kk.copy_(hk, non_blocking=True)
                 vv.copy_(hv, non_blocking=True)
-                self._tool_ready[gi].record(self._h2d)
+                self._tool_ready[gi].record(self._h2d_tool)
+            if timed:
+                self._tool_ev[k][1].record(self._h2d_tool)
 
     def host_buffers(self):
         """Pinned host copies of one turn's inputs and outputs (tool responses
@@ -1641,12 +1657,14 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     with Clocks(gpu_id(local)) as clk:
         start.record(b.stream)
+        host_dev = time.perf_counter()
         for i in range(K):
             if args.nvtx:
                 torch.cuda.nvtx.range_push("turn")
             b.turn(STEADY_FIRST + i, ev=evs[i])
             if args.nvtx:
                 torch.cuda.nvtx.range_pop()
+        host_dev = (time.perf_counter() - host_dev) / K
         stop.record(b.stream)
         torch.cuda.synchronize()
     barrier()
@@ -1668,6 +1686,10 @@ def gpu_arm(args):
     drp = [ev["drop"][0].elapsed_time(ev["drop"][1]) for ev, a in zip(evs, timed) if a["dropped"]]
     app = [(ev["append"][0].elapsed_time(ev["append"][1]), 2 * L * a["tool"] * kvt_of(sh))
            for ev, a in zip(evs, timed)]
+    # time between one decode step's last call and the next step's first
+    # (the next token's append, and in the end-to-end run any wait for inputs)
+    gap_dev = float(np.mean([sum(ev["dec"][t][1].elapsed_time(ev["dec"][t + 1][0])
+                                 for t in range(STEADY_DECODE - 1)) for ev in evs]))
     value = world * total / (ms * K * 1e-3) / 1e9
 
     # one decode call at a time (after an unrelated kernel streaming 1.5 GB),
@@ -1688,8 +1710,10 @@ def gpu_arm(args):
         s2, e2 = events(torch, 1)[0]
         evs2 = [b.events() for _ in range(K)]
         s2.record(b.stream)
+        host_s = time.perf_counter()
         for i in range(K):
             b.turn(k0 + 1 + i, ev=evs2[i], host=host)
+        host_s = (time.perf_counter() - host_s) / K
         e2.record(b.stream)
         torch.cuda.synchronize()
         barrier()
@@ -1697,6 +1721,8 @@ def gpu_arm(args):
         ms2 = reduce_max(s2.elapsed_time(e2) / K, dist, "cuda")
         tot2 = sum(b.acct[k0 + 1 + i]["total"] for i in range(K))
         dec2 = np.array([[s_.elapsed_time(e_) / L for s_, e_ in ev["dec"]] for ev in evs2])
+        gap2 = float(np.mean([sum(ev["dec"][t][1].elapsed_time(ev["dec"][t + 1][0])
+                                  for t in range(STEADY_DECODE - 1)) for ev in evs2]))
         app2 = [ev["append"][0].elapsed_time(ev["append"][1]) for ev in evs2]
         e2e = {"value": round(world * tot2 / (ms2 * K * 1e-3) / 1e9, 1), "unit": "GB/s",
                "h2d_bytes_per_step": int(np.mean([b.h2d_bytes(k0 + 1 + i) for i in range(K)])),
@@ -1705,10 +1731,31 @@ def gpu_arm(args):
                "turns": f"{k0 + 2}..{k0 + 1 + K}",
                "decode_avg_call_us": round(float(np.mean(dec2)) * 1e3, 2),
                "decode_ms_per_turn": round(float(np.sum(dec2)) * L / K, 1),
+               "decode_call_us_per_8_steps": [round(float(np.mean(dec2[:, j:j + 8])) * 1e3, 1)
+                                              for j in range(0, STEADY_DECODE, 8)],
                "append_ms_per_turn": round(float(np.mean(app2)), 3),
+               "between_decode_steps_ms_per_turn": round(gap2, 2),
+               "host_enqueue_ms_per_turn": round(host_s * 1e3, 1),
+               "appends_to_first_decode_ms": round(float(np.mean(
+                   [ev["append"][1].elapsed_time(ev["dec"][0][0]) for ev in evs2])), 2),
+               "last_decode_to_turn_end_ms": round(float(np.mean(
+                   [ev["dec"][-1][1].elapsed_time(ev["repos"][1]) for ev in evs2])), 2),
+               "tool_prefetch_ms": round(float(np.mean(
+                   [b._tool_ev[k][0].elapsed_time(b._tool_ev[k][1])
+                    for k in range(k0 + 2, k0 + 2 + K) if k in b._tool_ev])), 2),
+               "tool_prefetch_start_after_first_decode_ms": round(float(np.mean(
+                   [ev["dec"][0][0].elapsed_time(b._tool_ev[k0 + 2 + i][0])
+                    for i, ev in enumerate(evs2) if k0 + 2 + i in b._tool_ev])), 2),
+               "tool_prefetch_host_ms": round(float(np.mean(
+                   [b._tool_host_s[k] * 1e3 for k in range(k0 + 2, k0 + 2 + K)
+                    if k in b._tool_host_s])), 2),
+               "turn_start_to_first_append_ms": round(float(np.mean(
+                   [e_prev["repos"][1].elapsed_time(e_cur["append"][0])
+                    for e_prev, e_cur in zip(evs2[:-1], evs2[1:])])), 2) if K > 1 else None,
                "what": "public C-ABI calls (append / decode / drop / reposition) with every "
-                       "turn's inputs copied from pinned host memory on a copy stream: its "
-                       "tool responses' raw K/V during the previous turn's decode (one device "
+                       "turn's inputs copied from pinned host memory on copy streams: its "
+                       "tool responses' raw K/V during the previous turn's decode (from its "
+                       "eighth decode step on, one device "
                        "slot per group of 16 sequences; each group's append waits for its "
                        "copy), its decode steps' queries and new-token K/V while its decode "
                        "runs (each step waits for its own); every decode step's last-layer "
@@ -1758,6 +1805,8 @@ def gpu_arm(args):
                                         / 1e9, 1) if rep else None,
                            "frac": round(sum(r[1] for r in rep) / (sum(r[0] for r in rep) * 1e-3)
                                          / 1e9 / peak, 4) if rep else None},
+            "between_decode_steps_ms_per_turn": round(gap_dev, 2),
+            "host_enqueue_ms_per_turn": round(host_dev * 1e3, 1),
             "drop": {"kernel": "k_drop", "us_per_turn": round(float(np.mean(drp)) * 1e3, 1)
                      if drp else None, "calls_per_turn": STEADY_SEQS},
             "append": {"kernel": "k_append (tool responses, 80 layers)",

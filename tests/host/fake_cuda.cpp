@@ -32,6 +32,7 @@ cudaError_t cudaMalloc(void** p, size_t n) {
 cudaError_t cudaHostAlloc(void** p, size_t n, unsigned int) { return cudaMalloc(p, n); }
 cudaError_t cudaFree(void* p) { std::free(p); return cudaSuccess; }
 cudaError_t cudaFreeHost(void* p) { std::free(p); return cudaSuccess; }
+cudaError_t cudaHostGetDevicePointer(void** d, void* h, unsigned int) { *d = h; return cudaSuccess; }
 cudaError_t cudaMemcpy(void* d, const void* s, size_t n, cudaMemcpyKind) {
   if (n) std::memmove(d, s, n);
   return cudaSuccess;
@@ -70,6 +71,17 @@ cudaError_t launch_append(const Geom&, const SeqArrays&, const AppendItem*, cons
 }
 cudaError_t launch_copy_pages(const Geom&, const PagePair*, int, uint32_t*, cudaStream_t) {
   ++g_launches;
+  return cudaSuccess;
+}
+// the byte copy and fill kernels move host metadata: done here
+cudaError_t launch_copy_bytes(void* dst, const void* src, size_t n, cudaStream_t) {
+  ++g_launches;
+  if (n) std::memmove(dst, src, n);
+  return cudaSuccess;
+}
+cudaError_t launch_fill_u32(uint32_t* dst, uint32_t v, size_t n, cudaStream_t) {
+  ++g_launches;
+  for (size_t i = 0; i < n; ++i) dst[i] = v;
   return cudaSuccess;
 }
 cudaError_t launch_drop(const Geom&, const SeqArrays&, const DropItem*, int, const int32_t*,
