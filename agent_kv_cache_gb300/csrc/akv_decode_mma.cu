@@ -192,12 +192,14 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const __grid_constant__
   // the next decode call may be scheduled now: its blocks start as this
   // grid's blocks retire and wait (griddepcontrol.wait) before writing
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if ((int)blockIdx.x >= n_items) {             // the grid is sized for the larger split
+  // grid (KV head, item): the blocks of an item go out together, in the
+  // plan's order (longest items first)
+  if ((int)blockIdx.y >= n_items) {             // the grid is sized for the larger split
     if (threadIdx.x == 0 && a.call_id > 0) count_exit(a);
     return;
   }
-  const DecodeItem it = items[blockIdx.x];
-  const int kvh = blockIdx.y;
+  const DecodeItem it = items[blockIdx.y];
+  const int kvh = blockIdx.x;
   const Geom& g = a.g;
   const int G = g.hq / g.hkv;
   const int tpp = g.s / kTile;                  // tiles per page
@@ -705,7 +707,7 @@ bool make_pool_tensor_maps(const Geom& g, CUtensorMap* tk, CUtensorMap* tv) {
 // kernel that copies this call's new plan in) the launch is plain stream
 // order.
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
-  const dim3 grid(a.n_items_w > a.n_items ? a.n_items_w : a.n_items, a.g.hkv);
+  const dim3 grid(a.g.hkv, a.n_items_w > a.n_items ? a.n_items_w : a.n_items);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);

@@ -50,7 +50,7 @@ constexpr int kLoadWarp = kSoftmaxWarps + 1; // issues the tile copies (one thre
 constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kHalf = kBN / 2;              // tokens per softmax warp and tile
 constexpr int kCols = 256;                  // TMEM: two S buffers (2 x 64) and O (<= 128)
-constexpr int kMaxItemPages = 128;          // pages of one item (the planner takes 32..128)
+constexpr int kMaxItemPages = 256;          // pages of one item (the planner takes 32..256)
 static_assert(2 * kBN + 128 <= kCols, "S buffers and O must fit the TMEM allocation");
 
 // Bounded wait for the phase of `parity` to complete, polling try_wait

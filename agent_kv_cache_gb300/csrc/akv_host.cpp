@@ -19,6 +19,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <queue>
 #include <string>
 #include <unordered_map>
@@ -41,8 +42,9 @@ constexpr int kMaxMembers = 16384;         // members of shared decode items per
 constexpr int kMinSharedPages = 4;         // shorter runs of common pages are read per row
 constexpr int kShareRows = 128;            // query rows of a shared-prefix (tensor-core) item
 constexpr int kShareMaxMembers = 128;
-constexpr int kSharePagesMin = 32;         // pages per shared-prefix item (the kernel takes <= 128)
-constexpr int kSharePagesMax = 128;
+constexpr int kSharePagesMin = 32;         // pages per shared-prefix item (the kernel takes <= 256)
+constexpr int kSharePagesMax = 256;
+constexpr int kBlockStartPages = 6;       // a decode block's start-up, in pages of work
 
 // 128-bit key of an operation history: two independent 64-bit chains, each
 // step finished with the MurmurHash3 64-bit finaliser (Appleby).
@@ -1247,17 +1249,26 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
           parts += (int64_t)segs[k].ns * segs[k].rows.size();
           pq.push({(w + segs[k].ns - 1) / segs[k].ns, k});
         }
-        // shared-prefix items: 32..64 pages each, longer when that keeps all
-        // of them within about 90% of one wave of CTAs (two per SM): a CTA's
-        // set-up and epilogue weigh like a few tiles, and a second, partial
-        // wave costs a whole CTA's time
+        // shared-prefix items: at least kSharePagesMin pages each, longer
+        // until all of them fit one wave of CTAs (two per SM), counting the
+        // rounding up of every segment: a CTA's set-up and epilogue weigh
+        // like a few tiles, and a second, partial wave costs a whole CTA's
+        // time -- and holds back the one-row kernel of the call, which
+        // starts only once every CTA of this one has
         if (!tsegs.empty()) {
           int64_t tp = 0;
           for (auto& sg : tsegs) tp += sg.a1 - sg.a0;
-          const int64_t wave = std::max<int64_t>(1, 2 * c->sm_count * 9 / 10);
-          const int64_t per = std::min<int64_t>(
+          const int64_t wave = std::max<int64_t>(1, 2 * c->sm_count);
+          auto ctas = [&](int64_t per) {
+            int64_t n = 0;
+            for (auto& sg : tsegs) n += (sg.a1 - sg.a0 + per - 1) / per;
+            return n * c->cfg.hkv;
+          };
+          int64_t per = std::min<int64_t>(
               kSharePagesMax,
               std::max<int64_t>(kSharePagesMin, (tp * c->cfg.hkv + wave - 1) / wave));
+          while (per < kSharePagesMax && ctas(per) > wave)
+            per = std::min<int64_t>(kSharePagesMax, per + std::max<int64_t>(1, per / 16));
           for (auto& sg : tsegs) {
             sg.ns = (int32_t)std::max<int64_t>(1, (sg.a1 - sg.a0 + per - 1) / per);
             parts += (int64_t)sg.ns * sg.rows.size();
@@ -1276,18 +1287,79 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
           if (target > per_wave)
             target = std::min<int64_t>(kMaxItems, (target + per_wave - 1) / per_wave * per_wave);
         }
-        while (sum < target && !pq.empty()) {
-          Entry e = pq.top();
-          pq.pop();
-          Segment& sg = segs[e.second];
-          const int64_t na = sg.a1 - sg.a0;
-          if ((na + sg.ns - 1) / sg.ns <= 2) break;     // splits of 1-2 pages gain nothing
-          if (parts + (int64_t)sg.rows.size() > kMaxItems) continue;
-          ++sg.ns;
-          ++sum;
-          parts += sg.rows.size();
-          pq.push({(na * nb_of(sg) + sg.ns - 1) / sg.ns, e.second});
+        // split the segment with the most work per split until there are
+        // `tgt` splits (or nothing worth splitting is left)
+        auto split_upto = [&](int64_t tgt, std::vector<int32_t>* ns, int64_t* n_sum, int64_t* n_parts) {
+          ns->resize(segs.size());
+          for (size_t k = 0; k < segs.size(); ++k) (*ns)[k] = segs[k].ns;
+          auto q = pq;
+          int64_t s = sum, p = parts;
+          while (s < tgt && !q.empty()) {
+            const Entry e = q.top();
+            q.pop();
+            const Segment& sg = segs[e.second];
+            int32_t& m = (*ns)[e.second];
+            const int64_t na = sg.a1 - sg.a0;
+            if ((na + m - 1) / m <= 2) break;           // splits of 1-2 pages gain nothing
+            if (p + (int64_t)sg.rows.size() > kMaxItems) continue;
+            ++m;
+            ++s;
+            p += sg.rows.size();
+            q.push({(na * nb_of(sg) + m - 1) / m, e.second});
+          }
+          *n_sum = s;
+          *n_parts = p;
+        };
+        std::vector<int32_t> ns_best;
+        int64_t sum_best = sum, parts_best = parts;
+        if (tsegs.empty()) {
+          split_upto(target, &ns_best, &sum_best, &parts_best);
+        } else {
+          // Next to shared-prefix items the one-row kernel runs on its own
+          // (nothing of the next call overlaps its end), so the split count
+          // is chosen by the time the block scheduler would take: blocks
+          // dispatched in plan order (longest first, an item's KV heads
+          // together) onto the resident block slots as they free up, a block
+          // costing its pages x column blocks plus a fixed start-up.  The
+          // count that evens the slots out best wins; whole waves of
+          // similar items can end with some slots holding two long ones.
+          const int64_t per_wave = std::max<int64_t>(1, resident / c->cfg.hkv);
+          const int64_t step = std::max<int64_t>(1, per_wave / 4);
+          double best = -1.0;
+          std::vector<int32_t> ns;
+          std::vector<int64_t> w;
+          for (int64_t tgt = target; tgt <= std::min<int64_t>(kMaxItems, target + 4 * per_wave);
+               tgt += step) {
+            int64_t s = 0, p = 0;
+            split_upto(tgt, &ns, &s, &p);
+            w.clear();
+            for (size_t k = 0; k < segs.size(); ++k) {
+              const int64_t na = segs[k].a1 - segs[k].a0;
+              for (int32_t j = 0; j < ns[k]; ++j)
+                w.push_back((na * (j + 1) / ns[k] - na * j / ns[k]) * nb_of(segs[k]) + kBlockStartPages);
+            }
+            std::sort(w.begin(), w.end(), std::greater<int64_t>());
+            std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> slots;
+            for (int64_t i = 0; i < resident; ++i) slots.push(0);
+            int64_t end = 0;
+            for (int64_t x : w)
+              for (int h = 0; h < c->cfg.hkv; ++h) {
+                const int64_t t = slots.top() + x;
+                slots.pop();
+                slots.push(t);
+                end = std::max(end, t);
+              }
+            if (best < 0 || end < best) {
+              best = (double)end;
+              ns_best = ns;
+              sum_best = s;
+              parts_best = p;
+            }
+          }
         }
+        for (size_t k = 0; k < segs.size(); ++k) segs[k].ns = ns_best[k];
+        sum = sum_best;
+        parts = parts_best;
         if (sum > kMaxItems || parts > kMaxItems) return AKV_ECAPACITY;
         // the members of split k of a segment: those whose part reaches
         // into it; a row's partial slots are side by side
@@ -1382,6 +1454,10 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
           }
         }
         if ((int64_t)items.size() > kMaxItems || (int64_t)sitems.size() > kMaxItems) return AKV_ECAPACITY;
+        // longest first: the kernel's blocks go out in plan order
+        std::stable_sort(items.begin(), items.end(), [](const DecodeItem& x, const DecodeItem& y) {
+          return (int64_t)(x.p1 - x.p0) * x.nb > (int64_t)(y.p1 - y.p0) * y.nb;
+        });
         return AKV_OK;
       };
       // rows can hold the same pages only within a fork family

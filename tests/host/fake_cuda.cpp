@@ -15,15 +15,20 @@
 
 #include <cuda_runtime_api.h>
 
+#include "akv.h"
 #include "akv_internal.h"
 
 namespace {
 long g_launches = 0;
+bool g_tensor_cores = false;   // report the tensor-core decode kernels as usable
 }
 
 extern "C" {
 
 long akv_fake_launches() { return g_launches; }
+// Plans as for a GPU where the tensor-core decode kernels run (the planner's
+// choices depend on it); off by default.
+void akv_fake_set_tensor_cores(int on) { g_tensor_cores = on != 0; }
 
 cudaError_t cudaMalloc(void** p, size_t n) {
   *p = std::calloc(1, n ? n : 1);
@@ -117,11 +122,18 @@ cudaError_t launch_restore(const RestoreArgs&, cudaStream_t) {
   ++g_launches;
   return cudaSuccess;
 }
-bool decode_mma_supported(const Geom&) { return false; }
-bool decode_share_supported(const Geom&) { return false; }
+bool decode_mma_supported(const Geom& g) {
+  return g_tensor_cores && g.dtype == AKV_DTYPE_BF16 && g.s % 16 == 0 && g.hq / g.hkv <= 8 &&
+         (g.d == 64 || g.d == 128);
+}
+bool decode_share_supported(const Geom& g) {
+  const int G = g.hq / g.hkv;
+  return g_tensor_cores && g.dtype == AKV_DTYPE_BF16 && g.s == 16 && (g.d == 64 || g.d == 128) &&
+         (G == 1 || G == 2 || G == 4 || G == 8);
+}
 int decode_mma_blocks_per_sm(int) { return 3; }
-bool make_pool_tensor_maps(const Geom&, CUtensorMap*, CUtensorMap*) { return false; }
-bool make_pool_tensor_maps4(const Geom&, CUtensorMap*, CUtensorMap*) { return false; }
+bool make_pool_tensor_maps(const Geom& g, CUtensorMap*, CUtensorMap*) { return decode_mma_supported(g); }
+bool make_pool_tensor_maps4(const Geom& g, CUtensorMap*, CUtensorMap*) { return decode_mma_supported(g); }
 bool restore_mma_supported(const Geom&) { return false; }
 int restore_tile_tokens(const Geom&) { return 16; }
 bool make_restore_tensor_maps(const Geom&, const void*, const void*, int64_t, CUtensorMap*,
