@@ -337,3 +337,58 @@ def test_interval_sets_under_overlapping_drops(host_lib):
         c.check()
     c.free(a)
     c.close()
+
+
+@pytest.fixture()
+def tensor_core_plans(host_lib):
+    """Plan as for a GPU where the tensor-core decode kernels run."""
+    host_lib.akv_fake_set_tensor_cores(1)
+    yield host_lib
+    host_lib.akv_fake_set_tensor_cores(0)
+
+
+def test_shared_prefix_items_fit_one_wave(tensor_core_plans):
+    """Branches of one prefix, each with its own drops and repositions: the
+    decode plan reads pages that several branches hold through shared-prefix
+    items (page 1, 3.2: forks share pages copy-on-write), and those items fit
+    one wave of the shared-prefix kernel (two CTAs per SM on the 152 SMs the
+    stand-in reports, one CTA per KV head), whatever the segments' sizes."""
+    from workloads import traces
+    sh = traces.LLAMA8B
+    NB, P = 48, 8192
+    _, branches = traces.branching(11, n_branches=NB, prefix_len=P)
+    cfg = abi.make_config(1, sh.hq, sh.hkv, sh.head_dim, 16, "bf16", P // 16 + NB * 700 + 256,
+                          NB + 2, P + 64, sh.rope_theta)
+    nbytes = abi.akv_pool_bytes(cfg)
+    mem = [np.zeros(nbytes + 256, np.uint8) for _ in range(2)]
+    ptr = [m.ctypes.data + (-m.ctypes.data % 256) for m in mem]
+    h = abi.akv_cache_create(cfg, ptr[0], ptr[1], nbytes)
+    raw = np.zeros(16, np.float32)
+    root = abi.akv_seq_create(h)
+    abi.akv_append(h, [root], [P], raw.ctypes.data, raw.ctypes.data)
+    kids = [abi.akv_seq_fork(h, root) for _ in range(NB)]
+    for i in range(max(len(b.ops) for b in branches)):
+        rep = []
+        for k, br in zip(kids, branches):
+            if i < len(br.ops):
+                if br.ops[i][0] == "drop":
+                    abi.akv_drop(h, k, br.ops[i][1])
+                else:
+                    rep.append(k)
+        if rep:
+            abi.akv_reposition(h, rep)
+    abi.akv_append(h, kids, [1] * NB, raw.ctypes.data, raw.ctypes.data)
+    q = np.zeros(NB * sh.hq * sh.head_dim, np.uint16)
+    out = np.zeros(NB * sh.hq * sh.head_dim, np.float32)
+    abi.akv_decode_attention(h, 0, q.ctypes.data, kids, out.ctypes.data)
+    st = abi.akv_decode_plan_stats(h)
+    assert st["shared_items"] > 0
+    assert st["shared_items"] * sh.hkv <= 2 * 152
+    # every branch is merged by one item of the one-row kernel at least
+    assert st["items"] - st["shared_items"] >= NB
+    assert st["members"] >= 2 * st["shared_items"]
+    for k in kids:
+        abi.akv_seq_free(h, k)
+    abi.akv_seq_free(h, root)
+    assert abi.akv_pool_stats(h)[1] == 0
+    abi.akv_cache_destroy(h)
