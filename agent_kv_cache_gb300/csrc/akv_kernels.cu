@@ -90,21 +90,24 @@ __device__ __forceinline__ bool cancels(float x, float y, float xo, float yo) {
 }
 
 // Recompute the cancelling pairs of one unit (E pairs; table entry of pair
-// e at cs[e * stride], its low part at lo[e * stride]) and overwrite them in
-// dst_lo / dst_hi.
+// e at cs[e * cs_stride], its low part at lo[e * lo_stride] with the sine's
+// part times lo_sy, or zero when lo is null) and overwrite them in dst_lo /
+// dst_hi.  `lo` may point to global memory: this path is rare.
 template <int E>
 __device__ __noinline__ void refine_cancelling(uint4 u_lo, uint4 u_hi, __nv_bfloat16* dst_lo,
                                                __nv_bfloat16* dst_hi, const float2* cs,
-                                               const float2* lo, int stride) {
+                                               int cs_stride, const float2* lo, int lo_stride,
+                                               float lo_sy) {
   float x[E], y[E];
   Vec<__nv_bfloat16>::unpack(u_lo, x);
   Vec<__nv_bfloat16>::unpack(u_hi, y);
   for (int e = 0; e < E; ++e) {
-    const float2 t = cs[e * stride];
+    const float2 t = cs[e * cs_stride];
     const float xo = fmaf(x[e], t.x, -y[e] * t.y);
     const float yo = fmaf(x[e], t.y, y[e] * t.x);
     if (!cancels(x[e], y[e], xo, yo)) continue;
-    const float2 l = lo[e * stride];
+    float2 l = lo ? lo[e * lo_stride] : make_float2(0.f, 0.f);
+    l.y *= lo_sy;
     // x (c + cl) - y (s + sl) and x (s + sl) + y (c + cl); each product with
     // the fp32 entry split into its rounded value and its exact error
     const float p1 = x[e] * t.x, e1 = fmaf(x[e], t.x, -p1);
@@ -141,17 +144,19 @@ __device__ __forceinline__ void rotate_unit(const T* src, T* dst, int c, int hal
   st16(dst + c * E, Vec<T>::pack(xo));
   st16(dst + half + c * E, Vec<T>::pack(yo));
   if constexpr (std::is_same<T, __nv_bfloat16>::value)
-    if (any) refine_cancelling<E>(lo, hi, dst + c * E, dst + half + c * E, cs_row + c * E,
-                                  lo_row + c * E, 1);
+    if (any) refine_cancelling<E>(lo, hi, dst + c * E, dst + half + c * E, cs_row + c * E, 1,
+                                  lo_row + c * E, 1, 1.f);
 }
 
 // The same rotation on a unit already loaded into registers, with the row's
 // cos/sin stored unit-minor: pair c*E + e at cs_t[e * n_units + c], so the
 // lanes rotating one row read consecutive words (no bank conflicts); the low
-// parts in lo_t, same layout.
+// parts of the row's entries in the table's own row lo_row (pair order, read
+// only for a cancelling pair; null: zero), the sine's part times lo_sy.
 template <typename T>
 __device__ __forceinline__ void rotate_regs(uint4 lo, uint4 hi, T* dst, int c, int half,
-                                            const float2* cs_t, const float2* lo_t, int n_units) {
+                                            const float2* cs_t, int n_units, const float2* lo_row,
+                                            float lo_sy) {
   constexpr int E = Vec<T>::E;
   float x[E], y[E], xo[E], yo[E];
   Vec<T>::unpack(lo, x);
@@ -167,8 +172,8 @@ __device__ __forceinline__ void rotate_regs(uint4 lo, uint4 hi, T* dst, int c, i
   st16(dst + c * E, Vec<T>::pack(xo));
   st16(dst + half + c * E, Vec<T>::pack(yo));
   if constexpr (std::is_same<T, __nv_bfloat16>::value)
-    if (any) refine_cancelling<E>(lo, hi, dst + c * E, dst + half + c * E, cs_t + c, lo_t + c,
-                                  n_units);
+    if (any) refine_cancelling<E>(lo, hi, dst + c * E, dst + half + c * E, cs_t + c, n_units,
+                                  lo_row ? lo_row + c * E : nullptr, 1, lo_sy);
 }
 
 template <typename T>
@@ -499,7 +504,9 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, uint32_t li
 // fork: for every (layer, KV head) tile of destination page `dpage`, rows
 // t of the stage receive source rows (s_src_page[t], s_src_off[t]) through
 // one bulk copy per run, keys with s_rot[t] set are rotated in place with the
-// row's cos/sin (s_cs, unit-minor; their low parts in s_lo, same layout),
+// row's cos/sin (s_cs, unit-minor; their low parts read from the table's row
+// s_lrow[t] of g.cs_lo when a pair nearly cancels, the sine's part times
+// s_lsy[t]),
 // and rows [0, n_store) go out with one
 // bulk copy per tensor.  Rows without a source (dead slots of a prefix fork)
 // are written as zeros, so that a stored slot never holds stale bits.  Layers
@@ -507,7 +514,7 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, uint32_t li
 template <typename T>
 __device__ __forceinline__ void tile_pipeline(
     const Geom& g, int l_begin, int l_end, unsigned char* stage0, const float2* s_cs,
-    const float2* s_lo, const int* s_src_page,
+    const int* s_lrow, const float* s_lsy, const int* s_src_page,
     const int* s_src_off, const int* s_rot, const int* s_run_t0, const int* s_run_len, int n_runs,
     uint32_t bytes, int dpage, int n_store, int n_stages, uint64_t* s_full, uint32_t* err,
     uint32_t wait_limit) {
@@ -558,7 +565,8 @@ __device__ __forceinline__ void tile_pipeline(
       T* row = kt + (size_t)t * D;
       const uint4 lo = *reinterpret_cast<const uint4*>(row + c * E);
       const uint4 hi = *reinterpret_cast<const uint4*>(row + RH + c * E);
-      rotate_regs<T>(lo, hi, row, c, RH, s_cs + t * RH, s_lo + t * RH, kr);
+      rotate_regs<T>(lo, hi, row, c, RH, s_cs + t * RH, kr,
+                     s_lrow[t] >= 0 ? g.cs_lo + (int64_t)s_lrow[t] * RH : nullptr, s_lsy[t]);
     }
     if (n_dead > 0) {
       const int ch = (int)(row_bytes / 16);      // 16-byte chunks of a row
@@ -629,8 +637,8 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
   const uint32_t tile_bytes = S * row_bytes;                 // one (layer, head) tile of one tensor
   unsigned char* stage0 = gsm;                                // [n_stages][K, V][S][D]
   float2* s_cs = reinterpret_cast<float2*>(gsm + (size_t)n_stages * 2 * tile_bytes);   // [S][R/2]
-  float2* s_lo = s_cs + S * RH;                                                         // [S][R/2]
-  __shared__ int s_src_page[64], s_src_off[64], s_rot[64];
+  __shared__ int s_src_page[64], s_src_off[64], s_rot[64], s_lrow[64];
+  __shared__ float s_lsy[64];
   __shared__ int s_run_t0[64], s_run_len[64], s_n_runs, s_dst_page;
   __shared__ uint32_t s_bytes;
   __shared__ __align__(8) uint64_t s_full[8];
@@ -657,19 +665,18 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
     s_src_page[t] = sp;
     s_src_off[t] = src % S;
     s_rot[t] = src != j;
+    // the keys move down by delta = src - j: rotation by -delta
+    s_lrow[t] = (src - j >= 0 && src - j < sa.max_slots) ? src - j : -1;
+    s_lsy[t] = -1.f;
   }
   {
     const int kr = RH / E;
     for (int i = tid; i < nj * RH; i += kGatherThreads) {
       const int t = i / RH, jj = i % RH;
       const int delta = gather[j0 + t] - (j0 + t);
-      float2 c = make_float2(1.f, 0.f), l = make_float2(0.f, 0.f);
-      if (delta >= 0 && delta < sa.max_slots) {
-        c = cs[(int64_t)delta * RH + jj];
-        l = g.cs_lo[(int64_t)delta * RH + jj];
-      }
+      float2 c = make_float2(1.f, 0.f);
+      if (delta >= 0 && delta < sa.max_slots) c = cs[(int64_t)delta * RH + jj];
       s_cs[t * RH + (jj % E) * kr + jj / E] = make_float2(c.x, -c.y);
-      s_lo[t * RH + (jj % E) * kr + jj / E] = make_float2(l.x, -l.y);
     }
   }
   if (tid == 0) {
@@ -687,7 +694,7 @@ k_gather(Geom g, SeqArrays sa, const ReposItem* __restrict__ items, int n_items,
   if (dpage < 0) return;
   const int lper = (g.layers + gridDim.y - 1) / gridDim.y;    // layers of this block
   tile_pipeline<T>(g, blockIdx.y * lper, min(g.layers, (int)(blockIdx.y + 1) * lper), stage0, s_cs,
-                   s_lo, s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes, dpage, nj,
+                   s_lrow, s_lsy, s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes, dpage, nj,
                    n_stages, s_full, err, wait_limit);
 }
 
@@ -712,8 +719,8 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
   const uint32_t tile_bytes = S * row_bytes;
   unsigned char* stage0 = gsm;                                // [n_stages][K, V][S][D]
   float2* s_cs = reinterpret_cast<float2*>(gsm + (size_t)n_stages * 2 * tile_bytes);   // [S][R/2]
-  float2* s_lo = s_cs + S * RH;                                                         // [S][R/2]
-  __shared__ int s_src_page[64], s_src_off[64], s_rot[64], s_delta[64];
+  __shared__ int s_src_page[64], s_src_off[64], s_rot[64], s_delta[64], s_lrow[64];
+  __shared__ float s_lsy[64];
   __shared__ int s_run_t0[64], s_run_len[64], s_n_runs, s_n_store;
   __shared__ uint32_t s_bytes;
   __shared__ __align__(8) uint64_t s_full[8];
@@ -754,9 +761,12 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
     const int delta = s_delta[t];
     const int a = delta < 0 ? -delta : delta;
     const float2 c = a < max_pos ? cs[(int64_t)a * RH + j] : make_float2(1.f, 0.f);
-    const float2 l = a < max_pos ? g.cs_lo[(int64_t)a * RH + j] : make_float2(0.f, 0.f);
     s_cs[t * RH + (j % E) * kr + j / E] = make_float2(c.x, delta < 0 ? -c.y : c.y);
-    s_lo[t * RH + (j % E) * kr + j / E] = make_float2(l.x, delta < 0 ? -l.y : l.y);
+  }
+  for (int t = tid; t < n_store; t += kGatherThreads) {
+    const int a = s_delta[t] < 0 ? -s_delta[t] : s_delta[t];
+    s_lrow[t] = a < max_pos ? a : -1;
+    s_lsy[t] = s_delta[t] < 0 ? -1.f : 1.f;
   }
   if (tid == 0) {
     for (int st = 0; st < n_stages; ++st)
@@ -767,7 +777,7 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
   __syncthreads();
   const int lper = (g.phys_layers + gridDim.y - 1) / gridDim.y;   // slabs of this block
   tile_pipeline<T>(g, blockIdx.y * lper, min(g.phys_layers, (int)(blockIdx.y + 1) * lper), stage0,
-                   s_cs, s_lo, s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes,
+                   s_cs, s_lrow, s_lsy, s_src_page, s_src_off, s_rot, s_run_t0, s_run_len, s_n_runs, s_bytes,
                    mb.dst_page, n_store, n_stages, s_full, err, wait_limit);
 }
 
@@ -799,7 +809,7 @@ cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves,
   const size_t elem = g.dtype == AKV_DTYPE_BF16 ? 2 : 4;
   const size_t tile = (size_t)g.s * g.d * elem;
   const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
-  const size_t smem = (size_t)n_stages * 2 * tile + 2 * (size_t)g.s * (g.rope / 2) * sizeof(float2);
+  const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
   const dim3 grid(n_blocks, layer_groups(n_blocks, g.phys_layers));
   if (g.dtype == AKV_DTYPE_BF16) {
     cudaFuncSetAttribute(k_transplant<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -905,7 +915,7 @@ cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* i
   const size_t elem = g.dtype == AKV_DTYPE_BF16 ? 2 : 4;
   const size_t tile = (size_t)g.s * g.d * elem;             // one (layer, head) tile, one tensor
   const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
-  const size_t smem = (size_t)n_stages * 2 * tile + 2 * (size_t)g.s * (g.rope / 2) * sizeof(float2);
+  const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
   const dim3 grid(n_blocks, layer_groups(n_blocks, g.layers));
   if (g.dtype == AKV_DTYPE_BF16) {
     cudaFuncSetAttribute(k_gather<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
