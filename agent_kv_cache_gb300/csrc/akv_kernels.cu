@@ -11,6 +11,7 @@
 // touching memory out of bounds, sets a bit in the device error word and
 // skips the access.
 #include <algorithm>
+#include <cmath>
 #include <type_traits>
 
 #include <cuda_bf16.h>
@@ -427,7 +428,6 @@ k_compact(Geom g, SeqArrays sa, const ReposItem* __restrict__ items,
   int32_t* active = sa.active + (int64_t)it.dslot * sa.seq_pages;
   int32_t* oldp = sa.old_pages + (int64_t)it.dslot * sa.seq_pages;
   int32_t* gather = sa.gather + (int64_t)it.dslot * sa.max_slots;
-  const int S = g.s;
 
   // snapshot the page ids the gather will read from
   for (int k = it.n_kept + (int)threadIdx.x; k < it.old_pages; k += blockDim.x)
@@ -787,10 +787,14 @@ k_transplant(Geom g, const MoveItem* __restrict__ moves, int n_moves,
 // launchers
 // ---------------------------------------------------------------------------
 
-// Layer groups per destination page: enough (page, layer group) blocks for
-// about 32 per SM, so small calls still fill the GPU evenly; at most one
-// group per layer.
-inline int layer_groups(int n_blocks, int n_layers) {
+// Layer groups per destination page.  At least enough (page, layer group)
+// blocks for about 32 per SM, so small calls still fill the GPU evenly; then
+// the count (up to four times that, at most one group per layer) whose
+// blocks fill their last wave best: every block moves the same tiles, so a
+// last wave of a few blocks runs nearly as long as a full one, against a
+// block's fixed start-up of about four tiles.  `per_sm`: blocks resident per
+// SM; `tiles`: (layer, head) tiles of one page over all its layers.
+inline int layer_groups(int n_blocks, int n_layers, int per_sm, int tiles) {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0;
@@ -798,8 +802,31 @@ inline int layer_groups(int n_blocks, int n_layers) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
   }
-  const int want = (32 * sms + n_blocks - 1) / n_blocks;
-  return std::max(1, std::min(n_layers, want));
+  const int g0 = std::max(1, std::min(n_layers, (32 * sms + n_blocks - 1) / n_blocks));
+  const double slots = (double)std::max(1, per_sm) * sms;
+  int best = g0;
+  double best_cost = 0.0;
+  for (int gr = g0; gr <= std::min(n_layers, 4 * g0); ++gr) {
+    const double waves = (double)n_blocks * gr / slots;
+    const double per_block = (double)tiles / gr;             // tiles of one block
+    const double cost = std::ceil(waves) * (per_block + 4.0);
+    if (gr == g0 || cost < best_cost) {
+      best = gr;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// Blocks of `kernel` resident per SM with `smem` bytes of dynamic shared
+// memory (which it is also allowed here).
+template <typename K>
+int resident_blocks(K kernel, size_t smem) {
+  int n = 0;
+  cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kGatherThreads, smem) != cudaSuccess)
+    return 1;
+  return std::max(1, n);
 }
 
 cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves,
@@ -810,7 +837,9 @@ cudaError_t launch_transplant(const Geom& g, const MoveItem* moves, int n_moves,
   const size_t tile = (size_t)g.s * g.d * elem;
   const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
   const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
-  const dim3 grid(n_blocks, layer_groups(n_blocks, g.phys_layers));
+  const int per_sm = g.dtype == AKV_DTYPE_BF16 ? resident_blocks(k_transplant<__nv_bfloat16>, smem)
+                                              : resident_blocks(k_transplant<float>, smem);
+  const dim3 grid(n_blocks, layer_groups(n_blocks, g.phys_layers, per_sm, g.phys_layers * g.hkv));
   if (g.dtype == AKV_DTYPE_BF16) {
     cudaFuncSetAttribute(k_transplant<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k_transplant<__nv_bfloat16><<<grid, kGatherThreads, smem, st>>>(
@@ -916,7 +945,9 @@ cudaError_t launch_gather(const Geom& g, const SeqArrays& sa, const ReposItem* i
   const size_t tile = (size_t)g.s * g.d * elem;             // one (layer, head) tile, one tensor
   const int n_stages = (int)std::max<size_t>(2, std::min<size_t>(4, (96 << 10) / (2 * tile)));
   const size_t smem = (size_t)n_stages * 2 * tile + (size_t)g.s * (g.rope / 2) * sizeof(float2);
-  const dim3 grid(n_blocks, layer_groups(n_blocks, g.layers));
+  const int per_sm = g.dtype == AKV_DTYPE_BF16 ? resident_blocks(k_gather<__nv_bfloat16>, smem)
+                                              : resident_blocks(k_gather<float>, smem);
+  const dim3 grid(n_blocks, layer_groups(n_blocks, g.layers, per_sm, g.layers * g.hkv));
   if (g.dtype == AKV_DTYPE_BF16) {
     cudaFuncSetAttribute(k_gather<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k_gather<__nv_bfloat16><<<grid, kGatherThreads, smem, st>>>(g, sa, items, n_items, cs, err,
