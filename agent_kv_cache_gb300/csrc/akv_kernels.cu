@@ -396,25 +396,26 @@ k_drop(Geom g, SeqArrays sa, const DropItem* __restrict__ items,
   }
   __syncthreads();
 
-  int carry = 0;
-  for (int base = 0; base < it.n_pages; base += blockDim.x) {
-    const int k = base + threadIdx.x;
-    int live = 0;
-    if (k < it.n_pages) {
-      live = page_popc(keep, k, S) > 0;
-      if (!live && (int64_t)(k + 1) * S <= it.n_slots) pages[k] = -1;
-    }
-    const int pos = block_exclusive_scan(live, s_warp, &s_total);
-    if (live) active[carry + pos] = k;
-    carry += s_total;
+  // each thread a run of consecutive pages: one block scan of the run counts
+  // (not one per blockDim pages), then each run writes its live pages in order
+  const int per = (it.n_pages + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int k0 = (int)threadIdx.x * per, k1 = min(it.n_pages, k0 + per);
+  int live_n = 0;
+  for (int k = k0; k < k1; ++k) {
+    const bool live = page_popc(keep, k, S) > 0;
+    if (!live && (int64_t)(k + 1) * S <= it.n_slots) pages[k] = -1;
+    live_n += live;
   }
-  if (threadIdx.x == 0 && carry != it.expect_active) flag(err, AKV_DERR_COUNT);
+  int o = block_exclusive_scan(live_n, s_warp, &s_total);
+  for (int k = k0; k < k1; ++k)
+    if (page_popc(keep, k, S) > 0) active[o++] = k;
+  if (threadIdx.x == 0 && s_total != it.expect_active) flag(err, AKV_DERR_COUNT);
 }
 
 // ---------------------------------------------------------------------------
 // reposition, part 1: compaction.  Exclusive prefix sum of the keep bits
-// (ballot-free: each thread owns one 32-slot word, popc + block scan) gives
-// the gather map; the new page table, keep bits and active list follow.
+// (each thread owns a run of 32-slot words: popc + one block scan) gives the
+// gather map; the new page table, keep bits and active list follow.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(1024)
@@ -433,19 +434,23 @@ k_compact(Geom g, SeqArrays sa, const ReposItem* __restrict__ items,
   for (int k = it.n_kept + (int)threadIdx.x; k < it.old_pages; k += blockDim.x)
     oldp[k] = pages[k];
 
-  // gather map: new slot j <- old slot of the j-th set keep bit
+  // gather map: new slot j <- old slot of the j-th set keep bit.  Each
+  // thread owns a run of consecutive words: one block scan of the runs'
+  // counts, then each run writes its entries in order.
   const int nw = (it.old_slots + 31) / 32;
-  int carry = 0;
-  for (int base = 0; base < nw; base += blockDim.x) {
-    const int w = base + threadIdx.x;
-    uint32_t bits = 0;
-    if (w < nw) {
-      bits = keep[w];
-      const int tail = it.old_slots - w * 32;
-      if (tail < 32) bits &= (1u << tail) - 1u;
-    }
-    const int pos = block_exclusive_scan(__popc(bits), s_warp, &s_total);
-    int j = carry + pos;
+  auto word = [&](int w) {
+    uint32_t bits = keep[w];
+    const int tail = it.old_slots - w * 32;
+    if (tail < 32) bits &= (1u << tail) - 1u;
+    return bits;
+  };
+  const int per = (nw + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int w0 = (int)threadIdx.x * per, w1 = min(nw, w0 + per);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(word(w));
+  int j = block_exclusive_scan(cnt, s_warp, &s_total);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = word(w);
     while (bits) {
       const int b = __ffs(bits) - 1;
       bits &= bits - 1u;
@@ -453,9 +458,8 @@ k_compact(Geom g, SeqArrays sa, const ReposItem* __restrict__ items,
       else flag(err, AKV_DERR_INDEX);
       ++j;
     }
-    carry += s_total;
   }
-  if (threadIdx.x == 0 && carry != it.r) flag(err, AKV_DERR_COUNT);
+  if (threadIdx.x == 0 && s_total != it.r) flag(err, AKV_DERR_COUNT);
   __syncthreads();
 
   // new page table: kept prefix unchanged, fresh ids after, released tail
