@@ -122,38 +122,13 @@ __device__ __noinline__ void refine_cancelling(uint4 u_lo, uint4 u_hi, __nv_bflo
   }
 }
 
-// One rotation unit: E consecutive pairs (i, i + D/2) starting at i = c*E.
-// (x, y) -> (x cos - y sin, x sin + y cos), fp32, rounded once to T.
-// `lo_row`: the low parts of the row's table entries (same layout).
-template <typename T>
-__device__ __forceinline__ void rotate_unit(const T* src, T* dst, int c, int half,
-                                            const float2* cs_row, const float2* lo_row) {
-  constexpr int E = Vec<T>::E;
-  const uint4 lo = ld16(src + c * E);
-  const uint4 hi = ld16(src + half + c * E);
-  float x[E], y[E], xo[E], yo[E];
-  Vec<T>::unpack(lo, x);
-  Vec<T>::unpack(hi, y);
-  bool any = false;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const float2 t = cs_row[c * E + e];
-    xo[e] = fmaf(x[e], t.x, -y[e] * t.y);
-    yo[e] = fmaf(x[e], t.y, y[e] * t.x);
-    any |= cancels(x[e], y[e], xo[e], yo[e]);
-  }
-  st16(dst + c * E, Vec<T>::pack(xo));
-  st16(dst + half + c * E, Vec<T>::pack(yo));
-  if constexpr (std::is_same<T, __nv_bfloat16>::value)
-    if (any) refine_cancelling<E>(lo, hi, dst + c * E, dst + half + c * E, cs_row + c * E, 1,
-                                  lo_row + c * E, 1, 1.f);
-}
-
-// The same rotation on a unit already loaded into registers, with the row's
-// cos/sin stored unit-minor: pair c*E + e at cs_t[e * n_units + c], so the
-// lanes rotating one row read consecutive words (no bank conflicts); the low
-// parts of the row's entries in the table's own row lo_row (pair order, read
-// only for a cancelling pair; null: zero), the sine's part times lo_sy.
+// One rotation unit, already loaded into registers: E consecutive pairs
+// (i, i + D/2) starting at i = c*E, (x, y) -> (x cos - y sin, x sin + y cos)
+// in fp32, rounded once to T, with the row's cos/sin stored unit-minor:
+// pair c*E + e at cs_t[e * n_units + c], so the lanes rotating one row read
+// consecutive words (no bank conflicts); the low parts of the row's entries
+// in the table's own row lo_row (pair order, read only for a cancelling
+// pair; null: zero), the sine's part times lo_sy.
 template <typename T>
 __device__ __forceinline__ void rotate_regs(uint4 lo, uint4 hi, T* dst, int c, int half,
                                             const float2* cs_t, int n_units, const float2* lo_row,
@@ -191,13 +166,13 @@ __device__ __forceinline__ void flag(uint32_t* err, uint32_t bit) { atomicOr(err
 // ---------------------------------------------------------------------------
 
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
          const AppendBlock* __restrict__ blocks, const int32_t* __restrict__ ids,
          const int32_t* __restrict__ act, const T* __restrict__ k_raw,
          const T* __restrict__ v_raw, int64_t total_tokens,
          const float2* __restrict__ cs, uint32_t* err, AppendLimits lim) {
-  extern __shared__ float2 s_cs[];   // [kAppendTokens][R/2] cos/sin, then their low parts
+  extern __shared__ float2 s_cs[];   // [kAppendTokens][R/2] cos/sin, unit-minor
   __shared__ int s_page[kAppendTokens];
   __shared__ int s_off[kAppendTokens];
   const AppendBlock blk = blocks[blockIdx.x];
@@ -249,23 +224,28 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     s_page[t] = pid;
     s_off[t] = slot % S;
   }
+  // the rows' cos/sin, unit-minor (pair c*E + e of row t at
+  // s_cs[t*RH + e*kr + c]: the lanes rotating one row read consecutive words)
+  constexpr int E = Vec<T>::E;
   const int R = g.rope, RH = R / 2;
-  float2* s_lo = s_cs + kAppendTokens * RH;
+  const int kr = RH / E, kc = (D - R) / E, vu = D / E, per_row = kr + kc + vu;
   for (int i = tid; i < nt * RH; i += bs) {
-    const int slot = it.slot0 + blk.t0 + i / RH;
+    const int t = i / RH, jj = i % RH;
+    const int slot = it.slot0 + blk.t0 + t;
     const bool in = slot >= 0 && slot < sa.max_slots;
-    s_cs[i] = in ? cs[(int64_t)slot * RH + i % RH] : make_float2(1.f, 0.f);
-    s_lo[i] = in ? g.cs_lo[(int64_t)slot * RH + i % RH] : make_float2(0.f, 0.f);
+    s_cs[t * RH + (jj % E) * kr + jj / E] = in ? cs[(int64_t)slot * RH + jj] : make_float2(1.f, 0.f);
   }
   __syncthreads();
 
   // units of a row: rotary (pairs of 16-byte chunks), K dims past the rotary
-  // part (copied), V chunks (copied)
-  constexpr int E = Vec<T>::E;
-  const int kr = RH / E, kc = (D - R) / E, vu = D / E, per_row = kr + kc + vu;
+  // part (copied), V chunks (copied).  A thread's unit goes to several
+  // layers: the loads of kLayerBatch of them go out before their stores
+  // (they are independent; the stores keep layer order, so a slab shared by
+  // several logical layers keeps the last one).
+  constexpr int kLayerBatch = 2;
   const int units = g.hkv * nt * per_row;
-  const T* kb = k_raw;
-  const T* vb = v_raw;
+  const T* __restrict__ kb = k_raw;
+  const T* __restrict__ vb = v_raw;
   T* kp = static_cast<T*>(g.k);
   T* vp = static_cast<T*>(g.v);
   for (int u = tid; u < units; u += bs) {
@@ -277,17 +257,32 @@ k_append(Geom g, SeqArrays sa, const AppendItem* __restrict__ items,
     const int64_t tok = it.tok0 + blk.t0 + t;
     const int64_t dst_off = (int64_t)pid * g.page_stride + (int64_t)h * g.head_stride +
                             (int64_t)s_off[t] * D;
-    for (int l = l_begin; l < g.layers; l += l_step) {
-      const int64_t src_off = ((int64_t)l * total_tokens + tok) * g.hkv * D + (int64_t)h * D;
-      const int64_t slab = (int64_t)(l % g.phys_layers) * g.layer_stride;
-      if (r < kr) {
-        rotate_unit<T>(kb + src_off, kp + slab + dst_off, r, RH, s_cs + t * RH, s_lo + t * RH);
-      } else if (r < kr + kc) {
-        const int o = R + (r - kr) * E;
-        st16(kp + slab + dst_off + o, ld16(kb + src_off + o));
-      } else {
-        const int c = r - kr - kc;
-        st16(vp + slab + dst_off + c * E, ld16(vb + src_off + c * E));
+    const int slot = it.slot0 + blk.t0 + t;
+    const float2* lo_row = (slot >= 0 && slot < sa.max_slots) ? g.cs_lo + (int64_t)slot * RH : nullptr;
+    // element offset of this unit in a source row and in a stored row
+    const int o_a = r < kr ? r * E : r < kr + kc ? R + (r - kr) * E : (r - kr - kc) * E;
+    const T* src = r < kr + kc ? kb : vb;
+    T* dst = r < kr + kc ? kp : vp;
+    for (int l0 = l_begin; l0 < g.layers; l0 += kLayerBatch * l_step) {
+      uint4 a[kLayerBatch], b[kLayerBatch];
+#pragma unroll
+      for (int q = 0; q < kLayerBatch; ++q) {
+        const int l = l0 + q * l_step;
+        if (l < g.layers) {
+          const int64_t src_off = ((int64_t)l * total_tokens + tok) * g.hkv * D + (int64_t)h * D;
+          a[q] = ld16(src + src_off + o_a);
+          if (r < kr) b[q] = ld16(src + src_off + RH + o_a);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kLayerBatch; ++q) {
+        const int l = l0 + q * l_step;
+        if (l >= g.layers) break;
+        T* row = dst + (int64_t)(l % g.phys_layers) * g.layer_stride + dst_off;
+        if (r < kr)
+          rotate_regs<T>(a[q], b[q], row, r, RH, s_cs + t * RH, kr, lo_row, 1.f);
+        else
+          st16(row + o_a, a[q]);
       }
     }
   }
@@ -862,7 +857,7 @@ cudaError_t launch_append(const Geom& g, const SeqArrays& sa, const AppendItem* 
                           int64_t total_tokens, const float2* cs, uint32_t* err,
                           AppendLimits lim, cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
-  const size_t smem = 2 * (size_t)kAppendTokens * (g.rope / 2) * sizeof(float2);
+  const size_t smem = (size_t)kAppendTokens * (g.rope / 2) * sizeof(float2);
   const dim3 grid(n_blocks, g.phys_layers);
   if (g.dtype == AKV_DTYPE_BF16)
     k_append<__nv_bfloat16><<<grid, 256, smem, st>>>(
