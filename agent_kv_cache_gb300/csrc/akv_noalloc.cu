@@ -68,11 +68,22 @@ __global__ void __launch_bounds__(kWarps * 32) k_noalloc_decode(const __grid_con
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (r.pos_q >= 0) {
+    // The angle pos * theta^(-2d/D) in fp64 (positions reach 10^5 radians),
+    // reduced to one turn in fp64, then cos/sin in fp32: four fp64
+    // operations per pair, on a part whose fp64 rate is low.  The
+    // frequencies once per block.
+    __shared__ double s_w[H];
+    const double l2t = log2(a.theta);
+    for (int d = tid; d < H; d += blockDim.x) s_w[d] = exp2(-2.0 * d / D * l2t);
+    __syncthreads();
     const T* q = static_cast<const T*>(a.q) + ((int64_t)row * a.hq + (int64_t)kvh * G) * D;
     for (int i = tid; i < G * H; i += blockDim.x) {
       const int gq = i / H, d = i % H;
-      const double ang = (double)r.pos_q * pow(a.theta, -2.0 * d / D);
-      const float c = (float)cos(ang), sn = (float)sin(ang);
+      const double ang = (double)r.pos_q * s_w[d];
+      const double turns = rint(ang * 0.15915494309189535);       // ang / (2 pi)
+      const float red = (float)fma(-turns, 6.283185307179586, ang);
+      float sn, c;
+      sincosf(red, &sn, &c);
       const float x = to_f(q[gq * D + d]), y = to_f(q[gq * D + d + H]);
       s_q[gq][d] = fmaf(x, c, -y * sn) * a.scale_log2;
       s_q[gq][d + H] = fmaf(x, sn, y * c) * a.scale_log2;
