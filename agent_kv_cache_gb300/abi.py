@@ -126,6 +126,11 @@ SIGNATURES = {
     "akv_set_layer_window": (ctypes.c_int, [_P, _I32, _I32]),
     "akv_restore_attention": (ctypes.c_int, [_P, ctypes.POINTER(AkvOp), _I32, _I32, _P, _P, _P,
                                              _I32, _P]),
+    "akv_restore_attention_tokens": (ctypes.c_int, [_P, ctypes.POINTER(AkvOp), _I32, _I32, _P, _P,
+                                                    _P, _I32, _PI32, _I32, _P]),
+    "akv_restore_plan_recovery": (ctypes.c_int, [ctypes.POINTER(AkvOp), _I32, _I32,
+                                                 ctypes.POINTER(ctypes.c_uint8),
+                                                 ctypes.POINTER(ctypes.c_uint8), _PI32, _PI32]),
     "akv_decode_attention_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                                     ctypes.c_double, _P, _P, _P, _I32, _I32,
                                                     _PI32, _PI32, _P, _P, _I32, _P]),
@@ -357,6 +362,33 @@ def akv_restore_attention(cache, program, layer, q, k_raw, v, n_tokens, out):
     _check(lib().akv_restore_attention(cache, arr, len(program), layer, q, k_raw, v, n_tokens,
                                        out), cache)
     del keep
+
+
+def akv_restore_attention_tokens(cache, program, layer, q, k_raw, v, n_tokens, tokens, out):
+    arr, keep = make_program(program)
+    tk, ptk = _arr(tokens, np.int32, ctypes.c_int32)
+    _check(lib().akv_restore_attention_tokens(cache, arr, len(program), layer, q, k_raw, v,
+                                              n_tokens, ptk, len(tk), out), cache)
+    del keep
+
+
+def akv_restore_plan_recovery(program, n_tokens, missing, need=None):
+    """Tokens to recompute (increasing), given per-token missing / need flags
+    (need None: the tokens active at the end of the program)."""
+    arr, keep = make_program(program)
+    u8 = ctypes.POINTER(ctypes.c_uint8)
+    m = np.ascontiguousarray(np.asarray(missing, dtype=np.uint8).reshape(-1))
+    nd = None if need is None else np.ascontiguousarray(np.asarray(need, dtype=np.uint8).reshape(-1))
+    if m.size != n_tokens or (nd is not None and nd.size != n_tokens):
+        raise ValueError("missing / need need one flag per token")
+    out = np.zeros(max(1, n_tokens), np.int32)
+    n = ctypes.c_int32(0)
+    _check(lib().akv_restore_plan_recovery(
+        arr, len(program), n_tokens, m.ctypes.data_as(u8),
+        nd.ctypes.data_as(u8) if nd is not None else None,
+        out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ctypes.byref(n)))
+    del keep
+    return out[:n.value].tolist()
 
 
 def akv_set_layer_window(cache, layer, window):

@@ -77,6 +77,26 @@ class Cache:
                                   v.data_ptr(), n, out.data_ptr())
         return out
 
+    def restore_attention_tokens(self, program, layer, q, k_raw, v, tokens, out=None):
+        """Restore attention of the tokens `tokens` (increasing) only: rows of
+        `out` [T, hq, D] fp32 for those tokens are written, the rest kept;
+        q, k_raw, v cover all T tokens of the program."""
+        torch = self.torch
+        n = q.shape[0]
+        if out is None:
+            out = torch.zeros((n, self.hq, self.d), dtype=torch.float32, device="cuda")
+        assert q.is_contiguous() and k_raw.is_contiguous() and v.is_contiguous()
+        abi.akv_restore_attention_tokens(self.handle, program, layer, q.data_ptr(),
+                                         k_raw.data_ptr(), v.data_ptr(), n, tokens,
+                                         out.data_ptr())
+        return out
+
+    @staticmethod
+    def plan_recovery(program, n_tokens, missing, need=None):
+        """Tokens of `program` to recompute when the tokens flagged in
+        `missing` lost their KV (host only; see akv_restore_plan_recovery)."""
+        return abi.akv_restore_plan_recovery(program, n_tokens, missing, need)
+
     # -- history-keyed prefix sharing ----------------------------------------
     def prefix_publish(self, index, seq, program, token_ids):
         """Publish `seq` (whose history is `program` with `token_ids`) into a

@@ -1609,12 +1609,25 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
 
 // ---- segment-batch restore attention -------------------------------------------
 
-int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_t layer,
-                          const void* q, const void* k_raw, const void* v, int32_t n_tokens,
-                          float* out) {
+namespace {
+
+// Restore attention of the tokens with want[t] (all of them when `sel` is
+// null; else the n_sel increasing tokens of `sel`).
+int restore_impl(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_t layer, const void* q,
+                 const void* k_raw, const void* v, int32_t n_tokens, const int32_t* sel,
+                 int32_t n_sel, float* out) {
   if (!c || n_ops < 0 || (n_ops > 0 && !ops) || n_tokens < 0) return AKV_EINVAL;
   if (layer < 0 || layer >= c->cfg.layers) return fail(c, AKV_EINVAL, "layer %d out of range", layer);
   if (n_tokens > 0 && (!q || !k_raw || !v || !out)) return AKV_EINVAL;
+  std::vector<char> want(n_tokens, sel ? 0 : 1);
+  if (sel || n_sel) {
+    if (n_sel < 0 || (n_sel > 0 && !sel)) return AKV_EINVAL;
+    for (int32_t i = 0; i < n_sel; ++i) {
+      if (sel[i] < 0 || sel[i] >= n_tokens || (i > 0 && sel[i] <= sel[i - 1]))
+        return fail(c, AKV_EINVAL, "selected tokens must increase within [0, %d)", n_tokens);
+      want[sel[i]] = 1;
+    }
+  }
   // plan: times, eras, era slots (page 1 A.1.1: split at every drop/repos)
   constexpr int32_t kNever = INT32_MAX;
   std::vector<int32_t> held, pending;
@@ -1672,17 +1685,25 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
   }
   if (next != n_tokens) return fail(c, AKV_EINVAL, "program appends %d tokens, not %d", next, n_tokens);
   close_era();
-  if (n_tokens == 0) return AKV_OK;
+  if (n_tokens == 0 || (sel && n_sel == 0)) return AKV_OK;
+  // the selected queries, in order (the CUDA-core kernel takes one per block)
+  std::vector<RestoreQuery> squeries;
+  for (int32_t t = 0; t < n_tokens; ++t)
+    if (want[t]) squeries.push_back(queries[t]);
 
-  // tensor-core path: tiles of consecutive query tokens of one era
+  // tensor-core path: tiles of consecutive selected query tokens of one era
   std::vector<RestoreTile> tiles;
   const bool mma = restore_mma_supported(c->g) && !c->restore_generic;
   if (mma) {
     const int tt = restore_tile_tokens(c->g);
     const int32_t W = c->windows[layer];
     for (int32_t t = 0; t < n_tokens;) {
+      if (!want[t]) {
+        ++t;
+        continue;
+      }
       int32_t e = t + 1;
-      while (e < n_tokens && e - t < tt && queries[e].era_off == queries[t].era_off) ++e;
+      while (e < n_tokens && e - t < tt && want[e] && queries[e].era_off == queries[t].era_off) ++e;
       const int32_t lo = W > 0 ? std::max(0, queries[t].pos - W + 1) : 0;
       tiles.push_back({queries[t].era_off, t, e - t, lo, queries[e - 1].key_end});
       t = e;
@@ -1705,6 +1726,7 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
   Blob blob;
   const size_t o_keys = blob.put(keys.data(), keys.size());
   const size_t o_q = blob.put(queries.data(), queries.size());
+  const size_t o_sq = blob.put(squeries.data(), squeries.size());
   const size_t o_t = blob.put(tiles.data(), tiles.size());
   const size_t o_p = blob.put(pairs.data(), pairs.size());
   // scratch: [K versions | V versions | descriptor]
@@ -1735,8 +1757,10 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
   a.g = c->g;
   a.keys = reinterpret_cast<const RestoreKey*>(d + o_keys);
   a.n_keys = (int32_t)keys.size();
-  a.queries = reinterpret_cast<const RestoreQuery*>(d + o_q);
-  a.n_queries = n_tokens;
+  // the tensor-core kernels read queries by token, the CUDA-core one the
+  // selected ones in order
+  a.queries = reinterpret_cast<const RestoreQuery*>(d + (a.use_mma ? o_q : o_sq));
+  a.n_queries = a.use_mma ? n_tokens : (int32_t)squeries.size();
   a.q = q;
   a.k_raw = k_raw;
   a.v = v;
@@ -1751,6 +1775,80 @@ int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_
   a.err = c->d_err;
   CK(launch_restore(a, c->stream));
   c->launches += 2;
+  return AKV_OK;
+}
+
+}  // namespace
+
+int akv_restore_attention(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_t layer,
+                          const void* q, const void* k_raw, const void* v, int32_t n_tokens,
+                          float* out) {
+  return restore_impl(c, ops, n_ops, layer, q, k_raw, v, n_tokens, nullptr, 0, out);
+}
+
+int akv_restore_attention_tokens(akv_cache* c, const akv_op* ops, int32_t n_ops, int32_t layer,
+                                 const void* q, const void* k_raw, const void* v, int32_t n_tokens,
+                                 const int32_t* tokens, int32_t n_sel, float* out) {
+  if (n_sel > 0 && !tokens) return AKV_EINVAL;
+  static const int32_t kNone = 0;
+  return restore_impl(c, ops, n_ops, layer, q, k_raw, v, n_tokens, tokens ? tokens : &kNone,
+                      n_sel, out);
+}
+
+// Recovery plan (see akv.h).  A token u is in the plan when it is missing and
+// either needed or read by a plan token t > u: t's query read u when u was
+// still active at t's append (u dropped after t's append, or never).  Over
+// the plan tokens after u that holds for the earliest of them if it holds for
+// any (the earliest has the earliest append time), so one backward pass over
+// the tokens decides every token.
+int akv_restore_plan_recovery(const akv_op* ops, int32_t n_ops, int32_t n_tokens,
+                              const uint8_t* missing, const uint8_t* need,
+                              int32_t* tokens_out, int32_t* n_out) {
+  if (n_ops < 0 || (n_ops > 0 && !ops) || n_tokens < 0 || !n_out ||
+      (n_tokens > 0 && (!missing || !tokens_out)))
+    return AKV_EINVAL;
+  constexpr int64_t kNever = INT64_MAX;
+  std::vector<int64_t> birth(n_tokens, 0), death(n_tokens, kNever);
+  std::vector<char> alive(n_tokens, 0);
+  int32_t next = 0;
+  int64_t clock = 0;                     // one tick per appended token and per drop
+  for (int32_t i = 0; i < n_ops; ++i) {
+    const akv_op& op = ops[i];
+    if (op.kind == AKV_OP_APPEND) {
+      if (op.count < 0 || next + (int64_t)op.count > n_tokens) return AKV_EINVAL;
+      for (int32_t k = 0; k < op.count; ++k) {
+        birth[next] = clock++;
+        alive[next++] = 1;
+      }
+    } else if (op.kind == AKV_OP_DROP) {
+      if (op.count < 0 || (op.count > 0 && !op.ranges)) return AKV_EINVAL;
+      for (int32_t r = 0; r < op.count; ++r) {
+        const int64_t b = op.ranges[2 * r], e = op.ranges[2 * r + 1];
+        if (b < 0 || e < b || e > next) return AKV_ERANGE;
+        for (int64_t t = b; t < e; ++t)
+          if (alive[t]) {
+            alive[t] = 0;
+            death[t] = clock;
+          }
+      }
+      ++clock;
+    } else if (op.kind != AKV_OP_REPOS) {
+      return AKV_EINVAL;
+    }
+  }
+  if (next != n_tokens) return AKV_EINVAL;
+  int64_t first_birth = kNever;          // append time of the earliest plan token so far
+  int32_t n = 0;
+  for (int32_t u = n_tokens - 1; u >= 0; --u) {
+    if (!missing[u]) continue;
+    const bool needed = need ? need[u] != 0 : alive[u] != 0;
+    if (needed || death[u] > first_birth) {
+      tokens_out[n++] = u;
+      first_birth = birth[u];
+    }
+  }
+  std::reverse(tokens_out, tokens_out + n);
+  *n_out = n;
   return AKV_OK;
 }
 

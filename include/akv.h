@@ -222,6 +222,38 @@ int akv_restore_attention(akv_cache* cache, const akv_op* ops, int32_t n_ops, in
                           const void* q, const void* k_raw, const void* v,
                           int32_t n_tokens, float* out);
 
+/* The same for selected tokens only: out rows of tokens[0..n_sel) (host
+ * int32, increasing, each < n_tokens) are written, every other row is left
+ * as it is; q, k_raw and v still cover all n_tokens (every token's key
+ * versions are formed, since a selected query may read any earlier key).
+ * n_sel == 0 does nothing.  Used with akv_restore_plan_recovery to recompute
+ * only what is missing.  Errors: those of akv_restore_attention, and
+ * AKV_EINVAL for a token list that is not increasing or out of range. */
+int akv_restore_attention_tokens(akv_cache* cache, const akv_op* ops, int32_t n_ops,
+                                 int32_t layer, const void* q, const void* k_raw, const void* v,
+                                 int32_t n_tokens, const int32_t* tokens, int32_t n_sel,
+                                 float* out);
+
+/* Recovery plan of a restore ([Repo Review] AKV, 5.4: the dependencies of
+ * KV that later queries read but that is missing are closed backwards into
+ * the query ranges to recompute, resident ranges are kept; paper review
+ * 4.2.2 / A.1.1: a token's query reads the keys active when it was
+ * appended).  For the program ops[0..n_ops) of n_tokens appended tokens,
+ * with missing[t] != 0 for tokens whose KV is not resident and need[t] != 0
+ * for tokens whose KV the next step reads (need NULL: the tokens active at
+ * the end of the program), writes to tokens_out[0..*n_out), increasing, the
+ * least set of tokens that holds every needed missing token and, with each
+ * token in it, every missing token its query read (the tokens appended
+ * before it and not dropped by then).  Resident tokens are never in it.
+ *   missing, need : host uint8 [n_tokens]
+ *   tokens_out    : host int32, room for n_tokens
+ * Host only: no cache, no GPU work.  Errors: AKV_EINVAL (null pointer, bad
+ * op, the program appends a different number of tokens), AKV_ERANGE (drop
+ * range outside the tokens appended so far). */
+int akv_restore_plan_recovery(const akv_op* ops, int32_t n_ops, int32_t n_tokens,
+                              const uint8_t* missing, const uint8_t* need,
+                              int32_t* tokens_out, int32_t* n_out);
+
 /* ---- decode attention that allocates nothing (no counterpart in the paper) ----
  *
  * For callers that cannot allocate device memory: applications that reserve

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from agent_kv_cache_gb300 import abi, build
+from agent_kv_cache_gb300 import Cache, abi, build
 from workloads import synth, traces
 from twin import ATTN_TOL, Twin
 
@@ -332,6 +332,35 @@ def test_restore_attention_long_program(tc):
     t.set_window(1, 700)
     t.restore(prog, layer=0)
     t.restore(prog, layer=1)
+
+
+@pytest.mark.parametrize("tc", [1, 2, 0])
+def test_restore_recovers_only_the_planned_tokens(tc):
+    """A restore after some tokens lost their KV: the library's recovery plan
+    (which equals the oracle's) picks the tokens to recompute, and restore
+    attention over just those tokens gives each its original attention
+    (oracle replay of those tokens) and leaves every other output row alone.
+    Also: nothing selected, and every token selected."""
+    from oracle.akv_recovery import plan_recovery
+    rng = np.random.default_rng(31 + tc)
+    t = Twin(layers=2, hq=8, hkv=2, head_dim=128, page_size=16, dtype="bf16", rope_theta=5e5,
+             max_pages=512, max_seqs=4, max_slots=4096, seed=9)
+    t.gpu.set_restore_tensor_cores(tc)
+    for trial in range(3):
+        prog = _random_program(rng, int(rng.integers(300, 700)), 20)
+        n = sum(op[1] for op in prog if op[0] == "append")
+        missing = np.zeros(n, np.uint8)
+        b = int(rng.integers(0, n // 2))
+        missing[b:b + int(rng.integers(20, n // 2))] = 1          # an evicted stretch
+        missing[rng.random(n) < 0.1] = 1                          # and scattered pages
+        plan = Cache.plan_recovery(prog, n, missing)
+        assert plan == plan_recovery(prog, set(np.flatnonzero(missing).tolist()))[0]
+        assert 0 < len(plan) < n
+        t.restore_tokens(prog, 0, plan)
+    prog = _random_program(rng, 200, 10)
+    n = sum(op[1] for op in prog if op[0] == "append")
+    t.restore_tokens(prog, 1, [])
+    t.restore_tokens(prog, 1, list(range(n)))
 
 
 def test_restore_attention_figure10_program():

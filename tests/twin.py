@@ -282,6 +282,40 @@ class Twin:
         assert self.gpu.sync_errors() == 0
         return float(err.max()), float(err.mean())
 
+    def restore_tokens(self, program, layer, tokens):
+        """Restore attention of the tokens `tokens` only (GPU) vs the
+        oracle's replay of those tokens; the other rows must stay as they
+        were (NaN here).  Returns (max, mean) abs error."""
+        n = sum(op[1] for op in program if op[0] == "append")
+        tag = self.next_tag
+        self.next_tag += 1
+        w = self.width
+        q = synth.block(self.seed, tag, synth.KIND_Q, layer, 0, n * self.hq * self.d, w)
+        k = synth.block(self.seed, tag, synth.KIND_K, layer, 0, n * self.hkv * self.d, w)
+        v = synth.block(self.seed, tag, synth.KIND_V, layer, 0, n * self.hkv * self.d, w)
+        q = q.reshape(n, self.hq, self.d)
+        k = k.reshape(n, self.hkv, self.d)
+        v = v.reshape(n, self.hkv, self.d)
+        dev = lambda x: torch.from_numpy(x).to(self.tdtype).cuda().contiguous()
+        out = torch.full((n, self.hq, self.d), float("nan"), dtype=torch.float32, device="cuda")
+        self.gpu.restore_attention_tokens(program, layer, dev(q), dev(k), dev(v), list(tokens),
+                                          out=out)
+        got = out.double().cpu().numpy()
+        assert self.gpu.sync_errors() == 0
+        rest = np.ones(n, bool)
+        rest[list(tokens)] = False
+        assert np.isnan(got[rest]).all()
+        if not len(tokens):
+            return 0.0, 0.0
+        o = OracleCache(self.hq, self.hkv, self.d, self.orc.freq_theta, self.dtype, layers=(0,),
+                        page_size=self.S, rope_dim=self.orc.rope_dim)
+        want, _ = o.replay_attention(program, q[None][:, list(tokens)], k[None], v[None],
+                                     window=self.windows.get(layer, 0), only=list(tokens))
+        err = np.abs(got[list(tokens)] - want[0])
+        tmax, tmean = ATTN_TOL[self.dtype]
+        assert err.max() <= tmax and err.mean() <= tmean, (err.max(), err.mean())
+        return float(err.max()), float(err.mean())
+
     # -- comparison --------------------------------------------------------
     def check(self, g, kv=True):
         o = self.orc.seqs[self.o[g]]
