@@ -1201,6 +1201,33 @@ def restore_arm(args):
                      "traffic": None, "avg_call_ms": round(call_ms, 3)},
         "gpu_launches": int(launches),
     }
+    # recovery: the older half of the sequence lost its KV; the plan picks
+    # the missing tokens the end state reads and everything their
+    # recomputation reads, and restore attention runs over those only
+    missing = np.zeros(n, np.uint8)
+    missing[:n // 2] = 1
+    h0 = time.perf_counter()
+    plan = Cache.plan_recovery(prog, n, missing)
+    plan_ms = (time.perf_counter() - h0) * 1e3
+    for l in range(sh.layers):
+        cache.restore_attention_tokens(prog, l, q, k, v, plan, out=out)
+    torch.cuda.synchronize()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        r0.record(st)
+        for _ in range(args.steps):
+            for l in range(sh.layers):
+                cache.restore_attention_tokens(prog, l, q, k, v, plan, out=out)
+        r1.record(st)
+    torch.cuda.synchronize()
+    assert cache.sync_errors() == 0
+    line["recovery"] = {
+        "what": "the first half of the tokens missing; restore attention over the planned "
+                "tokens only (akv_restore_plan_recovery + akv_restore_attention_tokens), "
+                "all layers",
+        "missing": int(missing.sum()), "recomputed": len(plan), "plan_host_ms": round(plan_ms, 3),
+        "ms_per_step": round(r0.elapsed_time(r1) / args.steps, 3),
+        "full_restore_ms_per_step": round(ms, 3)}
     print(json.dumps(line), flush=True)
     cache.close()
 
