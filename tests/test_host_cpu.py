@@ -392,3 +392,28 @@ def test_shared_prefix_items_fit_one_wave(tensor_core_plans):
     abi.akv_seq_free(h, root)
     assert abi.akv_pool_stats(h)[1] == 0
     abi.akv_cache_destroy(h)
+
+
+def test_restore_token_list_checks(host_lib):
+    """akv_restore_attention_tokens checks its token list before any GPU
+    work: increasing and within the program's tokens; an empty list does
+    nothing (no launch)."""
+    c = HostCache(S=16)
+    prog = [("append", 5), ("drop", [(1, 2)]), ("repos",), ("append", 3)]
+    n = 8
+    buf = np.zeros(n * 4 * 64, np.float32)
+    p = buf.ctypes.data
+    n0 = host_lib.akv_fake_launches()
+    abi.akv_restore_attention_tokens(c.h, prog, 0, p, p, p, n, [], p)
+    assert host_lib.akv_fake_launches() == n0
+    for bad in ([3, 2], [1, 1], [-1], [n]):
+        with pytest.raises(abi.AkvError) as e:
+            abi.akv_restore_attention_tokens(c.h, prog, 0, p, p, p, n, bad, p)
+        assert e.value.code == abi.AKV_EINVAL
+    with pytest.raises(abi.AkvError) as e:        # the program appends 8 tokens, not 9
+        abi.akv_restore_attention_tokens(c.h, prog, 0, p, p, p, n + 1, [0], p)
+    assert e.value.code == abi.AKV_EINVAL
+    assert host_lib.akv_fake_launches() == n0
+    abi.akv_restore_attention_tokens(c.h, prog, 0, p, p, p, n, [0, 4, 7], p)
+    assert host_lib.akv_fake_launches() > n0
+    c.close()
