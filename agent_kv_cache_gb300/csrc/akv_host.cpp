@@ -1486,8 +1486,8 @@ int akv_decode_attention(akv_cache* c, int32_t layer, const void* q, const int64
       // quarters of the GPU idle with it.
       // Only where the quarter-wave split keeps too few tile copies in flight
       // to fill HBM on its own (its blocks x the ring's 8 stages of K and V
-      // tiles): the 120B-shaped call (184 blocks, D 64: ~6 MB) gains from a
-      // whole wave alone, the 8B-shaped one (228 blocks, D 128: ~15 MB)
+      // tiles): the 120B-shaped call (120 blocks, D 64: ~4 MB) gains from a
+      // whole wave alone, the 8B-shaped one (256 blocks, D 128: 16 MB)
       // loses to the extra splits' merges.
       const int64_t q_blocks = (int64_t)items.size() * c->cfg.hkv;
       const int64_t in_flight = q_blocks * 8 * 2 * 16 * (int64_t)c->cfg.head_dim * 2;
